@@ -1,0 +1,37 @@
+// Internal launchers shared by the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lin_state.h"
+
+namespace lin {
+
+inline int dtype_size(int dt) { return dt == LIN_BF16 ? 2 : 4; }
+
+// Slot copy family (copy_kernels.cu).
+cudaError_t launch_copy_slots(const lin_state_pool_t& pool, const int32_t* src,
+                              const int32_t* dst, int32_t n, int32_t layer_begin,
+                              int32_t layer_end, uint32_t flags, int32_t* status,
+                              cudaStream_t stream);
+cudaError_t launch_restore(const lin_state_pool_t& pool, const lin_cache_op_t* ops,
+                           int32_t n, int64_t* has_initial_state, int32_t* status,
+                           cudaStream_t stream);
+cudaError_t launch_spec_commit(const lin_state_pool_t& pool, const lin_commit_args_t& a,
+                               cudaStream_t stream);
+
+// Token-by-token kernels (token_kernels.cu).
+cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
+                          cudaStream_t stream);
+cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,
+                                     const lin_prefill_args_t& a, cudaStream_t stream);
+
+// Chunked tensor-core prefill (chunked_prefill.cu).
+bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_args_t& a);
+size_t chunked_prefill_workspace(const lin_state_pool_t& pool, const lin_prefill_args_t& a);
+cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
+                                   void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
+}  // namespace lin

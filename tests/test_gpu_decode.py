@@ -1,0 +1,187 @@
+"""Decode, speculative verify and commit on the GPU against the oracle."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_state_chunked_gb300 as L
+import workloads as W
+from oracle import lin_state_oracle as O
+from tests.helpers import TOL_BF16, TOL_F32, fill_pool, max_rel_per_head, np64, oracle_pool
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FLAGS = L.LIN_QK_L2NORM | L.LIN_CONV_SILU
+
+
+def _i32(v):
+    return torch.tensor(v, dtype=torch.int32, device=DEV)
+
+
+def _decode_both(pool, op, dims, conv_w, slots, pos, track, interval, gate, seed, step,
+                 out_dtype, n_draft=1, spec=None, ospec=None):
+    B = len(slots)
+    x, g, beta = W.make_decode_inputs(dims, B, n_draft, gate, dtype=conv_w.dtype, seed=seed,
+                                      step=step)
+    out = torch.zeros((B, n_draft, dims.num_heads, dims.head_v), dtype=out_dtype, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lin_state_decode(pool, layer=0, x=x.to(DEV), conv_w=conv_w.to(DEV), g=g.to(DEV),
+                       beta=beta.to(DEV), out=out, slot=_i32(slots), pos=_i32(pos),
+                       track_slot=_i32(track) if track is not None else None,
+                       track_interval=interval, spec=spec, gate_mode=gate, flags=FLAGS,
+                       status=st)
+    oo, ost = O.decode(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots, pos, track,
+                       interval, gate, FLAGS, 1.0, "bf16" if out_dtype == torch.bfloat16 else "f32",
+                       spec=ospec)
+    assert L.lin_state_read_status(st) == ost
+    return np64(out), oo
+
+
+@pytest.mark.parametrize("gate", [L.LIN_GATE_PER_HEAD, L.LIN_GATE_PER_KEY])
+@pytest.mark.parametrize("D", [16, 64])
+def test_decode_fp32_state_vs_oracle(gate, D):
+    dims = W.LayerDims(num_heads=3, head_k=D, head_v=D)
+    pool = L.StatePool(1, 20, 3, D, state_dtype=torch.float32, conv_dtype=torch.float32, device=DEV)
+    fill_pool(pool, 10, std=0.2)
+    op = oracle_pool(pool)
+    conv_w = W.randn((dims.conv_channels, 4), 0, "dec.w", std=0.5)
+    slots, track = [4, 9, 1, 17], [5, -1, 2, 3]
+    pos = [250, 10, 255, 511]
+    worst = 0.0
+    for step in range(8):
+        o, oo = _decode_both(pool, op, dims, conv_w, slots, pos, track, 256, gate, 10, step,
+                             torch.float32)
+        worst = max(worst, max_rel_per_head(o, oo, 2))
+        pos = [p + 1 for p in pos]
+    assert worst < TOL_F32
+    t = np64(pool.temporal[0])
+    for s in range(20):
+        assert max_rel_per_head(t[s], op["temporal"][0, s], 0) < TOL_F32
+    assert np.array_equal(np64(pool.conv), op["conv"])
+
+
+def test_decode_kda_bf16_crossing_track_boundary():
+    """KDA decode workload at reduced size: 16 requests x 300 steps, 12 heads,
+    bf16 state, interval 256 crossed by every request."""
+    dims = W.KIMI_K3_TP8
+    pool = L.StatePool(1, 64, 12, 128, state_dtype=torch.bfloat16, conv_dtype=torch.bfloat16,
+                       device=DEV)
+    fill_pool(pool, 11)
+    op = oracle_pool(pool)
+    conv_w = W.randn((dims.conv_channels, 4), 0, "kd.w", std=0.5).to(torch.bfloat16)
+    perm = W.randperm(64, 0, "kd.slots").tolist()
+    slots, track = perm[:16], perm[16:32]
+    pos = [1024 + 16 * i + (i % 5) for i in range(16)]  # all cross 1280 within 300 steps
+    worst = 0.0
+    for step in range(300):
+        o, oo = _decode_both(pool, op, dims, conv_w, slots, pos, track, 256, L.LIN_GATE_PER_KEY,
+                             11, step, torch.bfloat16)
+        worst = max(worst, max_rel_per_head(o, oo, 2))
+        pos = [p + 1 for p in pos]
+    assert worst < TOL_BF16, worst
+    t = np64(pool.temporal[0])
+    for s in slots + track:
+        assert max_rel_per_head(t[s], op["temporal"][0, s], 0) < TOL_BF16
+    assert np.array_equal(np64(pool.conv), op["conv"])
+
+
+def test_decode_track_positions_page_example():
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                       "decode_track_interval.json")))
+    dims = W.LayerDims(num_heads=1, head_k=16, head_v=16)
+    pool = L.StatePool(1, 4, 1, 16, device=DEV)
+    conv_w = W.randn((dims.conv_channels, 4), 0, "trk.w", std=0.5)
+    hits = []
+    pos = gold["prompt_len"]
+    for step in range(1, gold["decode_tokens_processed"][-1] + 5):
+        pool.temporal[0, 2].fill_(float("nan"))
+        x, g, b = W.make_decode_inputs(dims, 1, 1, L.LIN_GATE_PER_HEAD, torch.float32, 0,
+                                       tag="trk", step=step)
+        out = torch.zeros((1, 1, 1, 16), device=DEV)
+        L.lin_state_decode(pool, layer=0, x=x.to(DEV), conv_w=conv_w.to(DEV), g=g.to(DEV),
+                           beta=b.to(DEV), out=out, slot=_i32([1]), pos=_i32([pos]),
+                           track_slot=_i32([2]), track_interval=gold["interval"],
+                           gate_mode=L.LIN_GATE_PER_HEAD, flags=FLAGS)
+        if not torch.isnan(pool.temporal[0, 2]).any():
+            hits.append(step)
+            assert torch.equal(pool.temporal[0, 2], pool.temporal[0, 1])
+        pos += 1
+    assert hits == gold["decode_tokens_processed"]
+
+
+@pytest.mark.parametrize("sdt", [torch.float32, torch.bfloat16])
+def test_verify_commit_vs_oracle_and_linear_chain(sdt):
+    """MambaRadixCache page 8.4 / 9.4: after verify + commit(a) the slot equals a
+    single-token decodes, bit for bit on the GPU, and matches the oracle."""
+    dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
+    D = 4
+    B = 6
+    pool = L.StatePool(2, 24, 2, 128, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV)
+    fill_pool(pool, 12)
+    ref_pool = L.StatePool(2, 24, 2, 128, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV,
+                           temporal=pool.temporal.clone(), conv=pool.conv.clone())
+    op = oracle_pool(pool)
+    conv_w = W.randn((dims.conv_channels, 4), 0, "v.w", std=0.5).to(torch.bfloat16)
+    slots, track = [3, 7, 11, 15, 19, 21], [4, 8, 12, 16, -1, 22]
+    pos = [254, 100, 253, 255, 1, 600]
+    acc = [3, 4, 0, 1, 2, 4]
+    spec = L.SpecBuffer(pool, B, D)
+    ospec = O.make_spec_buffer(2, B, D, 2, 128, 128, dims.conv_channels)
+    for layer in range(2):
+        x, g, beta = W.make_decode_inputs(dims, B, D, L.LIN_GATE_PER_KEY, torch.bfloat16, 12,
+                                          tag=f"v{layer}")
+        out = torch.zeros((B, D, 2, 128), device=DEV)
+        L.lin_state_decode(pool, layer=layer, x=x.to(DEV), conv_w=conv_w.to(DEV), g=g.to(DEV),
+                           beta=beta.to(DEV), out=out, slot=_i32(slots), pos=_i32(pos), spec=spec,
+                           gate_mode=L.LIN_GATE_PER_KEY, flags=FLAGS)
+        oo, _ = O.decode(op, layer, np64(x), np64(conv_w), np64(g), np64(beta), slots, pos, None,
+                         0, O.GATE_PER_KEY, O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU, spec=ospec)
+        assert max_rel_per_head(np64(out), oo, 2) < (TOL_F32 if sdt == torch.float32 else TOL_BF16)
+        # the same tokens, one decode at a time, on a copy of the pool
+        for r in range(B):
+            for j in range(acc[r]):
+                o1 = torch.zeros((1, 1, 2, 128), device=DEV)
+                L.lin_state_decode(ref_pool, layer=layer, x=x[r:r + 1, j:j + 1].contiguous().to(DEV),
+                                   conv_w=conv_w.to(DEV), g=g[r:r + 1, j:j + 1].contiguous().to(DEV),
+                                   beta=beta[r:r + 1, j:j + 1].contiguous().to(DEV), out=o1,
+                                   slot=_i32([slots[r]]), pos=_i32([pos[r] + j]),
+                                   track_slot=_i32([track[r]]), track_interval=256,
+                                   gate_mode=L.LIN_GATE_PER_KEY, flags=FLAGS)
+                assert torch.equal(o1[0, 0], out[r, j])
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lin_state_spec_commit(pool, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
+                            n_draft=D, track_slot=_i32(track), track_interval=256, status=st)
+    assert L.lin_state_read_status(st) == 0
+    O.spec_commit(op, ospec, 0, 2, slots, pos, acc, track, 256, D)
+    assert torch.equal(pool.temporal, ref_pool.temporal)
+    assert torch.equal(pool.conv, ref_pool.conv)
+    tol = TOL_F32 if sdt == torch.float32 else TOL_BF16
+    t = np64(pool.temporal)
+    for layer in range(2):
+        for s in slots + [t_ for t_ in track if t_ >= 0]:
+            assert max_rel_per_head(t[layer, s], op["temporal"][layer, s], 0) < tol
+    assert np.array_equal(np64(pool.conv), op["conv"])
+    # accept_len out of range is reported and skipped
+    L.lin_state_spec_commit(pool, spec=spec, slot=_i32([3]), pos=_i32([0]), accept_len=_i32([5]),
+                            n_draft=D, status=st)
+    assert L.lin_state_read_status(st) == L.LIN_ST_BAD_ACCEPT
+
+
+def test_decode_status_bits():
+    dims = W.LayerDims(num_heads=1, head_k=32, head_v=32)
+    pool = L.StatePool(1, 8, 1, 32, device=DEV)
+    fill_pool(pool, 13)
+    before = pool.temporal.clone()
+    conv_w = W.randn((dims.conv_channels, 4), 0, "s.w")
+    x, g, b = W.make_decode_inputs(dims, 3, 1, L.LIN_GATE_PER_HEAD, torch.float32, 0, tag="s")
+    out = torch.zeros((3, 1, 1, 32), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lin_state_decode(pool, layer=0, x=x.to(DEV), conv_w=conv_w.to(DEV), g=g.to(DEV),
+                       beta=b.to(DEV), out=out, slot=_i32([8, 2, -1]), pos=_i32([0, 0, 0]),
+                       track_slot=_i32([1, 2, 3]), track_interval=256,
+                       gate_mode=L.LIN_GATE_PER_HEAD, flags=FLAGS, status=st)
+    assert L.lin_state_read_status(st) == L.LIN_ST_BAD_SLOT | L.LIN_ST_TRACK_ALIAS
+    assert torch.equal(pool.temporal, before)
