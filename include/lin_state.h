@@ -293,6 +293,15 @@ LIN_API int lin_state_read_status(int32_t* status, int32_t* value, void* stream)
 LIN_API const char* lin_state_strerror(int code);
 /* Text of the last host-side error on this thread ("" if none). */
 LIN_API const char* lin_state_last_error(void);
+/* Diagnostic: checks on the current device the tensor-core operand layouts
+ * the chunked prefill uses. Computes D[128][n] = A[128][k] * B[n][k]^T in one
+ * CTA with tcgen05.mma, operands rounded to fp16 (or bf16 with flags & 4) and
+ * staged in shared memory K-major, or MN-major for A (flags & 1) / B
+ * (flags & 2); fp32 accumulation. A, B, D: device fp32, row-major.
+ * n in {32, 64, 128}, k a multiple of 16 in [16, 128]. */
+LIN_API int lin_state_selftest_mma(const float* A, const float* B, float* D, int32_t n, int32_t k,
+                                   int32_t flags, int32_t* status, void* stream);
+
 /* ABI version: (major << 16) | minor. */
 LIN_API int lin_state_version(void);
 

@@ -33,7 +33,7 @@ EXPORTED = (
     "lin_state_prefill_kernel", "lin_state_prefill_workspace", "lin_state_prefill", "lin_state_decode",
     "lin_state_spec_commit", "lin_state_copy_slots", "lin_state_restore",
     "lin_state_slot_bytes", "lin_state_read_status", "lin_state_strerror",
-    "lin_state_last_error", "lin_state_version",
+    "lin_state_last_error", "lin_state_version", "lin_state_selftest_mma",
 )
 
 _c_i32p = ctypes.c_void_p
@@ -137,6 +137,9 @@ def _load():
     lib.lin_state_last_error.restype = ctypes.c_char_p
     lib.lin_state_version.argtypes = []
     lib.lin_state_version.restype = ctypes.c_int
+    lib.lin_state_selftest_mma.argtypes = [vp, vp, vp, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_int32, vp, vp]
+    lib.lin_state_selftest_mma.restype = ctypes.c_int
     return lib
 
 
@@ -361,6 +364,14 @@ def lin_state_read_status(status: torch.Tensor, stream=None) -> int:
     _check(lib.lin_state_read_status(_ptr(status), ctypes.byref(v), _stream(stream)),
            "lin_state_read_status")
     return v.value
+
+
+def lin_state_selftest_mma(A, B, D, a_mn=False, b_mn=False, bf16=False, status=None,
+                           stream=None) -> None:
+    """D[128][n] = A[128][k] B[n][k]^T on the tensor cores (layout self-test)."""
+    flags = (1 if a_mn else 0) | (2 if b_mn else 0) | (4 if bf16 else 0)
+    _check(lib.lin_state_selftest_mma(_ptr(A), _ptr(B), _ptr(D), B.shape[0], A.shape[1], flags,
+                                      _ptr(status), _stream(stream)), "lin_state_selftest_mma")
 
 
 def lin_state_version() -> int:

@@ -101,6 +101,17 @@ extern "C" {
 
 int lin_state_version(void) { return (1 << 16) | 0; }
 
+int lin_state_selftest_mma(const float* A, const float* B, float* D, int32_t n, int32_t k,
+                           int32_t flags, int32_t* status, void* stream) {
+  if (!A || !B || !D) return fail(LIN_EINVAL, "selftest: NULL matrix");
+  if ((n != 32 && n != 64 && n != 128) || k < 16 || k > 128 || (k % 16))
+    return fail(LIN_EINVAL, "selftest: n in {32,64,128}, k a multiple of 16 up to 128");
+  cudaError_t e = lin::launch_mma_selftest(A, B, D, n, k, flags & 7, status,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lin_state_selftest_mma launch");
+  return ok();
+}
+
 const char* lin_state_strerror(int code) {
   switch (code) {
     case LIN_OK: return "ok";

@@ -34,4 +34,8 @@ cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefi
                                    void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
 
+// Tensor-core layout self-test (selftest.cu).
+cudaError_t launch_mma_selftest(const float* A, const float* B, float* D, int N, int K, int flags,
+                                int32_t* status, cudaStream_t stream);
+
 }  // namespace lin
