@@ -1,14 +1,817 @@
-// Chunked tensor-core prefill (tcgen05 / TMEM / TMA, sm_103a).
+// Chunked tensor-core prefill of the gated delta rule (sm_103a: tcgen05 MMAs
+// with fp32 accumulators in tensor memory, TMA-staged inputs).
+//
+// The recurrence is the KDA / GDN update of the Kimi-K3 notes
+// ("企业官网建设流程全解析", "Speculative decoding"):
+//     S_t = S_{t-1} Diag(alpha_t) + d_t k_t^T,  d_t = beta_t (v_t - S_{t-1} Diag(alpha_t) k_t),
+//     o_t = S_t q_t.
+// The pages fix 64-token chunks aligned to absolute positions (Ping-Pong
+// page, parameters: FLA_CHUNK_SIZE = 64) but give no chunked algorithm; the
+// form below follows from the update by algebra. Inside a chunk starting from
+// state S0, with b_t = sum_{s<=t} log alpha_s (per key channel) and
+// gamma_t = exp(b_t):
+//     A[t][i] = beta_t sum_c k_tc k_ic exp(b_tc - b_ic)   (i < t)
+//     T       = (I + A)^-1 Diag(beta)
+//     W       = T (gamma . K),   U' = T V,   U = U' - W S0^T
+//     P[t][i] = sum_c q_tc k_ic exp(b_tc - b_ic)          (i <= t)
+//     O       = (gamma . Q) S0^T + P U
+//     S_end   = S0 Diag(gamma_last) + U^T ((gamma_last / gamma) . K)
+// Every product runs with V (= 128) as the MMA M dimension, so the state row v
+// is TMEM lane v and all MMAs are M = 128 (cta_group::1):
+//     MMA1  [A';P'] = [K_l;Q_l] K_r^T            N = 64,  K = 128
+//     MMA2  W^T = Khat^T T^T,  U'^T = V^T T^T     N = 64,  K = 64
+//     MMA3  U^T = U'^T + S0 (-W)^T                N = 64,  K = 128
+//     MMA4  O^T = S0 Qhat^T + U^T P^T             N = 64,  K = 128 + 64
+//     MMA5  S   = S0 Diag(gamma_last) + U^T Ktil  N = 128, K = 64
+// (KDA: K_l = k exp(b - b_ref), Q_l = q exp(b - b_ref), K_r = k exp(b_ref - b)
+// with b_ref the chunk's middle row, so no exponent leaves +-(half a chunk);
+// GDN: the scalar decay exp(b_t - b_i) is applied in fp32 to A' and P'.)
+// The state is carried in fp32 in tensor memory across chunks and written
+// (rounded to the pool dtype) at every snapshot boundary and at the end.
+// Operands are fp16 for GDN (10-bit mantissa; every decay-scaled factor stays
+// in [0, 1]) and bf16 for KDA (the per-channel decay ratios exceed fp16 range).
+//
+// One CTA (8 warps) runs one (request, head) sequentially over its chunks.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "umma.cuh"
 
 namespace lin {
+namespace {
 
-bool chunked_prefill_supported(const lin_state_pool_t&, const lin_prefill_args_t&) { return false; }
+constexpr int CH = 64;       // chunk length
+constexpr int DH = 128;      // head dim (K = V)
+constexpr int NT = 256;      // threads
+constexpr int XR = CH + 3;   // rows of a staged x tile (3 halo rows)
+constexpr uint32_t kWaitTries = 1u << 26;
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t OFF_SOP = 0;                 // S0 operand, rows v, 128 x 128 16-bit
+constexpr uint32_t OFF_KQ = 32768;              // [K_l; Q_l], 128 rows x 128
+constexpr uint32_t OFF_AX = OFF_KQ;             //   alias: fp32 A / X [64][65]
+constexpr uint32_t OFF_XD = OFF_KQ + 16640;     //   alias: fp32 diagonal inverses [4][16][16]
+constexpr uint32_t OFF_YB = OFF_XD + 4096;      //   alias: fp32 block temporaries [3][16][16]
+constexpr uint32_t OFF_KR = 65536;              // K_r (KDA), 64 x 128
+constexpr uint32_t OFF_TT = OFF_KR;             //   alias: T, 64 x 64
+constexpr uint32_t OFF_PP = OFF_KR + 8192;      //   alias: P, 64 x 64
+constexpr uint32_t OFF_KH = 81920;              // gamma . K, rows i (MN-major A)
+constexpr uint32_t OFF_WW = OFF_KH;             //   alias: -W, rows c (MN-major B)
+constexpr uint32_t OFF_VV = 98304;              // V, rows i (MN-major A)
+constexpr uint32_t OFF_UT = OFF_VV;             //   alias: U^T, rows v (K-major A)
+constexpr uint32_t OFF_QH = 114688;             // gamma . Q, rows t (K-major B)
+constexpr uint32_t OFF_KT = 131072;             // (gamma_last/gamma) . K, rows i (MN-major B)
+constexpr uint32_t OFF_XT = 147456;             // x tile, bf16 [3][67][128]
+constexpr uint32_t OFF_WC = OFF_XT + 52224;     // conv taps, fp32 [384][4]
+constexpr uint32_t OFF_HALO = OFF_WC + 6144;    // initial conv window, fp32 [3][384]
+constexpr uint32_t OFF_WEND = OFF_HALO + 4608;  // window at the chunk end, fp32 [3][384]
+constexpr uint32_t OFF_WTOT = OFF_WEND + 4608;  // per-warp gate sums, fp32 [8][128]
+constexpr uint32_t OFF_SBETA = OFF_WTOT + 4096; // beta_t, fp32 [64]
+constexpr uint32_t OFF_SB = OFF_SBETA + 256;    // GDN b_t, fp32 [64]
+constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
+constexpr uint32_t SMEM_USED = OFF_GLAST + 512;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_YB + 3 * 1024 <= OFF_KR, "solve scratch inside the KQ region");
+
+// Tensor-memory columns (256 allocated).
+constexpr uint32_t COL_S = 0;    // state, fp32, lanes v
+constexpr uint32_t COL_R1 = 128; // [A';P'] -> U'^T -> U^T
+constexpr uint32_t COL_R2 = 192; // W^T -> O^T
+constexpr uint32_t TMEM_COLS = 256;
+
+constexpr uint32_t XT_BYTES = 3 * XR * DH * 2;
+
+struct ChunkParams {
+  lin_state_pool_t pool;
+  lin_prefill_args_t a;
+};
+
+__device__ __forceinline__ int head_channel(int cl, int h, int H) {
+  const int part = cl >> 7, c = cl & 127;
+  return part * H * DH + h * DH + c;
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// 4 consecutive 16-bit values (cols c..c+3, c % 4 == 0) of row r of a row-panel buffer.
+template <bool BF>
+__device__ __forceinline__ void put4(uint32_t buf, int R, int r, int c, float a, float b, float cc,
+                                     float d) {
+  st_shared_v2(buf + umma::rp_offset(r, c, R), umma::pack2<BF>(a, b), umma::pack2<BF>(cc, d));
+}
+// 32 consecutive values (cols c0..c0+31) of row r.
+template <bool BF>
+__device__ __forceinline__ void put32(uint32_t buf, int R, int r, int c0, const float (&v)[32],
+                                      float scale) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m)
+    st_shared_v4(buf + umma::rp_offset(r, c0 + 8 * m, R),
+                 umma::pack2<BF>(scale * v[8 * m + 0], scale * v[8 * m + 1]),
+                 umma::pack2<BF>(scale * v[8 * m + 2], scale * v[8 * m + 3]),
+                 umma::pack2<BF>(scale * v[8 * m + 4], scale * v[8 * m + 5]),
+                 umma::pack2<BF>(scale * v[8 * m + 6], scale * v[8 * m + 7]));
+}
+
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane0, uint32_t col) {
+  return base + (static_cast<uint32_t>(lane0) << 16) + col;
+}
+
+// Stage x rows [row0 - 3, row0 + 64) of the head's q | k | v channel blocks.
+__device__ __forceinline__ void issue_x_tile(const CUtensorMap* tmap, uint32_t dst, int64_t row0,
+                                             int h, int H, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(umma::smem_u32(bar)),
+               "r"(XT_BYTES)
+               : "memory");
+  const int y = static_cast<int>(row0) - 3;
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const int x = part * H * DH + h * DH;
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst + part * XR * DH * 2),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(umma::smem_u32(bar))
+        : "memory");
+  }
+}
+
+// Gate inputs of one chunk for this thread: KDA log-decay for 8 tokens x 4
+// key channels, or the per-head scalar; beta for the 8 tokens.
+template <bool KDA>
+__device__ __forceinline__ void load_gates(const lin_prefill_args_t& a, int64_t row0, int n, int h,
+                                           int H, int warp, int lane, float (&gk)[8][4],
+                                           float (&bt)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = warp * 8 + i;
+    const bool ok = t < n;
+    const int64_t tok = row0 + t;
+    if (KDA) {
+      float4 v = ok ? *reinterpret_cast<const float4*>(a.g + (tok * H + h) * DH + lane * 4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      gk[i][0] = v.x; gk[i][1] = v.y; gk[i][2] = v.z; gk[i][3] = v.w;
+    } else {
+      gk[i][0] = ok ? a.g[tok * H + h] : 0.f;
+      gk[i][1] = gk[i][2] = gk[i][3] = 0.f;
+    }
+    bt[i] = ok ? a.beta[tok * H + h] : 0.f;
+  }
+}
+
+template <int ST>
+__device__ __forceinline__ void store_row32(char* base, int v, int c0, const float (&x)[32]) {
+  if (ST == LIN_BF16) {
+    uint16_t* p = reinterpret_cast<uint16_t*>(base) + v * DH + c0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = static_cast<uint32_t>(f32_to_bf16_bits(x[8 * m + 2 * q])) |
+               (static_cast<uint32_t>(f32_to_bf16_bits(x[8 * m + 2 * q + 1])) << 16);
+      *reinterpret_cast<uint4*>(p + 8 * m) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    float* p = reinterpret_cast<float*>(base) + v * DH + c0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      *reinterpret_cast<float4*>(p + 4 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+  }
+}
+
+template <bool KDA, int ST>
+__global__ void __launch_bounds__(NT, 1)
+    chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const ChunkParams p) {
+  constexpr bool BF = KDA;  // operand type
+  extern __shared__ uint8_t dsm[];
+  __shared__ uint64_t bar_mma, bar_x;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const lin_state_pool_t& pool = p.pool;
+  const lin_prefill_args_t& a = p.a;
+  const int H = pool.num_heads;
+  const int r = blockIdx.x / H, h = blockIdx.x % H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int vrow = quarter * 32 + lane;  // TMEM lane owned in the epilogues
+  const bool rep = (h == 0 && tid == 0);
+
+  // ---- request checks (uniform over the CTA) ----
+  const int slot = a.slot[r];
+  if (slot < 0) return;
+  if (slot >= pool.num_slots) {
+    if (rep) report(a.status, LIN_ST_BAD_SLOT);
+    return;
+  }
+  const int64_t bos = a.cu_seqlens[r], eos = a.cu_seqlens[r + 1];
+  if (bos < 0 || eos < bos || eos > a.total_tokens) {
+    if (rep) report(a.status, LIN_ST_BAD_SEQLEN);
+    return;
+  }
+  const int P = a.prefix_len[r];
+  if (P < 0 || (P & 63)) {
+    if (rep) report(a.status, LIN_ST_BAD_PREFIX);
+    return;
+  }
+  int t0 = 0, ntr = 0;
+  if (a.track_stride > 0 && a.cu_track) {
+    t0 = a.cu_track[r];
+    ntr = a.cu_track[r + 1] - t0;
+    for (int i = 0; i < ntr; ++i) {
+      const int t = a.track_slots[t0 + i];
+      if (t >= pool.num_slots) {
+        if (rep) report(a.status, LIN_ST_BAD_SLOT);
+        return;
+      }
+      if (t == slot) {
+        if (rep) report(a.status, LIN_ST_TRACK_ALIAS);
+        return;
+      }
+    }
+  }
+  const bool warm = a.has_initial_state[r] != 0;
+  const int L = static_cast<int>(eos - bos);
+  const int nch = (L + CH - 1) / CH;
+  constexpr int ES = ST == LIN_BF16 ? 2 : 4;
+  const int64_t head_bytes = int64_t(DH) * DH * ES;
+  char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                 slot * pool.temporal_slot_stride + h * head_bytes;
+  char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                 slot * pool.conv_slot_stride;
+
+  const uint32_t raw = umma::smem_u32(dsm);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* sm = dsm + (sb - raw);
+  float* WC = reinterpret_cast<float*>(sm + OFF_WC);
+  float* HALO = reinterpret_cast<float*>(sm + OFF_HALO);
+  float* WEND = reinterpret_cast<float*>(sm + OFF_WEND);
+  float* WTOT = reinterpret_cast<float*>(sm + OFF_WTOT);
+  float* SBETA = reinterpret_cast<float*>(sm + OFF_SBETA);
+  float* SB = reinterpret_cast<float*>(sm + OFF_SB);
+  float* GLAST = reinterpret_cast<float*>(sm + OFF_GLAST);
+  float* AX = reinterpret_cast<float*>(sm + OFF_AX);
+  float* XD = reinterpret_cast<float*>(sm + OFF_XD);
+  float* YB = reinterpret_cast<float*>(sm + OFF_YB);
+  const __nv_bfloat16* XT = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_XT);
+
+  for (int i = tid; i < 384 * 4; i += NT)
+    WC[i] = load_elem(a.conv_w, int64_t(head_channel(i >> 2, h, H)) * 4 + (i & 3), a.io_dtype);
+  for (int i = tid; i < 3 * 384; i += NT) {
+    const int rr = i / 384, cl = i % 384;
+    HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
+  }
+
+  if (nch == 0) {
+    // No tokens: the slot keeps its state; a cold start leaves zeros in it.
+    if (!warm) {
+      for (int i = tid; i < DH * DH; i += NT) store_elem(slot_t, i, ST, 0.f);
+      for (int i = tid; i < 3 * 384; i += NT)
+        store_elem(slot_c, int64_t(head_channel(i / 3, h, H)) * 3 + (i % 3), pool.conv_dtype, 0.f);
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    umma::mbar_init(&bar_mma, 1);
+    umma::mbar_init(&bar_x, 1);
+    umma::mbar_fence_init();
+    abort_sh = 0;
+  }
+  if (warp == 0) umma::tmem_alloc(&tmem_base_sh, TMEM_COLS);
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tm = tmem_base_sh;
+  bool x_inflight = false;  // thread 0 only
+  if (tid == 0) {
+    issue_x_tile(&tmap_x, sb + OFF_XT, bos, h, H, &bar_x);
+    x_inflight = true;
+  }
+
+  // ---- initial state: fp32 into TMEM, 16-bit operand copy into shared memory
+  {
+    float s[32];
+    for (int cc = half * 64; cc < half * 64 + 64; cc += 32) {
+      if (warm) {
+        if (ST == LIN_BF16) {
+          const uint16_t* src = reinterpret_cast<const uint16_t*>(slot_t) + vrow * DH + cc;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint4 u = *reinterpret_cast<const uint4*>(src + 8 * m);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              s[8 * m + 2 * q] = __uint_as_float(w[q] << 16);
+              s[8 * m + 2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+            }
+          }
+        } else {
+          const float* src = reinterpret_cast<const float*>(slot_t) + vrow * DH + cc;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            float4 u = *reinterpret_cast<const float4*>(src + 4 * m);
+            s[4 * m] = u.x; s[4 * m + 1] = u.y; s[4 * m + 2] = u.z; s[4 * m + 3] = u.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < 32; ++m) s[m] = 0.f;
+      }
+      umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), s);
+      put32<BF>(sb + OFF_SOP, 128, vrow, cc, s, 1.f);
+    }
+  }
+  umma::fence_smem_to_async();
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+
+  float gk[8][4], bt[8];
+  load_gates<KDA>(a, bos, L < CH ? L : CH, h, H, warp, lane, gk, bt);
+
+  uint32_t ph_mma = 0, ph_x = 0;
+  int snap = 0;
+  const bool silu_on = a.flags & LIN_CONV_SILU;
+  const bool l2_on = a.flags & LIN_QK_L2NORM;
+
+  // Waits for the MMAs committed so far (thread 0 polls, everyone syncs).
+  auto wait_mma = [&]() -> bool {
+    if (tid == 0) {
+      if (!umma::mbar_wait(&bar_mma, ph_mma, kWaitTries)) {
+        abort_sh = 1;
+        report(a.status, LIN_ST_TIMEOUT);
+      }
+    }
+    ph_mma ^= 1;
+    __syncthreads();
+    umma::fence_after_sync();
+    return abort_sh == 0;
+  };
+
+  for (int j = 0; j < nch; ++j) {
+    const int n = (L - j * CH) < CH ? (L - j * CH) : CH;
+    const int64_t row0 = bos + int64_t(j) * CH;
+
+    // ---- x tile of this chunk
+    if (tid == 0) {
+      if (!umma::mbar_wait(&bar_x, ph_x, kWaitTries)) {
+        abort_sh = 1;
+        report(a.status, LIN_ST_TIMEOUT);
+      } else {
+        x_inflight = false;
+      }
+    }
+    ph_x ^= 1;
+    __syncthreads();
+    if (abort_sh) break;
+
+    // ---- gates: in-chunk inclusive sums b_t (rows past n carry log-decay 0)
+    float cs[8][4];
+    {
+      float run[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          run[e] += gk[i][e];
+          cs[i][e] = run[e];
+        }
+      if (KDA) {
+        *reinterpret_cast<float4*>(WTOT + warp * DH + lane * 4) = make_float4(run[0], run[1], run[2], run[3]);
+      } else if (lane == 0) {
+        WTOT[warp] = run[0];
+      }
+    }
+    __syncthreads();
+    float bref[4], blast[4];
+    {
+      float pre[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        bref[e] = 0.f;
+        blast[e] = 0.f;
+      }
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float tw = KDA ? WTOT[w * DH + lane * 4 + e] : WTOT[w];
+          if (w < warp) pre[e] += tw;
+          if (w < 4) bref[e] += tw;
+          blast[e] += tw;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cs[i][e] += pre[e];
+      if (warp == 0) {
+        if (KDA) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) GLAST[lane * 4 + e] = expf(blast[e]);
+        } else if (lane == 0) {
+          GLAST[0] = expf(blast[0]);
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          SBETA[warp * 8 + i] = bt[i];
+          SB[warp * 8 + i] = cs[i][0];
+        }
+      }
+    }
+
+    // ---- conv, activation, q/k normalisation, operand rows
+    {
+      auto xval = [&](int rr, int part, int c) -> float {
+        if (j == 0 && rr < 3) return HALO[rr * 384 + part * 128 + c];
+        return __bfloat162float(XT[(part * XR + rr) * DH + c]);
+      };
+      const int tfirst = warp * 8;
+      float win[3][4][3];
+#pragma unroll
+      for (int part = 0; part < 3; ++part)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int m = 0; m < 3; ++m) win[part][e][m] = xval(tfirst + m, part, lane * 4 + e);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int t = tfirst + i;
+        float y[3][4];
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cl = part * 128 + lane * 4 + e;
+            const float xin = xval(t + 3, part, lane * 4 + e);
+            const float4 w = *reinterpret_cast<const float4*>(WC + cl * 4);
+            float yy = w.x * win[part][e][0] + w.y * win[part][e][1] + w.z * win[part][e][2] + w.w * xin;
+            win[part][e][0] = win[part][e][1];
+            win[part][e][1] = win[part][e][2];
+            win[part][e][2] = xin;
+            y[part][e] = silu_on ? silu(yy) : yy;
+          }
+        }
+        float sq = y[0][0] * y[0][0] + y[0][1] * y[0][1] + y[0][2] * y[0][2] + y[0][3] * y[0][3];
+        float sk = y[1][0] * y[1][0] + y[1][1] * y[1][1] + y[1][2] * y[1][2] + y[1][3] * y[1][3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        }
+        const float rq = (l2_on ? rsqrtf(sq + 1e-6f) : 1.f) * a.q_scale;
+        const float rk = l2_on ? rsqrtf(sk + 1e-6f) : 1.f;
+        const bool ok = t < n;
+        float kn[4], qn[4], vv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kn[e] = ok ? y[1][e] * rk : 0.f;
+          qn[e] = ok ? y[0][e] * rq : 0.f;
+          vv[e] = ok ? y[2][e] : 0.f;
+        }
+        float eL[4], eR[4], eH[4], eT[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ee = KDA ? e : 0;
+          const float b = cs[i][ee];
+          eH[e] = expf(b);
+          eT[e] = expf(blast[ee] - b);
+          eL[e] = KDA ? expf(b - bref[ee]) : 1.f;
+          eR[e] = KDA ? expf(bref[ee] - b) : 1.f;
+        }
+        const int c = lane * 4;
+        put4<BF>(sb + OFF_KQ, 128, t, c, kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3]);
+        put4<BF>(sb + OFF_KQ, 128, CH + t, c, qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3]);
+        if (KDA)
+          put4<BF>(sb + OFF_KR, 64, t, c, kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3]);
+        put4<BF>(sb + OFF_KH, 64, t, c, kn[0] * eH[0], kn[1] * eH[1], kn[2] * eH[2], kn[3] * eH[3]);
+        put4<BF>(sb + OFF_VV, 64, t, c, vv[0], vv[1], vv[2], vv[3]);
+        put4<BF>(sb + OFF_QH, 64, t, c, qn[0] * eH[0], qn[1] * eH[1], qn[2] * eH[2], qn[3] * eH[3]);
+        put4<BF>(sb + OFF_KT, 64, t, c, kn[0] * eT[0], kn[1] * eT[1], kn[2] * eT[2], kn[3] * eT[3]);
+      }
+      // conv window after the chunk's last token: chunk rows n-3 .. n-1
+      for (int idx = tid; idx < 3 * 384; idx += NT) {
+        const int m = idx / 384, cl = idx % 384;
+        WEND[idx] = xval(n + m, cl >> 7, cl & 127);
+      }
+    }
+    umma::fence_smem_to_async();
+    __syncthreads();
+
+    // ---- MMA1: [A'; P'] = [K_l; Q_l] K_r^T; prefetch the next x tile
+    if (tid == 0) {
+      if (j + 1 < nch) {
+        issue_x_tile(&tmap_x, sb + OFF_XT, row0 + CH, h, H, &bar_x);
+        x_inflight = true;
+      }
+      umma::fence_after_sync();
+      constexpr uint32_t id1 = umma::idesc_f16(128, 64, BF, false, false);
+      const uint32_t kr = KDA ? sb + OFF_KR : sb + OFF_KQ;
+      const int kr_rows = KDA ? 64 : 128;
+#pragma unroll
+      for (int k0 = 0; k0 < DH; k0 += 16)
+        umma::mma_f16(tm + COL_R1, umma::desc_kmajor(sb + OFF_KQ, 128, k0),
+                      umma::desc_kmajor(kr, kr_rows, k0), id1, k0 > 0);
+      umma::mma_commit(&bar_mma);
+    }
+    if (j + 1 < nch) {
+      const int n2 = (L - (j + 1) * CH) < CH ? (L - (j + 1) * CH) : CH;
+      load_gates<KDA>(a, row0 + CH, n2, h, H, warp, lane, gk, bt);
+    }
+    if (!wait_mma()) break;
+
+    // ---- A (fp32, for the solve) and P (operand) from [A'; P']
+    {
+      float v[32];
+      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R1 + half * 32), v);
+      if (quarter < 2) {
+        const int t = vrow;
+        const float bet = SBETA[t];
+        const float bt_ = SB[t];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int i = half * 32 + k;
+          const float dec = KDA ? 1.f : expf(bt_ - SB[i < t ? i : t]);
+          AX[t * 65 + i] = (i < t) ? bet * v[k] * dec : 0.f;
+        }
+      } else {
+        const int t = vrow - 64;
+        const float bt_ = SB[t];
+        float pv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int i = half * 32 + k;
+          const float dec = KDA ? 1.f : expf(bt_ - SB[i <= t ? i : t]);
+          pv[k] = (i <= t) ? v[k] * dec : 0.f;
+        }
+        put32<BF>(sb + OFF_PP, 64, t, half * 32, pv, 1.f);
+      }
+    }
+    __syncthreads();
+
+    // ---- T = (I + A)^-1 Diag(beta), blocked over 16 x 16 tiles
+    if (tid < 64) {
+      // inverses of the four unit lower-triangular diagonal blocks, one column per thread
+      const int blk = tid >> 4, jj = tid & 15, base = blk * 16;
+      float x[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < t; ++i) s += AX[(base + t) * 65 + base + i] * x[i];
+        x[t] = t < jj ? 0.f : (t == jj ? 1.f : -s);
+      }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) XD[blk * 256 + t * 16 + jj] = x[t];
+    }
+    __syncthreads();
+    for (int ab = 1; ab < 4; ++ab) {
+      // Y(ab, b) = sum_{c=b}^{ab-1} A(ab, c) X(c, b)
+      for (int item = tid; item < ab * 256; item += NT) {
+        const int b = item >> 8, t = (item >> 4) & 15, jj = item & 15;
+        float s = 0.f;
+        for (int c = b; c < ab; ++c) {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const float av = AX[(ab * 16 + t) * 65 + c * 16 + m];
+            const float xv = (c == b) ? XD[c * 256 + m * 16 + jj] : AX[(c * 16 + m) * 65 + b * 16 + jj];
+            s += av * xv;
+          }
+        }
+        YB[b * 256 + t * 16 + jj] = s;
+      }
+      __syncthreads();
+      // X(ab, b) = -X(ab, ab) Y(ab, b)
+      for (int item = tid; item < ab * 256; item += NT) {
+        const int b = item >> 8, t = (item >> 4) & 15, jj = item & 15;
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) s += XD[ab * 256 + t * 16 + m] * YB[b * 256 + m * 16 + jj];
+        AX[(ab * 16 + t) * 65 + b * 16 + jj] = -s;
+      }
+      __syncthreads();
+    }
+    {
+      const int t = tid >> 2, c0 = (tid & 3) * 16;
+      float tv[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const int i = c0 + m;
+        float xv;
+        if ((i >> 4) == (t >> 4))
+          xv = XD[(t >> 4) * 256 + (t & 15) * 16 + (i & 15)];
+        else
+          xv = AX[t * 65 + i];  // zero above the diagonal blocks
+        tv[m] = xv * SBETA[i];
+      }
+      st_shared_v4(sb + OFF_TT + umma::rp_offset(t, c0, 64), umma::pack2<BF>(tv[0], tv[1]),
+                   umma::pack2<BF>(tv[2], tv[3]), umma::pack2<BF>(tv[4], tv[5]),
+                   umma::pack2<BF>(tv[6], tv[7]));
+      st_shared_v4(sb + OFF_TT + umma::rp_offset(t, c0 + 8, 64), umma::pack2<BF>(tv[8], tv[9]),
+                   umma::pack2<BF>(tv[10], tv[11]), umma::pack2<BF>(tv[12], tv[13]),
+                   umma::pack2<BF>(tv[14], tv[15]));
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+
+    // ---- MMA2: W^T = Khat^T T^T (R2), U'^T = V^T T^T (R1)
+    if (tid == 0) {
+      umma::fence_after_sync();
+      constexpr uint32_t id2 = umma::idesc_f16(128, 64, BF, true, false);
+#pragma unroll
+      for (int k0 = 0; k0 < CH; k0 += 16) {
+        const uint64_t bd = umma::desc_kmajor(sb + OFF_TT, 64, k0);
+        umma::mma_f16(tm + COL_R2, umma::desc_mnmajor(sb + OFF_KH, 64, k0), bd, id2, k0 > 0);
+        umma::mma_f16(tm + COL_R1, umma::desc_mnmajor(sb + OFF_VV, 64, k0), bd, id2, k0 > 0);
+      }
+      umma::mma_commit(&bar_mma);
+    }
+    if (!wait_mma()) break;
+
+    // ---- -W into shared memory (rows c); S0 <- S0 Diag(gamma_last) in TMEM
+    {
+      float v[32];
+      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R2 + half * 32), v);
+      put32<BF>(sb + OFF_WW, 128, vrow, half * 32, v, -1.f);
+#pragma unroll 1
+      for (int cc = half * 64; cc < half * 64 + 64; cc += 32) {
+        umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] *= GLAST[KDA ? cc + k : 0];
+        umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
+      }
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+
+    // ---- MMA3: U^T = U'^T + S0 (-W)^T (R1);  MMA4a: O^T = S0 Qhat^T (R2)
+    if (tid == 0) {
+      umma::fence_after_sync();
+      constexpr uint32_t id3 = umma::idesc_f16(128, 64, BF, false, true);
+      constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
+#pragma unroll
+      for (int k0 = 0; k0 < DH; k0 += 16) {
+        const uint64_t ad = umma::desc_kmajor(sb + OFF_SOP, 128, k0);
+        umma::mma_f16(tm + COL_R1, ad, umma::desc_mnmajor(sb + OFF_WW, 128, k0), id3, 1);
+        umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
+      }
+      umma::mma_commit(&bar_mma);
+    }
+    if (!wait_mma()) break;
+
+    // ---- U^T into shared memory (rows v)
+    {
+      float v[32];
+      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R1 + half * 32), v);
+      put32<BF>(sb + OFF_UT, 128, vrow, half * 32, v, 1.f);
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+
+    // ---- MMA4b: O^T += U^T P^T (R2);  MMA5: S += U^T Ktil (S)
+    if (tid == 0) {
+      umma::fence_after_sync();
+      constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
+      constexpr uint32_t id5 = umma::idesc_f16(128, 128, BF, false, true);
+#pragma unroll
+      for (int k0 = 0; k0 < CH; k0 += 16) {
+        const uint64_t ad = umma::desc_kmajor(sb + OFF_UT, 128, k0);
+        umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_PP, 64, k0), id4, 1);
+        umma::mma_f16(tm + COL_S, ad, umma::desc_mnmajor(sb + OFF_KT, 64, k0), id5, 1);
+      }
+      umma::mma_commit(&bar_mma);
+    }
+    if (!wait_mma()) break;
+
+    // ---- outputs, state operand for the next chunk, snapshots, final state
+    {
+      float v[32];
+      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R2 + half * 32), v);
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const int t = half * 32 + k;
+        if (t < n) store_elem(a.out, ((row0 + t) * H + h) * DH + vrow, a.out_dtype, v[k]);
+      }
+      const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
+      int snap_dst = -1;
+      if (ntr > 0 && n == CH && (end_pos % a.track_stride) == 0) {
+        snap_dst = a.track_slots[t0 + (snap % ntr)];
+        ++snap;
+      }
+      const bool last = (j == nch - 1);
+      char* snap_t = snap_dst >= 0 ? static_cast<char*>(pool.temporal) +
+                                         a.layer * pool.temporal_layer_stride +
+                                         snap_dst * pool.temporal_slot_stride + h * head_bytes
+                                   : nullptr;
+#pragma unroll 1
+      for (int cc = half * 64; cc < half * 64 + 64; cc += 32) {
+        umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
+        put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
+        if (snap_t) store_row32<ST>(snap_t, vrow, cc, v);
+        if (last) store_row32<ST>(slot_t, vrow, cc, v);
+      }
+      if (snap_dst >= 0 || last) {
+        char* snap_c = snap_dst >= 0 ? static_cast<char*>(pool.conv) +
+                                           a.layer * pool.conv_layer_stride +
+                                           snap_dst * pool.conv_slot_stride
+                                     : nullptr;
+        for (int idx = tid; idx < 3 * 384; idx += NT) {
+          const int cl = idx / 3, m = idx % 3;
+          const int64_t off = int64_t(head_channel(cl, h, H)) * 3 + m;
+          const float wv = WEND[m * 384 + cl];
+          if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
+          if (last) store_elem(slot_c, off, pool.conv_dtype, wv);
+        }
+      }
+    }
+    umma::fence_smem_to_async();
+    umma::fence_before_sync();
+    __syncthreads();
+  }
+
+  // ---- teardown: no copy may still target shared memory when the CTA exits
+  if (tid == 0 && x_inflight) {
+    if (!umma::mbar_wait(&bar_x, ph_x, kWaitTries)) report(a.status, LIN_ST_TIMEOUT);
+  }
+  __syncthreads();
+  umma::fence_after_sync();
+  if (warp == 0) umma::tmem_dealloc(tm, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <bool KDA, int ST>
+cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, cudaStream_t s) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pool.conv_channels),
+                              static_cast<cuuint64_t>(a.total_tokens)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pool.conv_channels) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(DH), static_cast<cuuint32_t>(XR)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.x), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  auto kern = chunked_prefill_kernel<KDA, ST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  ChunkParams p{pool, a};
+  const unsigned grid = static_cast<unsigned>(a.batch) * static_cast<unsigned>(pool.num_heads);
+  kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
+  return pool.head_k == DH && pool.head_v == DH && a.io_dtype == LIN_BF16 && a.total_tokens > 0 &&
+         int64_t(a.batch) * pool.num_heads < (int64_t(1) << 31) &&
+         (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(a.g) & 15) == 0 && encode_fn() != nullptr;
+}
+
 size_t chunked_prefill_workspace(const lin_state_pool_t&, const lin_prefill_args_t&) { return 0; }
-cudaError_t launch_prefill_chunked(const lin_state_pool_t&, const lin_prefill_args_t&, void*, size_t,
-                                   cudaStream_t) {
-  return cudaErrorNotSupported;
+
+cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a, void*,
+                                   size_t, cudaStream_t stream) {
+  const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
+  const bool bf = pool.state_dtype == LIN_BF16;
+  if (kda) return bf ? launch_t<true, LIN_BF16>(pool, a, stream) : launch_t<true, LIN_F32>(pool, a, stream);
+  return bf ? launch_t<false, LIN_BF16>(pool, a, stream) : launch_t<false, LIN_F32>(pool, a, stream);
 }
 
 }  // namespace lin

@@ -163,8 +163,17 @@ def test_long_request_placement_page_example(path):
         assert d <= tol * pool.temporal[0, s].abs().max().item() + (0 if path == "chunked" else 1e-6)
 
 
+def tol_for(path, gate_mode, state_dtype):
+    """The chunked kernel runs KDA products with bf16 operands (the per-channel
+    decay ratios overflow fp16), so KDA is held to the bf16 bar there."""
+    if state_dtype == torch.bfloat16 or (path == "chunked" and gate_mode == W.GATE_PER_KEY):
+        return TOL_BF16
+    return TOL_F32
+
+
+@pytest.mark.parametrize("gate", [W.GATE_PER_HEAD, W.GATE_PER_KEY])
 @pytest.mark.parametrize("path", list(PATHS))
-def test_edge_cases(path):
+def test_edge_cases(path, gate):
     """Empty and very short requests, a padding slot, a misaligned prefix, a
     track slot equal to the live slot, a bad slot id: the bad ones are
     reported and skipped, the rest complete."""
@@ -172,7 +181,7 @@ def test_edge_cases(path):
     lengths = [0, 1, 2, 65, 64, 5, 9, 70]
     prefixes = [0, 64, 0, 0, 32, 0, 0, 128]
     warm = [1, 1, 0, 1, 1, 0, 0, 1]
-    b = W.make_prefill_batch(dims, lengths, W.GATE_PER_KEY, dtype=torch.bfloat16, seed=0,
+    b = W.make_prefill_batch(dims, lengths, gate, dtype=torch.bfloat16, seed=0,
                              prefixes=prefixes, warm=warm, tag="edge")
     pool = L.StatePool(1, 16, 2, 128, state_dtype=torch.float32, conv_dtype=torch.bfloat16,
                        device=DEV)
@@ -185,8 +194,9 @@ def test_edge_cases(path):
     out, oo = run_both(pool, op, b, slots, tracks, cu_track, 64, path, expect_status=expect)
     ok_reqs = [0, 1, 2, 7]
     skip = [r for r in range(len(lengths)) if r not in ok_reqs]
-    compare_outputs(out, oo, b.cu_seqlens.tolist(), TOL_F32, skip=skip)
-    compare_slots(pool, op, list(range(16)), TOL_F32)
+    tol = tol_for(path, gate, torch.float32)
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), tol, skip=skip)
+    compare_slots(pool, op, list(range(16)), tol)
     o = np64(out)
     for r in skip:
         a, e = int(b.cu_seqlens[r]), int(b.cu_seqlens[r + 1])
