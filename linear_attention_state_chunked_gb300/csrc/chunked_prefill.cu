@@ -31,7 +31,7 @@
 // Operands are fp16 for GDN (10-bit mantissa; every decay-scaled factor stays
 // in [0, 1]) and bf16 for KDA (the per-channel decay ratios exceed fp16 range).
 //
-// One CTA (8 warps) runs one (request, head) sequentially over its chunks.
+// One CTA (16 warps) runs one (request, head) sequentially over its chunks.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -45,37 +45,42 @@ namespace {
 
 constexpr int CH = 64;       // chunk length
 constexpr int DH = 128;      // head dim (K = V)
-constexpr int NT = 256;      // threads
+constexpr int NT = 512;      // threads (16 warps)
+constexpr int NW = NT / 32;
+constexpr int TPW = CH / NW; // tokens per warp in the conv phase
 constexpr int XR = CH + 3;   // rows of a staged x tile (3 halo rows)
 constexpr uint32_t kWaitTries = 1u << 26;
 
-// Shared-memory map (offsets from a 1024-byte aligned base).
+// Shared-memory map (offsets from a 1024-byte aligned base). Regions are
+// reused once their previous contents have been consumed by an MMA.
 constexpr uint32_t OFF_SOP = 0;                 // S0 operand, rows v, 128 x 128 16-bit
-constexpr uint32_t OFF_KQ = 32768;              // [K_l; Q_l], 128 rows x 128
-constexpr uint32_t OFF_AX = OFF_KQ;             //   alias: fp32 A / X [64][65]
-constexpr uint32_t OFF_XD = OFF_KQ + 16640;     //   alias: fp32 diagonal inverses [4][16][16]
-constexpr uint32_t OFF_YB = OFF_XD + 4096;      //   alias: fp32 block temporaries [3][16][16]
-constexpr uint32_t OFF_KR = 65536;              // K_r (KDA), 64 x 128
-constexpr uint32_t OFF_TT = OFF_KR;             //   alias: T, 64 x 64
-constexpr uint32_t OFF_PP = OFF_KR + 8192;      //   alias: P, 64 x 64
-constexpr uint32_t OFF_KH = 81920;              // gamma . K, rows i (MN-major A)
-constexpr uint32_t OFF_WW = OFF_KH;             //   alias: -W, rows c (MN-major B)
-constexpr uint32_t OFF_VV = 98304;              // V, rows i (MN-major A)
-constexpr uint32_t OFF_UT = OFF_VV;             //   alias: U^T, rows v (K-major A)
-constexpr uint32_t OFF_QH = 114688;             // gamma . Q, rows t (K-major B)
-constexpr uint32_t OFF_KT = 131072;             // (gamma_last/gamma) . K, rows i (MN-major B)
-constexpr uint32_t OFF_XT = 147456;             // x tile, bf16 [3][67][128]
-constexpr uint32_t OFF_WC = OFF_XT + 52224;     // conv taps, fp32 [384][4]
+constexpr uint32_t OFF_KQ = 32768;              // [K_l; Q_l] (high part), 128 rows x 128
+constexpr uint32_t OFF_TT = OFF_KQ;             //   after MMA1: T (high), 64 x 64
+constexpr uint32_t OFF_TTL = OFF_KQ + 8192;     //   after MMA1: T (low part, GDN)
+constexpr uint32_t OFF_PP = OFF_KQ + 16384;     //   after MMA1: P (high), 64 x 64
+constexpr uint32_t OFF_PPL = OFF_KQ + 24576;    //   after MMA1: P (low part, GDN)
+constexpr uint32_t OFF_KQL = 65536;             // [K; Q] low part (GDN), 128 rows x 128
+constexpr uint32_t OFF_AX = OFF_KQL;            //   after MMA1: fp32 A / X [64][65]
+constexpr uint32_t OFF_XD = OFF_KQL + 16640;    //   after MMA1: fp32 diagonal inverses [4][16][16]
+constexpr uint32_t OFF_YB = OFF_XD + 4096;      //   after MMA1: fp32 block temporaries [3][16][16]
+constexpr uint32_t OFF_KR = 98304;              // K_r (KDA), 64 x 128
+constexpr uint32_t OFF_UTL = OFF_KR;            //   after MMA2: U^T low part (GDN), rows v
+constexpr uint32_t OFF_KH = 114688;             // gamma . K, rows i (MN-major A)
+constexpr uint32_t OFF_WW = OFF_KH;             //   after MMA2: -W, rows c (MN-major B)
+constexpr uint32_t OFF_VV = 131072;             // V, rows i (MN-major A)
+constexpr uint32_t OFF_UT = OFF_VV;             //   after MMA2: U^T (high), rows v (K-major A)
+constexpr uint32_t OFF_QH = 147456;             // gamma . Q, rows t (K-major B)
+constexpr uint32_t OFF_KT = 163840;             // (gamma_last/gamma) . K, rows i (MN-major B)
+constexpr uint32_t OFF_WC = 180224;             // conv taps, fp32 [4][384] (tap-major)
 constexpr uint32_t OFF_HALO = OFF_WC + 6144;    // initial conv window, fp32 [3][384]
-constexpr uint32_t OFF_WEND = OFF_HALO + 4608;  // window at the chunk end, fp32 [3][384]
-constexpr uint32_t OFF_WTOT = OFF_WEND + 4608;  // per-warp gate sums, fp32 [8][128]
-constexpr uint32_t OFF_SBETA = OFF_WTOT + 4096; // beta_t, fp32 [64]
+constexpr uint32_t OFF_WTOT = OFF_HALO + 4608;  // per-warp gate sums, fp32 [16][128]
+constexpr uint32_t OFF_SBETA = OFF_WTOT + 8192; // beta_t, fp32 [64]
 constexpr uint32_t OFF_SB = OFF_SBETA + 256;    // GDN b_t, fp32 [64]
 constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
 constexpr uint32_t SMEM_USED = OFF_GLAST + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_YB + 3 * 1024 <= OFF_KR, "solve scratch inside the KQ region");
+static_assert(OFF_YB + 3 * 1024 <= OFF_KR, "solve scratch inside the low-part region");
 
 // Tensor-memory columns (256 allocated).
 constexpr uint32_t COL_S = 0;    // state, fp32, lanes v
@@ -83,7 +88,6 @@ constexpr uint32_t COL_R1 = 128; // [A';P'] -> U'^T -> U^T
 constexpr uint32_t COL_R2 = 192; // W^T -> O^T
 constexpr uint32_t TMEM_COLS = 256;
 
-constexpr uint32_t XT_BYTES = 3 * XR * DH * 2;
 
 struct ChunkParams {
   lin_state_pool_t pool;
@@ -124,37 +128,58 @@ __device__ __forceinline__ void put32(uint32_t buf, int R, int r, int c0, const 
                  umma::pack2<BF>(scale * v[8 * m + 6], scale * v[8 * m + 7]));
 }
 
+// 16 consecutive values (cols c0..c0+15) of row r.
+template <bool BF>
+__device__ __forceinline__ void put16(uint32_t buf, int R, int r, int c0, const float (&v)[16],
+                                      float scale) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+    st_shared_v4(buf + umma::rp_offset(r, c0 + 8 * m, R),
+                 umma::pack2<BF>(scale * v[8 * m + 0], scale * v[8 * m + 1]),
+                 umma::pack2<BF>(scale * v[8 * m + 2], scale * v[8 * m + 3]),
+                 umma::pack2<BF>(scale * v[8 * m + 4], scale * v[8 * m + 5]),
+                 umma::pack2<BF>(scale * v[8 * m + 6], scale * v[8 * m + 7]));
+}
+
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane0, uint32_t col) {
   return base + (static_cast<uint32_t>(lane0) << 16) + col;
 }
 
-// Stage x rows [row0 - 3, row0 + 64) of the head's q | k | v channel blocks.
-__device__ __forceinline__ void issue_x_tile(const CUtensorMap* tmap, uint32_t dst, int64_t row0,
-                                             int h, int H, uint64_t* bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(umma::smem_u32(bar)),
-               "r"(XT_BYTES)
-               : "memory");
+// Prefetch x rows [row0 - 3, row0 + 64) of the head's q | k | v channel blocks
+// into L2 (tensor-map prefetch; the conv phase then reads them from L2).
+__device__ __forceinline__ void prefetch_x_tile(const CUtensorMap* tmap, int64_t row0, int h, int H) {
   const int y = static_cast<int>(row0) - 3;
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
     const int x = part * H * DH + h * DH;
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst + part * XR * DH * 2),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(umma::smem_u32(bar))
-        : "memory");
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
   }
 }
 
-// Gate inputs of one chunk for this thread: KDA log-decay for 8 tokens x 4
-// key channels, or the per-head scalar; beta for the 8 tokens.
+// hi / lo fp16 split of four values: hi = fp16(x), lo = fp16(x - hi).
+__device__ __forceinline__ void split4(float a, float b, float c, float d, uint32_t (&hi)[2],
+                                       uint32_t (&lo)[2]) {
+  const __half2 h0 = __floats2half2_rn(a, b), h1 = __floats2half2_rn(c, d);
+  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+  const __half2 l0 = __floats2half2_rn(a - f0.x, b - f0.y), l1 = __floats2half2_rn(c - f1.x, d - f1.y);
+  hi[0] = *reinterpret_cast<const uint32_t*>(&h0);
+  hi[1] = *reinterpret_cast<const uint32_t*>(&h1);
+  lo[0] = *reinterpret_cast<const uint32_t*>(&l0);
+  lo[1] = *reinterpret_cast<const uint32_t*>(&l1);
+}
+
+// Gate inputs of one chunk for this thread: KDA log-decay for TPW tokens x 4
+// key channels, or the per-head scalar; beta for the TPW tokens.
 template <bool KDA>
 __device__ __forceinline__ void load_gates(const lin_prefill_args_t& a, int64_t row0, int n, int h,
-                                           int H, int warp, int lane, float (&gk)[8][4],
-                                           float (&bt)[8]) {
+                                           int H, int warp, int lane, float (&gk)[TPW][4],
+                                           float (&bt)[TPW]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = warp * 8 + i;
+  for (int i = 0; i < TPW; ++i) {
+    const int t = warp * TPW + i;
     const bool ok = t < n;
     const int64_t tok = row0 + t;
     if (KDA) {
@@ -190,12 +215,30 @@ __device__ __forceinline__ void store_row32(char* base, int v, int c0, const flo
   }
 }
 
+// 16 values (cols c0..c0+15) of row r as fp16 high parts into `hi` and low
+// parts into `lo`.
+__device__ __forceinline__ void put16_split(uint32_t hi_buf, uint32_t lo_buf, int R, int r, int c0,
+                                            const float (&v)[16], float scale) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    uint32_t h0[2], l0[2], h1[2], l1[2];
+    split4(scale * v[8 * m + 0], scale * v[8 * m + 1], scale * v[8 * m + 2], scale * v[8 * m + 3], h0, l0);
+    split4(scale * v[8 * m + 4], scale * v[8 * m + 5], scale * v[8 * m + 6], scale * v[8 * m + 7], h1, l1);
+    const uint32_t off = umma::rp_offset(r, c0 + 8 * m, R);
+    st_shared_v4(hi_buf + off, h0[0], h0[1], h1[0], h1[1]);
+    st_shared_v4(lo_buf + off, l0[0], l0[1], l1[0], l1[1]);
+  }
+}
+
 template <bool KDA, int ST>
 __global__ void __launch_bounds__(NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const ChunkParams p) {
-  constexpr bool BF = KDA;  // operand type
+  // GDN: fp16 operands with high / low splits on the products that set the
+  // error (see the header); KDA: bf16 operands, single products.
+  constexpr bool BF = KDA;
+  constexpr bool SPLIT = !KDA;
   extern __shared__ uint8_t dsm[];
-  __shared__ uint64_t bar_mma, bar_x;
+  __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -204,8 +247,8 @@ __global__ void __launch_bounds__(NT, 1)
   const int H = pool.num_heads;
   const int r = blockIdx.x / H, h = blockIdx.x % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int vrow = quarter * 32 + lane;  // TMEM lane owned in the epilogues
+  const int quarter = warp & 3, slice = warp >> 2;  // four warps share each lane quarter
+  const int vrow = quarter * 32 + lane;             // TMEM lane owned in the epilogues
   const bool rep = (h == 0 && tid == 0);
 
   // ---- request checks (uniform over the CTA) ----
@@ -250,13 +293,14 @@ __global__ void __launch_bounds__(NT, 1)
                  slot * pool.temporal_slot_stride + h * head_bytes;
   char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                  slot * pool.conv_slot_stride;
+  const int C_all = pool.conv_channels;
+  const uint16_t* xg = static_cast<const uint16_t*>(a.x);
 
   const uint32_t raw = umma::smem_u32(dsm);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sm = dsm + (sb - raw);
   float* WC = reinterpret_cast<float*>(sm + OFF_WC);
   float* HALO = reinterpret_cast<float*>(sm + OFF_HALO);
-  float* WEND = reinterpret_cast<float*>(sm + OFF_WEND);
   float* WTOT = reinterpret_cast<float*>(sm + OFF_WTOT);
   float* SBETA = reinterpret_cast<float*>(sm + OFF_SBETA);
   float* SB = reinterpret_cast<float*>(sm + OFF_SB);
@@ -264,10 +308,11 @@ __global__ void __launch_bounds__(NT, 1)
   float* AX = reinterpret_cast<float*>(sm + OFF_AX);
   float* XD = reinterpret_cast<float*>(sm + OFF_XD);
   float* YB = reinterpret_cast<float*>(sm + OFF_YB);
-  const __nv_bfloat16* XT = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_XT);
 
+  if (tid == 0) prefetch_x_tile(&tmap_x, bos, h, H);
   for (int i = tid; i < 384 * 4; i += NT)
-    WC[i] = load_elem(a.conv_w, int64_t(head_channel(i >> 2, h, H)) * 4 + (i & 3), a.io_dtype);
+    WC[(i & 3) * 384 + (i >> 2)] =
+        load_elem(a.conv_w, int64_t(head_channel(i >> 2, h, H)) * 4 + (i & 3), a.io_dtype);
   for (int i = tid; i < 3 * 384; i += NT) {
     const int rr = i / 384, cl = i % 384;
     HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
@@ -285,7 +330,6 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (tid == 0) {
     umma::mbar_init(&bar_mma, 1);
-    umma::mbar_init(&bar_x, 1);
     umma::mbar_fence_init();
     abort_sh = 0;
   }
@@ -294,54 +338,48 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tm = tmem_base_sh;
-  bool x_inflight = false;  // thread 0 only
-  if (tid == 0) {
-    issue_x_tile(&tmap_x, sb + OFF_XT, bos, h, H, &bar_x);
-    x_inflight = true;
-  }
 
   // ---- initial state: fp32 into TMEM, 16-bit operand copy into shared memory
   {
     float s[32];
-    for (int cc = half * 64; cc < half * 64 + 64; cc += 32) {
-      if (warm) {
-        if (ST == LIN_BF16) {
-          const uint16_t* src = reinterpret_cast<const uint16_t*>(slot_t) + vrow * DH + cc;
+    const int cc = slice * 32;
+    if (warm) {
+      if (ST == LIN_BF16) {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(slot_t) + vrow * DH + cc;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            uint4 u = *reinterpret_cast<const uint4*>(src + 8 * m);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int m = 0; m < 4; ++m) {
+          uint4 u = *reinterpret_cast<const uint4*>(src + 8 * m);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              s[8 * m + 2 * q] = __uint_as_float(w[q] << 16);
-              s[8 * m + 2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
-            }
-          }
-        } else {
-          const float* src = reinterpret_cast<const float*>(slot_t) + vrow * DH + cc;
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            float4 u = *reinterpret_cast<const float4*>(src + 4 * m);
-            s[4 * m] = u.x; s[4 * m + 1] = u.y; s[4 * m + 2] = u.z; s[4 * m + 3] = u.w;
+          for (int q = 0; q < 4; ++q) {
+            s[8 * m + 2 * q] = __uint_as_float(w[q] << 16);
+            s[8 * m + 2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
           }
         }
       } else {
+        const float* src = reinterpret_cast<const float*>(slot_t) + vrow * DH + cc;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) s[m] = 0.f;
+        for (int m = 0; m < 8; ++m) {
+          float4 u = *reinterpret_cast<const float4*>(src + 4 * m);
+          s[4 * m] = u.x; s[4 * m + 1] = u.y; s[4 * m + 2] = u.z; s[4 * m + 3] = u.w;
+        }
       }
-      umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), s);
-      put32<BF>(sb + OFF_SOP, 128, vrow, cc, s, 1.f);
+    } else {
+#pragma unroll
+      for (int m = 0; m < 32; ++m) s[m] = 0.f;
     }
+    umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), s);
+    put32<BF>(sb + OFF_SOP, 128, vrow, cc, s, 1.f);
   }
   umma::fence_smem_to_async();
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
 
-  float gk[8][4], bt[8];
+  float gk[TPW][4], bt[TPW];
   load_gates<KDA>(a, bos, L < CH ? L : CH, h, H, warp, lane, gk, bt);
 
-  uint32_t ph_mma = 0, ph_x = 0;
+  uint32_t ph_mma = 0;
   int snap = 0;
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2_on = a.flags & LIN_QK_L2NORM;
@@ -364,25 +402,27 @@ __global__ void __launch_bounds__(NT, 1)
     const int n = (L - j * CH) < CH ? (L - j * CH) : CH;
     const int64_t row0 = bos + int64_t(j) * CH;
 
-    // ---- x tile of this chunk
-    if (tid == 0) {
-      if (!umma::mbar_wait(&bar_x, ph_x, kWaitTries)) {
-        abort_sh = 1;
-        report(a.status, LIN_ST_TIMEOUT);
-      } else {
-        x_inflight = false;
-      }
+    // ---- x rows of this warp's tokens (and the 3 before them), straight from
+    // global memory (L2, prefetched): 8 bytes = 4 channels per lane and part.
+    const int tfirst = warp * TPW;
+    uint2 xr[TPW + 3][3];
+#pragma unroll
+    for (int m = 0; m < TPW + 3; ++m) {
+      const int rel = tfirst - 3 + m;  // row relative to the chunk start
+      const bool from_x = (rel < n) && (j > 0 || rel >= 0);
+#pragma unroll
+      for (int part = 0; part < 3; ++part)
+        xr[m][part] = from_x ? *reinterpret_cast<const uint2*>(
+                                   xg + (row0 + rel) * C_all + part * H * DH + h * DH + lane * 4)
+                             : make_uint2(0u, 0u);
     }
-    ph_x ^= 1;
-    __syncthreads();
-    if (abort_sh) break;
 
     // ---- gates: in-chunk inclusive sums b_t (rows past n carry log-decay 0)
-    float cs[8][4];
+    float cs[TPW][4];
     {
       float run[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < TPW; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           run[e] += gk[i][e];
@@ -404,65 +444,63 @@ __global__ void __launch_bounds__(NT, 1)
         blast[e] = 0.f;
       }
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
+      for (int w = 0; w < NW; ++w) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float tw = KDA ? WTOT[w * DH + lane * 4 + e] : WTOT[w];
           if (w < warp) pre[e] += tw;
-          if (w < 4) bref[e] += tw;
+          if (w < NW / 2) bref[e] += tw;
           blast[e] += tw;
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < TPW; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) cs[i][e] += pre[e];
       if (warp == 0) {
         if (KDA) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) GLAST[lane * 4 + e] = expf(blast[e]);
+          for (int e = 0; e < 4; ++e) GLAST[lane * 4 + e] = __expf(blast[e]);
         } else if (lane == 0) {
-          GLAST[0] = expf(blast[0]);
+          GLAST[0] = __expf(blast[0]);
         }
       }
       if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          SBETA[warp * 8 + i] = bt[i];
-          SB[warp * 8 + i] = cs[i][0];
+        for (int i = 0; i < TPW; ++i) {
+          SBETA[warp * TPW + i] = bt[i];
+          SB[warp * TPW + i] = cs[i][0];
         }
       }
     }
 
     // ---- conv, activation, q/k normalisation, operand rows
     {
-      auto xval = [&](int rr, int part, int c) -> float {
-        if (j == 0 && rr < 3) return HALO[rr * 384 + part * 128 + c];
-        return __bfloat162float(XT[(part * XR + rr) * DH + c]);
+      // x value of window row m (chunk row tfirst - 3 + m), part, channel lane*4+e
+      auto xv = [&](int m, int part, int e) -> float {
+        const int rel = tfirst - 3 + m;
+        if (j == 0 && rel < 0) return HALO[(rel + 3) * 384 + part * 128 + lane * 4 + e];
+        const uint32_t w = (e < 2) ? xr[m][part].x : xr[m][part].y;
+        return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
       };
-      const int tfirst = warp * 8;
-      float win[3][4][3];
 #pragma unroll
-      for (int part = 0; part < 3; ++part)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int m = 0; m < 3; ++m) win[part][e][m] = xval(tfirst + m, part, lane * 4 + e);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < TPW; ++i) {
         const int t = tfirst + i;
         float y[3][4];
 #pragma unroll
         for (int part = 0; part < 3; ++part) {
+          float4 w4[4];
+#pragma unroll
+          for (int tap = 0; tap < 4; ++tap)
+            w4[tap] = *reinterpret_cast<const float4*>(WC + tap * 384 + part * 128 + lane * 4);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cl = part * 128 + lane * 4 + e;
-            const float xin = xval(t + 3, part, lane * 4 + e);
-            const float4 w = *reinterpret_cast<const float4*>(WC + cl * 4);
-            float yy = w.x * win[part][e][0] + w.y * win[part][e][1] + w.z * win[part][e][2] + w.w * xin;
-            win[part][e][0] = win[part][e][1];
-            win[part][e][1] = win[part][e][2];
-            win[part][e][2] = xin;
+            const float w0 = e == 0 ? w4[0].x : e == 1 ? w4[0].y : e == 2 ? w4[0].z : w4[0].w;
+            const float w1 = e == 0 ? w4[1].x : e == 1 ? w4[1].y : e == 2 ? w4[1].z : w4[1].w;
+            const float w2 = e == 0 ? w4[2].x : e == 1 ? w4[2].y : e == 2 ? w4[2].z : w4[2].w;
+            const float w3 = e == 0 ? w4[3].x : e == 1 ? w4[3].y : e == 2 ? w4[3].z : w4[3].w;
+            const float yy = w0 * xv(i, part, e) + w1 * xv(i + 1, part, e) + w2 * xv(i + 2, part, e) +
+                             w3 * xv(i + 3, part, e);
             y[part][e] = silu_on ? silu(yy) : yy;
           }
         }
@@ -488,44 +526,51 @@ __global__ void __launch_bounds__(NT, 1)
         for (int e = 0; e < 4; ++e) {
           const int ee = KDA ? e : 0;
           const float b = cs[i][ee];
-          eH[e] = expf(b);
-          eT[e] = expf(blast[ee] - b);
-          eL[e] = KDA ? expf(b - bref[ee]) : 1.f;
-          eR[e] = KDA ? expf(bref[ee] - b) : 1.f;
+          eH[e] = __expf(b);
+          eT[e] = __expf(blast[ee] - b);
+          eL[e] = KDA ? __expf(b - bref[ee]) : 1.f;
+          eR[e] = KDA ? __expf(bref[ee] - b) : 1.f;
         }
         const int c = lane * 4;
-        put4<BF>(sb + OFF_KQ, 128, t, c, kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3]);
-        put4<BF>(sb + OFF_KQ, 128, CH + t, c, qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3]);
-        if (KDA)
+        if (SPLIT) {
+          uint32_t hi[2], lo[2];
+          split4(kn[0], kn[1], kn[2], kn[3], hi, lo);
+          st_shared_v2(sb + OFF_KQ + umma::rp_offset(t, c, 128), hi[0], hi[1]);
+          st_shared_v2(sb + OFF_KQL + umma::rp_offset(t, c, 128), lo[0], lo[1]);
+          split4(qn[0], qn[1], qn[2], qn[3], hi, lo);
+          st_shared_v2(sb + OFF_KQ + umma::rp_offset(CH + t, c, 128), hi[0], hi[1]);
+          st_shared_v2(sb + OFF_KQL + umma::rp_offset(CH + t, c, 128), lo[0], lo[1]);
+        } else {
+          put4<BF>(sb + OFF_KQ, 128, t, c, kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3]);
+          put4<BF>(sb + OFF_KQ, 128, CH + t, c, qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3]);
           put4<BF>(sb + OFF_KR, 64, t, c, kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3]);
+        }
         put4<BF>(sb + OFF_KH, 64, t, c, kn[0] * eH[0], kn[1] * eH[1], kn[2] * eH[2], kn[3] * eH[3]);
         put4<BF>(sb + OFF_VV, 64, t, c, vv[0], vv[1], vv[2], vv[3]);
         put4<BF>(sb + OFF_QH, 64, t, c, qn[0] * eH[0], qn[1] * eH[1], qn[2] * eH[2], qn[3] * eH[3]);
         put4<BF>(sb + OFF_KT, 64, t, c, kn[0] * eT[0], kn[1] * eT[1], kn[2] * eT[2], kn[3] * eT[3]);
       }
-      // conv window after the chunk's last token: chunk rows n-3 .. n-1
-      for (int idx = tid; idx < 3 * 384; idx += NT) {
-        const int m = idx / 384, cl = idx % 384;
-        WEND[idx] = xval(n + m, cl >> 7, cl & 127);
-      }
     }
     umma::fence_smem_to_async();
     __syncthreads();
 
-    // ---- MMA1: [A'; P'] = [K_l; Q_l] K_r^T; prefetch the next x tile
+    // ---- MMA1: [A'; P'] = [K_l; Q_l] K_r^T; prefetch the next chunk's x rows
     if (tid == 0) {
-      if (j + 1 < nch) {
-        issue_x_tile(&tmap_x, sb + OFF_XT, row0 + CH, h, H, &bar_x);
-        x_inflight = true;
-      }
+      if (j + 1 < nch) prefetch_x_tile(&tmap_x, row0 + CH, h, H);
       umma::fence_after_sync();
       constexpr uint32_t id1 = umma::idesc_f16(128, 64, BF, false, false);
-      const uint32_t kr = KDA ? sb + OFF_KR : sb + OFF_KQ;
-      const int kr_rows = KDA ? 64 : 128;
 #pragma unroll
-      for (int k0 = 0; k0 < DH; k0 += 16)
-        umma::mma_f16(tm + COL_R1, umma::desc_kmajor(sb + OFF_KQ, 128, k0),
-                      umma::desc_kmajor(kr, kr_rows, k0), id1, k0 > 0);
+      for (int k0 = 0; k0 < DH; k0 += 16) {
+        const uint64_t ah = umma::desc_kmajor(sb + OFF_KQ, 128, k0);
+        if (SPLIT) {
+          const uint64_t al = umma::desc_kmajor(sb + OFF_KQL, 128, k0);
+          umma::mma_f16(tm + COL_R1, ah, ah, id1, k0 > 0);  // B: rows 0..63 of the same panels
+          umma::mma_f16(tm + COL_R1, ah, al, id1, 1);
+          umma::mma_f16(tm + COL_R1, al, ah, id1, 1);
+        } else {
+          umma::mma_f16(tm + COL_R1, ah, umma::desc_kmajor(sb + OFF_KR, 64, k0), id1, k0 > 0);
+        }
+      }
       umma::mma_commit(&bar_mma);
     }
     if (j + 1 < nch) {
@@ -536,29 +581,32 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- A (fp32, for the solve) and P (operand) from [A'; P']
     {
-      float v[32];
-      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R1 + half * 32), v);
+      float v[16];
+      umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R1 + slice * 16), v);
       if (quarter < 2) {
         const int t = vrow;
         const float bet = SBETA[t];
         const float bt_ = SB[t];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int i = half * 32 + k;
-          const float dec = KDA ? 1.f : expf(bt_ - SB[i < t ? i : t]);
+        for (int k = 0; k < 16; ++k) {
+          const int i = slice * 16 + k;
+          const float dec = KDA ? 1.f : __expf(bt_ - SB[i < t ? i : t]);
           AX[t * 65 + i] = (i < t) ? bet * v[k] * dec : 0.f;
         }
       } else {
         const int t = vrow - 64;
         const float bt_ = SB[t];
-        float pv[32];
+        float pv[16];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int i = half * 32 + k;
-          const float dec = KDA ? 1.f : expf(bt_ - SB[i <= t ? i : t]);
+        for (int k = 0; k < 16; ++k) {
+          const int i = slice * 16 + k;
+          const float dec = KDA ? 1.f : __expf(bt_ - SB[i <= t ? i : t]);
           pv[k] = (i <= t) ? v[k] * dec : 0.f;
         }
-        put32<BF>(sb + OFF_PP, 64, t, half * 32, pv, 1.f);
+        if (SPLIT)
+          put16_split(sb + OFF_PP, sb + OFF_PPL, 64, t, slice * 16, pv, 1.f);
+        else
+          put16<BF>(sb + OFF_PP, 64, t, slice * 16, pv, 1.f);
       }
     }
     __syncthreads();
@@ -606,24 +654,29 @@ __global__ void __launch_bounds__(NT, 1)
       __syncthreads();
     }
     {
-      const int t = tid >> 2, c0 = (tid & 3) * 16;
-      float tv[16];
+      const int t = tid >> 3, c0 = (tid & 7) * 8;
+      float tv[8];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
+      for (int m = 0; m < 8; ++m) {
         const int i = c0 + m;
-        float xv;
+        float xvv;
         if ((i >> 4) == (t >> 4))
-          xv = XD[(t >> 4) * 256 + (t & 15) * 16 + (i & 15)];
+          xvv = XD[(t >> 4) * 256 + (t & 15) * 16 + (i & 15)];
         else
-          xv = AX[t * 65 + i];  // zero above the diagonal blocks
-        tv[m] = xv * SBETA[i];
+          xvv = AX[t * 65 + i];  // zero above the diagonal blocks
+        tv[m] = xvv * SBETA[i];
       }
-      st_shared_v4(sb + OFF_TT + umma::rp_offset(t, c0, 64), umma::pack2<BF>(tv[0], tv[1]),
-                   umma::pack2<BF>(tv[2], tv[3]), umma::pack2<BF>(tv[4], tv[5]),
-                   umma::pack2<BF>(tv[6], tv[7]));
-      st_shared_v4(sb + OFF_TT + umma::rp_offset(t, c0 + 8, 64), umma::pack2<BF>(tv[8], tv[9]),
-                   umma::pack2<BF>(tv[10], tv[11]), umma::pack2<BF>(tv[12], tv[13]),
-                   umma::pack2<BF>(tv[14], tv[15]));
+      const uint32_t off = umma::rp_offset(t, c0, 64);
+      if (SPLIT) {
+        uint32_t h0[2], l0[2], h1[2], l1[2];
+        split4(tv[0], tv[1], tv[2], tv[3], h0, l0);
+        split4(tv[4], tv[5], tv[6], tv[7], h1, l1);
+        st_shared_v4(sb + OFF_TT + off, h0[0], h0[1], h1[0], h1[1]);
+        st_shared_v4(sb + OFF_TTL + off, l0[0], l0[1], l1[0], l1[1]);
+      } else {
+        st_shared_v4(sb + OFF_TT + off, umma::pack2<BF>(tv[0], tv[1]), umma::pack2<BF>(tv[2], tv[3]),
+                     umma::pack2<BF>(tv[4], tv[5]), umma::pack2<BF>(tv[6], tv[7]));
+      }
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -636,8 +689,15 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16) {
         const uint64_t bd = umma::desc_kmajor(sb + OFF_TT, 64, k0);
-        umma::mma_f16(tm + COL_R2, umma::desc_mnmajor(sb + OFF_KH, 64, k0), bd, id2, k0 > 0);
-        umma::mma_f16(tm + COL_R1, umma::desc_mnmajor(sb + OFF_VV, 64, k0), bd, id2, k0 > 0);
+        const uint64_t akh = umma::desc_mnmajor(sb + OFF_KH, 64, k0);
+        const uint64_t avv = umma::desc_mnmajor(sb + OFF_VV, 64, k0);
+        umma::mma_f16(tm + COL_R2, akh, bd, id2, k0 > 0);
+        umma::mma_f16(tm + COL_R1, avv, bd, id2, k0 > 0);
+        if (SPLIT) {
+          const uint64_t bl = umma::desc_kmajor(sb + OFF_TTL, 64, k0);
+          umma::mma_f16(tm + COL_R2, akh, bl, id2, 1);
+          umma::mma_f16(tm + COL_R1, avv, bl, id2, 1);
+        }
       }
       umma::mma_commit(&bar_mma);
     }
@@ -645,16 +705,15 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- -W into shared memory (rows c); S0 <- S0 Diag(gamma_last) in TMEM
     {
+      float w16[16];
+      umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), w16);
+      put16<BF>(sb + OFF_WW, 128, vrow, slice * 16, w16, -1.f);
       float v[32];
-      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R2 + half * 32), v);
-      put32<BF>(sb + OFF_WW, 128, vrow, half * 32, v, -1.f);
-#pragma unroll 1
-      for (int cc = half * 64; cc < half * 64 + 64; cc += 32) {
-        umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
+      const int cc = slice * 32;
+      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] *= GLAST[KDA ? cc + k : 0];
-        umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
-      }
+      for (int k = 0; k < 32; ++k) v[k] *= GLAST[KDA ? cc + k : 0];
+      umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -677,9 +736,12 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- U^T into shared memory (rows v)
     {
-      float v[32];
-      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R1 + half * 32), v);
-      put32<BF>(sb + OFF_UT, 128, vrow, half * 32, v, 1.f);
+      float v[16];
+      umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R1 + slice * 16), v);
+      if (SPLIT)
+        put16_split(sb + OFF_UT, sb + OFF_UTL, 128, vrow, slice * 16, v, 1.f);
+      else
+        put16<BF>(sb + OFF_UT, 128, vrow, slice * 16, v, 1.f);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -693,8 +755,16 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16) {
         const uint64_t ad = umma::desc_kmajor(sb + OFF_UT, 128, k0);
-        umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_PP, 64, k0), id4, 1);
-        umma::mma_f16(tm + COL_S, ad, umma::desc_mnmajor(sb + OFF_KT, 64, k0), id5, 1);
+        const uint64_t bp = umma::desc_kmajor(sb + OFF_PP, 64, k0);
+        const uint64_t bk = umma::desc_mnmajor(sb + OFF_KT, 64, k0);
+        umma::mma_f16(tm + COL_R2, ad, bp, id4, 1);
+        umma::mma_f16(tm + COL_S, ad, bk, id5, 1);
+        if (SPLIT) {
+          const uint64_t al = umma::desc_kmajor(sb + OFF_UTL, 128, k0);
+          umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_PPL, 64, k0), id4, 1);
+          umma::mma_f16(tm + COL_R2, al, bp, id4, 1);
+          umma::mma_f16(tm + COL_S, al, bk, id5, 1);
+        }
       }
       umma::mma_commit(&bar_mma);
     }
@@ -702,13 +772,28 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- outputs, state operand for the next chunk, snapshots, final state
     {
-      float v[32];
-      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_R2 + half * 32), v);
-#pragma unroll 4
-      for (int k = 0; k < 32; ++k) {
-        const int t = half * 32 + k;
-        if (t < n) store_elem(a.out, ((row0 + t) * H + h) * DH + vrow, a.out_dtype, v[k]);
+      {
+        float o16[16];
+        umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), o16);
+        const int64_t ob = (row0 * H + h) * DH + vrow;
+        const int64_t ostep = int64_t(H) * DH;
+        if (a.out_dtype == LIN_BF16) {
+          uint16_t* op = static_cast<uint16_t*>(a.out) + ob;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int t = slice * 16 + k;
+            if (t < n) op[t * ostep] = f32_to_bf16_bits(o16[k]);
+          }
+        } else {
+          float* op = static_cast<float*>(a.out) + ob;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int t = slice * 16 + k;
+            if (t < n) op[t * ostep] = o16[k];
+          }
+        }
       }
+      float v[32];
       const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
       int snap_dst = -1;
       if (ntr > 0 && n == CH && (end_pos % a.track_stride) == 0) {
@@ -720,22 +805,27 @@ __global__ void __launch_bounds__(NT, 1)
                                          a.layer * pool.temporal_layer_stride +
                                          snap_dst * pool.temporal_slot_stride + h * head_bytes
                                    : nullptr;
-#pragma unroll 1
-      for (int cc = half * 64; cc < half * 64 + 64; cc += 32) {
+      {
+        const int cc = slice * 32;
         umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
         put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
         if (snap_t) store_row32<ST>(snap_t, vrow, cc, v);
         if (last) store_row32<ST>(slot_t, vrow, cc, v);
       }
       if (snap_dst >= 0 || last) {
+        // conv window after the chunk: its last 3 inputs (chunk rows n-3 .. n-1)
         char* snap_c = snap_dst >= 0 ? static_cast<char*>(pool.conv) +
                                            a.layer * pool.conv_layer_stride +
                                            snap_dst * pool.conv_slot_stride
                                      : nullptr;
         for (int idx = tid; idx < 3 * 384; idx += NT) {
           const int cl = idx / 3, m = idx % 3;
-          const int64_t off = int64_t(head_channel(cl, h, H)) * 3 + m;
-          const float wv = WEND[m * 384 + cl];
+          const int rel = n - 3 + m;
+          const int ch = head_channel(cl, h, H);
+          const float wv = (j == 0 && rel < 0)
+                               ? HALO[(rel + 3) * 384 + cl]
+                               : bf16_bits_to_f32(xg[(row0 + rel) * C_all + ch]);
+          const int64_t off = int64_t(ch) * 3 + m;
           if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
           if (last) store_elem(slot_c, off, pool.conv_dtype, wv);
         }
@@ -746,10 +836,7 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
   }
 
-  // ---- teardown: no copy may still target shared memory when the CTA exits
-  if (tid == 0 && x_inflight) {
-    if (!umma::mbar_wait(&bar_x, ph_x, kWaitTries)) report(a.status, LIN_ST_TIMEOUT);
-  }
+  // ---- teardown
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 0) umma::tmem_dealloc(tm, TMEM_COLS);

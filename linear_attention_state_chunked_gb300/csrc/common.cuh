@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/lin_state.h"
+#include "lin_state.h"
 
 namespace lin {
 
@@ -85,6 +85,6 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
-__device__ __forceinline__ float silu(float y) { return y / (1.0f + __expf(-y)); }
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
 
 }  // namespace lin

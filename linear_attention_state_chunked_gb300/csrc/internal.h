@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/lin_state.h"
+#include "lin_state.h"
 
 namespace lin {
 

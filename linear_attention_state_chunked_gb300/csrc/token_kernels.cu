@@ -197,17 +197,30 @@ __device__ __forceinline__ void store_window(void* conv_base, int conv_dtype,
 }
 
 // ---------------------------------------------------------------------------
-// Decode / verify. grid (batch, H), block NT.
+// Decode / verify. One CTA per (request, head). The head's state block
+// (D x D in the pool dtype) is staged into shared memory with one bulk async
+// copy issued before any other work, so the bytes in flight do not cost
+// registers and many CTAs stream per SM; the conv of the head's q|k|v channels
+// and the q / k norms overlap with that copy. Each thread then updates its
+// rows from shared memory (8 key channels per lane, D/8 lanes per row) and
+// writes them straight to their destinations.
 // ---------------------------------------------------------------------------
 struct DecodeParams {
   lin_state_pool_t pool;
   lin_decode_args_t a;
 };
 
+constexpr uint32_t kDecWaitTries = 1u << 24;
+
 template <int D, int ST>
-__global__ void __launch_bounds__(TokCfg<D>::NT) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(TokCfg<D>::NT, 3) decode_kernel(DecodeParams p) {
   using C = TokCfg<D>;
-  __shared__ TokSmem<D> sm;
+  constexpr int ES = ST == LIN_BF16 ? 2 : 4;
+  constexpr int BLK = D * D * ES;
+  extern __shared__ __align__(16) uint8_t dsm_state[];
+  __shared__ float ysm[2][3 * D + 2];
+  __shared__ uint64_t bar;
+  __shared__ int abort_sh;
   const lin_state_pool_t& pool = p.pool;
   const lin_decode_args_t& a = p.a;
   const int r = blockIdx.x, h = blockIdx.y;
@@ -229,15 +242,24 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) decode_kernel(DecodeParams p) {
     if (rep) report(a.status, LIN_ST_TRACK_ALIAS);
     return;
   }
-  constexpr int ES = ST == LIN_BF16 ? 2 : 4;
-  const int64_t head_bytes = int64_t(D) * D * ES;
+  const int64_t head_bytes = BLK;
   char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
                  slot * pool.temporal_slot_stride + h * head_bytes;
   char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                  slot * pool.conv_slot_stride;
-
-  float s[C::RPT][8];
-  load_rows<D, ST>(slot_t, s);
+  const uint32_t sst = static_cast<uint32_t>(__cvta_generic_to_shared(dsm_state));
+  const uint32_t sbar = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sbar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sbar), "r"(BLK)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sst),
+        "l"(reinterpret_cast<uint64_t>(slot_t)), "r"(BLK), "r"(sbar)
+        : "memory");
+  }
 
   const int C_all = pool.conv_channels;
   int chan[C::CPT];
@@ -253,47 +275,99 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) decode_kernel(DecodeParams p) {
       for (int j = 0; j < 4; ++j) w[i][j] = load_elem(a.conv_w, int64_t(chan[i]) * 4 + j, a.io_dtype);
     }
   }
-
+  const bool silu_on = a.flags & LIN_CONV_SILU;
   const int ND = a.n_draft;
+  const int lr = threadIdx.x % C::LPR, row0 = threadIdx.x / C::LPR;
   for (int j = 0; j < ND; ++j) {
-    float* ys = sm.y[j & 1];
+    float* ys = ysm[j & 1];
     const int64_t tok = int64_t(r) * ND + j;
-    conv_token<D>(win, w, a.x, tok * C_all, chan, a.io_dtype, a.flags & LIN_CONV_SILU, ys);
-    __syncthreads();
-    qk_norms<D>(ys, a.flags & LIN_QK_L2NORM);
-    __syncthreads();
-    float a8[8];
-    const int64_t gbase = a.gate_mode == LIN_GATE_PER_KEY ? (tok * H + h) * D : tok * H + h;
-    load_alpha<D>(a8, a.g, gbase, a.gate_mode);
-    const float beta = a.beta[tok * H + h];
-    rows_update<D>(s, ys, a8, beta, a.q_scale, a.out, (tok * H + h) * D, a.out_dtype);
-    // The state and window are stored after every token; keep the stored values.
-#pragma unroll
-    for (int i = 0; i < C::RPT; ++i) Vec8<ST>::round(s[i]);
+    conv_token<D>(win, w, a.x, tok * C_all, chan, a.io_dtype, silu_on, ys);
 #pragma unroll
     for (int i = 0; i < C::CPT; ++i)
 #pragma unroll
       for (int q = 0; q < 3; ++q) win[i][q] = round_to_dtype(win[i][q], pool.conv_dtype);
+    __syncthreads();
+    qk_norms<D>(ys, a.flags & LIN_QK_L2NORM);
+    if (j == 0 && threadIdx.x == 0) {
+      // the state block must have landed before anyone reads it
+      bool ok = false;
+      for (uint32_t it = 0; it < kDecWaitTries && !ok; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(sbar)
+            : "memory");
+        ok = done != 0;
+      }
+      if (!ok) {
+        abort_sh = 1;
+        report(a.status, LIN_ST_TIMEOUT);
+      }
+    }
+    __syncthreads();
+    if (abort_sh) return;  // (the copy was given up on; nothing is written)
+    float a8[8];
+    const int64_t gbase = a.gate_mode == LIN_GATE_PER_KEY ? (tok * H + h) * D : tok * H + h;
+    load_alpha<D>(a8, a.g, gbase, a.gate_mode);
+    const float beta = a.beta[tok * H + h];
+    const float rq = ys[3 * D] * a.q_scale, rk = ys[3 * D + 1];
+    float q8[8], k8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      q8[e] = ys[lr * 8 + e] * rq;
+      k8[e] = ys[D + lr * 8 + e] * rk;
+    }
+    char* dt;
+    char* dc;
+    char* tt = nullptr;
+    char* tc = nullptr;
     if (ND == 1) {
-      store_rows<D, ST>(slot_t, s);
-      store_window<D>(slot_c, pool.conv_dtype, chan, win);
+      dt = slot_t;
+      dc = slot_c;
       const int n = a.pos[r] + 1;
       if (ts >= 0 && a.track_interval > 0 && n % a.track_interval == 0) {
-        char* tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
-                   ts * pool.temporal_slot_stride + h * head_bytes;
-        char* tc = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
-                   ts * pool.conv_slot_stride;
-        store_rows<D, ST>(tt, s);
-        store_window<D>(tc, pool.conv_dtype, chan, win);
+        tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+             ts * pool.temporal_slot_stride + h * head_bytes;
+        tc = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+             ts * pool.conv_slot_stride;
       }
     } else {
-      char* st = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
-                 r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + h * head_bytes;
-      char* sc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
-                 r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
-      store_rows<D, ST>(st, s);
-      store_window<D>(sc, pool.conv_dtype, chan, win);
+      dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
+           r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + h * head_bytes;
+      dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
+           r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
     }
+#pragma unroll 2
+    for (int i = 0; i < C::RPT; ++i) {
+      const int row = row0 + i * C::RSTEP;
+      const int64_t off = (int64_t(row) * D + lr * 8) * ES;
+      float sv[8];
+      Vec8<ST>::load(dsm_state + off, sv);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sv[e] *= a8[e];
+        dot = fmaf(sv[e], k8[e], dot);
+      }
+      dot = row_sum<C::LPR>(dot);
+      const float u = beta * (ys[2 * D + row] - dot);
+      float o = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sv[e] = fmaf(u, k8[e], sv[e]);
+        o = fmaf(sv[e], q8[e], o);
+      }
+      o = row_sum<C::LPR>(o);
+      if (lr == 0) store_elem(a.out, (tok * H + h) * D + row, a.out_dtype, o);
+      Vec8<ST>::round(sv);  // the stored state is what the next token starts from
+      Vec8<ST>::store(dt + off, sv);
+      if (tt) Vec8<ST>::store(tt + off, sv);
+      if (ND > 1) Vec8<ST>::store(dsm_state + off, sv);
+    }
+    store_window<D>(dc, pool.conv_dtype, chan, win);
+    if (tc) store_window<D>(tc, pool.conv_dtype, chan, win);
   }
 }
 
@@ -414,7 +488,11 @@ template <int D, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           cudaStream_t stream) {
   DecodeParams p{pool, a};
-  decode_kernel<D, ST><<<dim3(a.batch, pool.num_heads), TokCfg<D>::NT, 0, stream>>>(p);
+  const int smem = D * D * (ST == LIN_BF16 ? 2 : 4);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, ST>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<D, ST><<<dim3(a.batch, pool.num_heads), TokCfg<D>::NT, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
