@@ -569,9 +569,11 @@ def main():
         line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16-in/fp32-state" if names[0] == HEADLINE else "bf16",
+                "dtype": "f32",
                 "data": "synthetic",
                 "config": {**head["config"], "parallelism": f"replicas{world}",
+                           "arithmetic": "fp32 state and accumulation; tensor-core operands fp16 "
+                                         "with hi/lo splits (GDN) or bf16 (KDA); bf16 inputs",
                            "l2": "inputs larger than L2 (x alone is 805 MB); decode rotates 4 pool "
                                  "replicas and writes a 256 MB buffer between steps"},
                 "roofline": {**head["roofline"], "peak_source": peaks["source"]},
