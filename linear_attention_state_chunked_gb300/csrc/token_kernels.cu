@@ -181,15 +181,13 @@ __device__ __forceinline__ void load_rows(const char* base, float (&s)[TokCfg<D>
     Vec8<ST>::load(base + (int64_t(row0 + i * C::RSTEP) * D + lr * 8) * ES, s[i]);
 }
 
-template <int D>
-__device__ __forceinline__ void store_window(void* conv_base, int conv_dtype,
-                                             const int (&chan)[TokCfg<D>::CPT],
-                                             const float (&win)[TokCfg<D>::CPT][3]) {
-  using C = TokCfg<D>;
+template <int CPT, int D>
+__device__ __forceinline__ void store_window(void* conv_base, int conv_dtype, const int (&chan)[CPT],
+                                             const float (&win)[CPT][3]) {
 #pragma unroll
-  for (int i = 0; i < C::CPT; ++i) {
-    const int cl = threadIdx.x + i * C::NT;
-    if (cl < C::CH) {
+  for (int i = 0; i < CPT; ++i) {
+    const int cl = threadIdx.x + i * blockDim.x;
+    if (cl < 3 * D) {
 #pragma unroll
       for (int j = 0; j < 3; ++j) store_elem(conv_base, int64_t(chan[i]) * 3 + j, conv_dtype, win[i][j]);
     }
@@ -197,11 +195,11 @@ __device__ __forceinline__ void store_window(void* conv_base, int conv_dtype,
 }
 
 // ---------------------------------------------------------------------------
-// Decode / verify. One CTA per (request, head). The head's state block
-// (D x D in the pool dtype) is staged into shared memory with one bulk async
-// copy issued before any other work, so the bytes in flight do not cost
-// registers and many CTAs stream per SM; the conv of the head's q|k|v channels
-// and the q / k norms overlap with that copy. Each thread then updates its
+// Decode / verify. One CTA per (request, head). Everything the head needs --
+// its state block, the conv window and taps of its q|k|v channels, and the
+// step's x (and per-key g) rows -- is staged into shared memory by bulk async
+// copies on one mbarrier, issued before any other work, so loads in flight
+// cost no registers and the CTA stays small. Each thread then updates its
 // rows from shared memory (8 key channels per lane, D/8 lanes per row) and
 // writes them straight to their destinations.
 // ---------------------------------------------------------------------------
@@ -212,12 +210,42 @@ struct DecodeParams {
 
 constexpr uint32_t kDecWaitTries = 1u << 24;
 
+template <int D>
+struct DecCfg {
+  static constexpr int LPR = D / 8;
+  static constexpr int NT = (D * LPR) < 128 ? ((D * LPR) < 32 ? 32 : D * LPR) : 128;
+  static constexpr int RSTEP = NT / LPR;
+  static constexpr int RPT = D / RSTEP;
+  static constexpr int CH = 3 * D;
+  static constexpr int CPT = (CH + NT - 1) / NT;
+  static_assert(RPT * RSTEP == D, "rows");
+};
+
+// Shared-memory layout of one decode CTA (byte offsets; every piece 16-aligned).
+struct DecSmem {
+  int state, conv, w, x, g, total;
+  __host__ __device__ DecSmem(int D, int es_state, int es_conv, int es_io, int nd, bool per_key) {
+    state = 0;
+    conv = state + D * D * es_state;
+    w = conv + 3 * D * 3 * es_conv;
+    x = w + 3 * D * 4 * es_io;
+    g = x + nd * 3 * D * es_io;
+    total = g + (per_key ? nd * D * 4 : 0);
+  }
+};
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 template <int D, int ST>
-__global__ void __launch_bounds__(TokCfg<D>::NT, 3) decode_kernel(DecodeParams p) {
-  using C = TokCfg<D>;
+__global__ void __launch_bounds__(DecCfg<D>::NT) decode_kernel(DecodeParams p) {
+  using C = DecCfg<D>;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
-  constexpr int BLK = D * D * ES;
-  extern __shared__ __align__(16) uint8_t dsm_state[];
+  extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ float ysm[2][3 * D + 2];
   __shared__ uint64_t bar;
   __shared__ int abort_sh;
@@ -242,26 +270,66 @@ __global__ void __launch_bounds__(TokCfg<D>::NT, 3) decode_kernel(DecodeParams p
     if (rep) report(a.status, LIN_ST_TRACK_ALIAS);
     return;
   }
-  const int64_t head_bytes = BLK;
+  const int ND = a.n_draft;
+  const bool per_key = a.gate_mode == LIN_GATE_PER_KEY;
+  const int esc = pool.conv_dtype == LIN_BF16 ? 2 : 4;
+  const int esi = a.io_dtype == LIN_BF16 ? 2 : 4;
+  const DecSmem L(D, ES, esc, esi, ND, per_key);
+  const int64_t head_bytes = int64_t(D) * D * ES;
   char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
                  slot * pool.temporal_slot_stride + h * head_bytes;
   char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                  slot * pool.conv_slot_stride;
-  const uint32_t sst = static_cast<uint32_t>(__cvta_generic_to_shared(dsm_state));
+  const int C_all = pool.conv_channels;
+  const uint32_t s0 = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
   const uint32_t sbar = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
   if (threadIdx.x == 0) {
     abort_sh = 0;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sbar) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sbar), "r"(BLK)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sbar),
+                 "r"(static_cast<uint32_t>(L.total))
                  : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sst),
-        "l"(reinterpret_cast<uint64_t>(slot_t)), "r"(BLK), "r"(sbar)
-        : "memory");
+    bulk_g2s(s0 + L.state, slot_t, D * D * ES, sbar);
+    for (int part = 0; part < 3; ++part) {
+      const int64_t ch0 = int64_t(part) * H * D + int64_t(h) * D;  // first channel of the part
+      bulk_g2s(s0 + L.conv + part * D * 3 * esc, static_cast<const char*>(slot_c) + ch0 * 3 * esc,
+               D * 3 * esc, sbar);
+      bulk_g2s(s0 + L.w + part * D * 4 * esi, static_cast<const char*>(a.conv_w) + ch0 * 4 * esi,
+               D * 4 * esi, sbar);
+      for (int j = 0; j < ND; ++j) {
+        const int64_t tok = int64_t(r) * ND + j;
+        bulk_g2s(s0 + L.x + (j * 3 + part) * D * esi,
+                 static_cast<const char*>(a.x) + (tok * C_all + ch0) * esi, D * esi, sbar);
+      }
+    }
+    if (per_key)
+      for (int j = 0; j < ND; ++j) {
+        const int64_t tok = int64_t(r) * ND + j;
+        bulk_g2s(s0 + L.g + j * D * 4, a.g + (tok * H + h) * D, D * 4, sbar);
+      }
+    bool ok = false;
+    for (uint32_t it = 0; it < kDecWaitTries && !ok; ++it) {
+      uint32_t done;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(done)
+          : "r"(sbar)
+          : "memory");
+      ok = done != 0;
+    }
+    if (!ok) {
+      abort_sh = 1;
+      report(a.status, LIN_ST_TIMEOUT);
+    }
   }
+  __syncthreads();
+  if (abort_sh) return;  // the copies were given up on; nothing is written
 
-  const int C_all = pool.conv_channels;
+  const uint8_t* sconv = dsm + L.conv;
+  const uint8_t* sw = dsm + L.w;
+  // conv channels: local cl in [0, 3D), part = cl / D
   int chan[C::CPT];
   float win[C::CPT][3], w[C::CPT][4];
 #pragma unroll
@@ -270,47 +338,55 @@ __global__ void __launch_bounds__(TokCfg<D>::NT, 3) decode_kernel(DecodeParams p
     chan[i] = cl < C::CH ? head_channel(cl, h, H, D) : 0;
     if (cl < C::CH) {
 #pragma unroll
-      for (int j = 0; j < 3; ++j) win[i][j] = load_elem(slot_c, int64_t(chan[i]) * 3 + j, pool.conv_dtype);
+      for (int q = 0; q < 3; ++q) win[i][q] = load_elem(sconv, cl * 3 + q, pool.conv_dtype);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[i][j] = load_elem(a.conv_w, int64_t(chan[i]) * 4 + j, a.io_dtype);
+      for (int q = 0; q < 4; ++q) w[i][q] = load_elem(sw, cl * 4 + q, a.io_dtype);
     }
   }
   const bool silu_on = a.flags & LIN_CONV_SILU;
-  const int ND = a.n_draft;
   const int lr = threadIdx.x % C::LPR, row0 = threadIdx.x / C::LPR;
   for (int j = 0; j < ND; ++j) {
     float* ys = ysm[j & 1];
     const int64_t tok = int64_t(r) * ND + j;
-    conv_token<D>(win, w, a.x, tok * C_all, chan, a.io_dtype, silu_on, ys);
+    const uint8_t* sx = dsm + L.x + j * 3 * D * esi;
 #pragma unroll
-    for (int i = 0; i < C::CPT; ++i)
+    for (int i = 0; i < C::CPT; ++i) {
+      const int cl = threadIdx.x + i * C::NT;
+      if (cl < C::CH) {
+        const float xin = load_elem(sx, cl, a.io_dtype);
+        float y = w[i][0] * win[i][0] + w[i][1] * win[i][1] + w[i][2] * win[i][2] + w[i][3] * xin;
+        win[i][0] = win[i][1];
+        win[i][1] = win[i][2];
+        win[i][2] = xin;
 #pragma unroll
-      for (int q = 0; q < 3; ++q) win[i][q] = round_to_dtype(win[i][q], pool.conv_dtype);
-    __syncthreads();
-    qk_norms<D>(ys, a.flags & LIN_QK_L2NORM);
-    if (j == 0 && threadIdx.x == 0) {
-      // the state block must have landed before anyone reads it
-      bool ok = false;
-      for (uint32_t it = 0; it < kDecWaitTries && !ok; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(sbar)
-            : "memory");
-        ok = done != 0;
-      }
-      if (!ok) {
-        abort_sh = 1;
-        report(a.status, LIN_ST_TIMEOUT);
+        for (int q = 0; q < 3; ++q) win[i][q] = round_to_dtype(win[i][q], pool.conv_dtype);
+        ys[cl] = silu_on ? silu(y) : y;
       }
     }
     __syncthreads();
-    if (abort_sh) return;  // (the copy was given up on; nothing is written)
+    {
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      constexpr int NWp = C::NT / 32;
+      for (int part = (NWp >= 2 ? warp : 0); part < 2; part += (NWp >= 2 ? 2 : 1)) {
+        if (NWp >= 2 && warp >= 2) break;
+        float ss = 0.f;
+        for (int i = lane; i < D; i += 32) ss += ys[part * D + i] * ys[part * D + i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) ys[3 * D + part] = (a.flags & LIN_QK_L2NORM) ? rsqrtf(ss + kL2Eps) : 1.f;
+      }
+    }
+    __syncthreads();
     float a8[8];
-    const int64_t gbase = a.gate_mode == LIN_GATE_PER_KEY ? (tok * H + h) * D : tok * H + h;
-    load_alpha<D>(a8, a.g, gbase, a.gate_mode);
+    if (per_key) {
+      const float* sg = reinterpret_cast<const float*>(dsm + L.g) + j * D + lr * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a8[e] = expf(sg[e]);
+    } else {
+      const float av = expf(a.g[tok * H + h]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a8[e] = av;
+    }
     const float beta = a.beta[tok * H + h];
     const float rq = ys[3 * D] * a.q_scale, rk = ys[3 * D + 1];
     float q8[8], k8[8];
@@ -339,12 +415,13 @@ __global__ void __launch_bounds__(TokCfg<D>::NT, 3) decode_kernel(DecodeParams p
       dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
            r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
     }
-#pragma unroll 2
+    uint8_t* sst = dsm + L.state;
+#pragma unroll 4
     for (int i = 0; i < C::RPT; ++i) {
       const int row = row0 + i * C::RSTEP;
       const int64_t off = (int64_t(row) * D + lr * 8) * ES;
       float sv[8];
-      Vec8<ST>::load(dsm_state + off, sv);
+      Vec8<ST>::load(sst + off, sv);
       float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -364,10 +441,10 @@ __global__ void __launch_bounds__(TokCfg<D>::NT, 3) decode_kernel(DecodeParams p
       Vec8<ST>::round(sv);  // the stored state is what the next token starts from
       Vec8<ST>::store(dt + off, sv);
       if (tt) Vec8<ST>::store(tt + off, sv);
-      if (ND > 1) Vec8<ST>::store(dsm_state + off, sv);
+      if (ND > 1) Vec8<ST>::store(sst + off, sv);
     }
-    store_window<D>(dc, pool.conv_dtype, chan, win);
-    if (tc) store_window<D>(tc, pool.conv_dtype, chan, win);
+    store_window<DecCfg<D>::CPT, D>(dc, pool.conv_dtype, chan, win);
+    if (tc) store_window<DecCfg<D>::CPT, D>(tc, pool.conv_dtype, chan, win);
   }
 }
 
@@ -476,23 +553,25 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
         char* tc = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                    dst * pool.conv_slot_stride;
         store_rows<D, ST>(tt, s);
-        store_window<D>(tc, pool.conv_dtype, chan, win);
+        store_window<TokCfg<D>::CPT, D>(tc, pool.conv_dtype, chan, win);
       }
     }
   }
   store_rows<D, ST>(slot_t, s);
-  store_window<D>(slot_c, pool.conv_dtype, chan, win);
+  store_window<TokCfg<D>::CPT, D>(slot_c, pool.conv_dtype, chan, win);
 }
 
 template <int D, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           cudaStream_t stream) {
   DecodeParams p{pool, a};
-  const int smem = D * D * (ST == LIN_BF16 ? 2 : 4);
+  const DecSmem L(D, ST == LIN_BF16 ? 2 : 4, dtype_size(pool.conv_dtype), dtype_size(a.io_dtype),
+                  a.n_draft, a.gate_mode == LIN_GATE_PER_KEY);
+  if (L.total > 200 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, ST>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, ST><<<dim3(a.batch, pool.num_heads), TokCfg<D>::NT, smem, stream>>>(p);
+  decode_kernel<D, ST><<<dim3(a.batch, pool.num_heads), DecCfg<D>::NT, L.total, stream>>>(p);
   return cudaGetLastError();
 }
 
