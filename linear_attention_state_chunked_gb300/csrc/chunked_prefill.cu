@@ -54,15 +54,18 @@ constexpr uint32_t kWaitTries = 1u << 26;
 // Shared-memory map (offsets from a 1024-byte aligned base). Regions are
 // reused once their previous contents have been consumed by an MMA.
 constexpr uint32_t OFF_SOP = 0;                 // S0 operand, rows v, 128 x 128 16-bit
+constexpr uint32_t OFF_STG = 32768;             // epilogue: state tiles for TMA stores (64 KB)
 constexpr uint32_t OFF_KQ = 32768;              // [K_l; Q_l] (high part), 128 rows x 128
 constexpr uint32_t OFF_TT = OFF_KQ;             //   after MMA1: T (high), 64 x 64
 constexpr uint32_t OFF_TTL = OFF_KQ + 8192;     //   after MMA1: T (low part, GDN)
 constexpr uint32_t OFF_PP = OFF_KQ + 16384;     //   after MMA1: P (high), 64 x 64
 constexpr uint32_t OFF_PPL = OFF_KQ + 24576;    //   after MMA1: P (low part, GDN)
 constexpr uint32_t OFF_KQL = 65536;             // [K; Q] low part (GDN), 128 rows x 128
-constexpr uint32_t OFF_AX = OFF_KQL;            //   after MMA1: fp32 A / X [64][65]
-constexpr uint32_t OFF_XD = OFF_KQL + 16640;    //   after MMA1: fp32 diagonal inverses [4][16][16]
-constexpr uint32_t OFF_YB = OFF_XD + 4096;      //   after MMA1: fp32 block temporaries [3][16][16]
+constexpr int AXS = 68;                         // row stride (floats) of the fp32 A / X matrix
+constexpr uint32_t OFF_AX = OFF_KQL;            //   after MMA1: fp32 A / X [64][AXS]
+constexpr uint32_t OFF_XD = OFF_KQL + 64 * AXS * 4;  // after MMA1: fp32 diagonal inverses [4][16][16]
+constexpr uint32_t OFF_YB = OFF_XD + 4096;      //   after MMA1: fp32 M blocks X_aa A_ac [6][16][16]
+constexpr uint32_t OFF_OSTG = 98304;            // epilogue: output tile for a TMA store (32 KB)
 constexpr uint32_t OFF_KR = 98304;              // K_r (KDA), 64 x 128
 constexpr uint32_t OFF_UTL = OFF_KR;            //   after MMA2: U^T low part (GDN), rows v
 constexpr uint32_t OFF_KH = 114688;             // gamma . K, rows i (MN-major A)
@@ -80,7 +83,7 @@ constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
 constexpr uint32_t SMEM_USED = OFF_GLAST + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_YB + 3 * 1024 <= OFF_KR, "solve scratch inside the low-part region");
+static_assert(OFF_YB + 6 * 1024 <= OFF_KR, "solve scratch inside the low-part region");
 
 // Tensor-memory columns (256 allocated).
 constexpr uint32_t COL_S = 0;    // state, fp32, lanes v
@@ -159,6 +162,27 @@ __device__ __forceinline__ void prefetch_x_tile(const CUtensorMap* tmap, int64_t
   }
 }
 
+// TMA bulk-group stores from shared memory.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* tmap, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tmap, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // hi / lo fp16 split of four values: hi = fp16(x), lo = fp16(x - hi).
 __device__ __forceinline__ void split4(float a, float b, float c, float d, uint32_t (&hi)[2],
                                        uint32_t (&lo)[2]) {
@@ -232,7 +256,9 @@ __device__ __forceinline__ void put16_split(uint32_t hi_buf, uint32_t lo_buf, in
 
 template <bool KDA, int ST>
 __global__ void __launch_bounds__(NT, 1)
-    chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const ChunkParams p) {
+    chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                           const __grid_constant__ CUtensorMap tmap_state,
+                           const __grid_constant__ CUtensorMap tmap_out, const ChunkParams p) {
   // GDN: fp16 operands with high / low splits on the products that set the
   // error (see the header); KDA: bf16 operands, single products.
   constexpr bool BF = KDA;
@@ -417,6 +443,9 @@ __global__ void __launch_bounds__(NT, 1)
                              : make_uint2(0u, 0u);
     }
 
+    // the previous chunk's TMA stores must have read their staging tiles
+    if (tid == 0) bulk_wait_read();
+
     // ---- gates: in-chunk inclusive sums b_t (rows past n carry log-decay 0)
     float cs[TPW][4];
     {
@@ -483,43 +512,51 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t w = (e < 2) ? xr[m][part].x : xr[m][part].y;
         return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
       };
+      // part-major: the taps of one part are loaded once and applied to all
+      // of this warp's tokens; q and k get their per-token norms
+      float yq[TPW][4], yk[TPW][4], yv[TPW][4], rq[TPW], rk[TPW];
 #pragma unroll
-      for (int i = 0; i < TPW; ++i) {
-        const int t = tfirst + i;
-        float y[3][4];
+      for (int part = 0; part < 3; ++part) {
+        float4 w4[4];
 #pragma unroll
-        for (int part = 0; part < 3; ++part) {
-          float4 w4[4];
+        for (int tap = 0; tap < 4; ++tap)
+          w4[tap] = *reinterpret_cast<const float4*>(WC + tap * 384 + part * 128 + lane * 4);
 #pragma unroll
-          for (int tap = 0; tap < 4; ++tap)
-            w4[tap] = *reinterpret_cast<const float4*>(WC + tap * 384 + part * 128 + lane * 4);
+        for (int i = 0; i < TPW; ++i) {
+          float ss = 0.f;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float w0 = e == 0 ? w4[0].x : e == 1 ? w4[0].y : e == 2 ? w4[0].z : w4[0].w;
             const float w1 = e == 0 ? w4[1].x : e == 1 ? w4[1].y : e == 2 ? w4[1].z : w4[1].w;
             const float w2 = e == 0 ? w4[2].x : e == 1 ? w4[2].y : e == 2 ? w4[2].z : w4[2].w;
             const float w3 = e == 0 ? w4[3].x : e == 1 ? w4[3].y : e == 2 ? w4[3].z : w4[3].w;
-            const float yy = w0 * xv(i, part, e) + w1 * xv(i + 1, part, e) + w2 * xv(i + 2, part, e) +
-                             w3 * xv(i + 3, part, e);
-            y[part][e] = silu_on ? silu(yy) : yy;
+            float yy = w0 * xv(i, part, e) + w1 * xv(i + 1, part, e) + w2 * xv(i + 2, part, e) +
+                       w3 * xv(i + 3, part, e);
+            yy = silu_on ? silu(yy) : yy;
+            ss += yy * yy;
+            if (part == 0) yq[i][e] = yy;
+            else if (part == 1) yk[i][e] = yy;
+            else yv[i][e] = yy;
+          }
+          if (part < 2) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float rr = l2_on ? rsqrtf(ss + 1e-6f) : 1.f;
+            if (part == 0) rq[i] = rr * a.q_scale;
+            else rk[i] = rr;
           }
         }
-        float sq = y[0][0] * y[0][0] + y[0][1] * y[0][1] + y[0][2] * y[0][2] + y[0][3] * y[0][3];
-        float sk = y[1][0] * y[1][0] + y[1][1] * y[1][1] + y[1][2] * y[1][2] + y[1][3] * y[1][3];
+      }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          sq += __shfl_xor_sync(0xffffffffu, sq, o);
-          sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        }
-        const float rq = (l2_on ? rsqrtf(sq + 1e-6f) : 1.f) * a.q_scale;
-        const float rk = l2_on ? rsqrtf(sk + 1e-6f) : 1.f;
+      for (int i = 0; i < TPW; ++i) {
+        const int t = tfirst + i;
         const bool ok = t < n;
         float kn[4], qn[4], vv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          kn[e] = ok ? y[1][e] * rk : 0.f;
-          qn[e] = ok ? y[0][e] * rq : 0.f;
-          vv[e] = ok ? y[2][e] : 0.f;
+          kn[e] = ok ? yk[i][e] * rk[i] : 0.f;
+          qn[e] = ok ? yq[i][e] * rq[i] : 0.f;
+          vv[e] = ok ? yv[i][e] : 0.f;
         }
         float eL[4], eR[4], eH[4], eT[4];
 #pragma unroll
@@ -591,7 +628,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int k = 0; k < 16; ++k) {
           const int i = slice * 16 + k;
           const float dec = KDA ? 1.f : __expf(bt_ - SB[i < t ? i : t]);
-          AX[t * 65 + i] = (i < t) ? bet * v[k] * dec : 0.f;
+          AX[t * AXS + i] = (i < t) ? bet * v[k] * dec : 0.f;
         }
       } else {
         const int t = vrow - 64;
@@ -611,45 +648,79 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncthreads();
 
-    // ---- T = (I + A)^-1 Diag(beta), blocked over 16 x 16 tiles
-    if (tid < 64) {
-      // inverses of the four unit lower-triangular diagonal blocks, one column per thread
-      const int blk = tid >> 4, jj = tid & 15, base = blk * 16;
-      float x[16];
+    // ---- T = (I + A)^-1 Diag(beta), blocked over 16 x 16 tiles a, c:
+    //   X_aa = (I + A_aa)^-1 (unit lower triangular, forward substitution),
+    //   M_ac = X_aa A_ac for c < a (all six at once),
+    //   X_ab = -sum_{c=b}^{a-1} M_ac X_cb, by levels a - b = 1, 2, 3.
+    // Off-diagonal X blocks overwrite the A blocks in AX once those are used.
+    if (tid < 256) {
+      // one 4-lane group per (block, column); lane q of the group holds rows q, q+4, q+8, q+12
+      const int grp = tid >> 2, q = tid & 3;
+      const int blk = grp >> 4, jj = grp & 15, base = blk * 16;
+      float x[4];
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        float s = 0.f;
+      for (int u = 0; u < 4; ++u) x[u] = (4 * u + q == jj) ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < t; ++i) s += AX[(base + t) * 65 + base + i] * x[i];
-        x[t] = t < jj ? 0.f : (t == jj ? 1.f : -s);
+      for (int t = 1; t < 16; ++t) {
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = 4 * u + q;
+          if (i < t) part = fmaf(AX[(base + t) * AXS + base + i], x[u], part);
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if ((t & 3) == q && t > jj) x[t >> 2] = -part;
       }
 #pragma unroll
-      for (int t = 0; t < 16; ++t) XD[blk * 256 + t * 16 + jj] = x[t];
+      for (int u = 0; u < 4; ++u) XD[blk * 256 + (4 * u + q) * 16 + jj] = x[u];
     }
     __syncthreads();
-    for (int ab = 1; ab < 4; ++ab) {
-      // Y(ab, b) = sum_{c=b}^{ab-1} A(ab, c) X(c, b)
-      for (int item = tid; item < ab * 256; item += NT) {
-        const int b = item >> 8, t = (item >> 4) & 15, jj = item & 15;
-        float s = 0.f;
-        for (int c = b; c < ab; ++c) {
+    {
+      // M_ac = X_aa A_ac, blocks (a, c) in order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2);
+      // each thread: one row, four consecutive columns
+      for (int item = tid; item < 6 * 64; item += NT) {
+        const int mb = item >> 6, t = (item >> 2) & 15, j4 = (item & 3) * 4;
+        const int a_ = mb < 1 ? 1 : (mb < 3 ? 2 : 3);
+        const int c_ = mb - (a_ * (a_ - 1)) / 2;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float xd = XD[a_ * 256 + t * 16 + m];
+          const float4 av = *reinterpret_cast<const float4*>(AX + (a_ * 16 + m) * AXS + c_ * 16 + j4);
+          acc[0] = fmaf(xd, av.x, acc[0]);
+          acc[1] = fmaf(xd, av.y, acc[1]);
+          acc[2] = fmaf(xd, av.z, acc[2]);
+          acc[3] = fmaf(xd, av.w, acc[3]);
+        }
+        *reinterpret_cast<float4*>(YB + mb * 256 + t * 16 + j4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int lev = 1; lev < 4; ++lev) {
+      // blocks (a, b) with a - b = lev
+      for (int item = tid; item < (4 - lev) * 64; item += NT) {
+        const int b_ = item >> 6, a_ = b_ + lev, t = (item >> 2) & 15, j4 = (item & 3) * 4;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c_ = b_; c_ < a_; ++c_) {
+          const int mb = (a_ * (a_ - 1)) / 2 + c_;
 #pragma unroll
           for (int m = 0; m < 16; ++m) {
-            const float av = AX[(ab * 16 + t) * 65 + c * 16 + m];
-            const float xv = (c == b) ? XD[c * 256 + m * 16 + jj] : AX[(c * 16 + m) * 65 + b * 16 + jj];
-            s += av * xv;
+            const float mv = YB[mb * 256 + t * 16 + m];
+            float4 xv;
+            if (c_ == b_)
+              xv = *reinterpret_cast<const float4*>(XD + b_ * 256 + m * 16 + j4);
+            else
+              xv = *reinterpret_cast<const float4*>(AX + (c_ * 16 + m) * AXS + b_ * 16 + j4);
+            acc[0] = fmaf(mv, xv.x, acc[0]);
+            acc[1] = fmaf(mv, xv.y, acc[1]);
+            acc[2] = fmaf(mv, xv.z, acc[2]);
+            acc[3] = fmaf(mv, xv.w, acc[3]);
           }
         }
-        YB[b * 256 + t * 16 + jj] = s;
-      }
-      __syncthreads();
-      // X(ab, b) = -X(ab, ab) Y(ab, b)
-      for (int item = tid; item < ab * 256; item += NT) {
-        const int b = item >> 8, t = (item >> 4) & 15, jj = item & 15;
-        float s = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) s += XD[ab * 256 + t * 16 + m] * YB[b * 256 + m * 16 + jj];
-        AX[(ab * 16 + t) * 65 + b * 16 + jj] = -s;
+        *reinterpret_cast<float4*>(AX + (a_ * 16 + t) * AXS + b_ * 16 + j4) =
+            make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
       }
       __syncthreads();
     }
@@ -663,7 +734,7 @@ __global__ void __launch_bounds__(NT, 1)
         if ((i >> 4) == (t >> 4))
           xvv = XD[(t >> 4) * 256 + (t & 15) * 16 + (i & 15)];
         else
-          xvv = AX[t * 65 + i];  // zero above the diagonal blocks
+          xvv = AX[t * AXS + i];  // zero above the diagonal blocks
         tv[m] = xvv * SBETA[i];
       }
       const uint32_t off = umma::rp_offset(t, c0, 64);
@@ -770,49 +841,84 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (!wait_mma()) break;
 
-    // ---- outputs, state operand for the next chunk, snapshots, final state
+    // ---- outputs, state operand for the next chunk, snapshots, final state.
+    // Full-chunk outputs and every stored state go through swizzled staging
+    // tiles and TMA stores, so the copy engine drains them while the next
+    // chunk's conv phase runs.
     {
+      const bool full = (n == CH);
+      const int oes = a.out_dtype == LIN_BF16 ? 2 : 4;
       {
         float o16[16];
         umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), o16);
-        const int64_t ob = (row0 * H + h) * DH + vrow;
-        const int64_t ostep = int64_t(H) * DH;
-        if (a.out_dtype == LIN_BF16) {
-          uint16_t* op = static_cast<uint16_t*>(a.out) + ob;
+        if (full) {
+          uint8_t* ost = sm + OFF_OSTG;
+          if (oes == 2) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int t = slice * 16 + k;
-            if (t < n) op[t * ostep] = f32_to_bf16_bits(o16[k]);
+            for (int k = 0; k < 16; ++k)
+              reinterpret_cast<uint16_t*>(ost)[(slice * 16 + k) * DH + vrow] = f32_to_bf16_bits(o16[k]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) reinterpret_cast<float*>(ost)[(slice * 16 + k) * DH + vrow] = o16[k];
           }
         } else {
-          float* op = static_cast<float*>(a.out) + ob;
+          const int64_t ob = (row0 * H + h) * DH + vrow;
+          const int64_t ostep = int64_t(H) * DH;
+          if (oes == 2) {
+            uint16_t* op = static_cast<uint16_t*>(a.out) + ob;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int t = slice * 16 + k;
-            if (t < n) op[t * ostep] = o16[k];
+            for (int k = 0; k < 16; ++k) {
+              const int t = slice * 16 + k;
+              if (t < n) op[t * ostep] = f32_to_bf16_bits(o16[k]);
+            }
+          } else {
+            float* op = static_cast<float*>(a.out) + ob;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int t = slice * 16 + k;
+              if (t < n) op[t * ostep] = o16[k];
+            }
           }
         }
       }
-      float v[32];
       const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
       int snap_dst = -1;
-      if (ntr > 0 && n == CH && (end_pos % a.track_stride) == 0) {
+      if (ntr > 0 && full && (end_pos % a.track_stride) == 0) {
         snap_dst = a.track_slots[t0 + (snap % ntr)];
         ++snap;
       }
       const bool last = (j == nch - 1);
-      char* snap_t = snap_dst >= 0 ? static_cast<char*>(pool.temporal) +
-                                         a.layer * pool.temporal_layer_stride +
-                                         snap_dst * pool.temporal_slot_stride + h * head_bytes
-                                   : nullptr;
+      const bool store_state = snap_dst >= 0 || last;
       {
+        float v[32];
         const int cc = slice * 32;
         umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
         put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
-        if (snap_t) store_row32<ST>(snap_t, vrow, cc, v);
-        if (last) store_row32<ST>(slot_t, vrow, cc, v);
+        if (store_state) {
+          // state tile of 32 rows x 128 bytes, 128-byte swizzle (chunk m of row r at m ^ (r % 8))
+          if (ST == LIN_BF16) {
+            const uint32_t tile = sb + OFF_STG + (quarter * 2 + (slice >> 1)) * 4096 + lane * 128;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int chunk = ((slice & 1) * 4 + m) ^ (lane & 7);
+              st_shared_v4(tile + chunk * 16,
+                           static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m])) | (static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 1])) << 16),
+                           static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 2])) | (static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 3])) << 16),
+                           static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 4])) | (static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 5])) << 16),
+                           static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 6])) | (static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 7])) << 16));
+            }
+          } else {
+            const uint32_t tile = sb + OFF_STG + (quarter * 4 + slice) * 4096 + lane * 128;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const int chunk = m ^ (lane & 7);
+              st_shared_v4(tile + chunk * 16, __float_as_uint(v[4 * m]), __float_as_uint(v[4 * m + 1]),
+                           __float_as_uint(v[4 * m + 2]), __float_as_uint(v[4 * m + 3]));
+            }
+          }
+        }
       }
-      if (snap_dst >= 0 || last) {
+      if (store_state) {
         // conv window after the chunk: its last 3 inputs (chunk rows n-3 .. n-1)
         char* snap_c = snap_dst >= 0 ? static_cast<char*>(pool.conv) +
                                            a.layer * pool.conv_layer_stride +
@@ -830,13 +936,28 @@ __global__ void __launch_bounds__(NT, 1)
           if (last) store_elem(slot_c, off, pool.conv_dtype, wv);
         }
       }
+      umma::fence_smem_to_async();
+      umma::fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        if (full) tma_store_3d(&tmap_out, sb + OFF_OSTG, 0, h, static_cast<int>(row0));
+        if (store_state) {
+          constexpr int KB = ST == LIN_BF16 ? 64 : 32;  // key channels per tile
+          constexpr int NKB = DH / KB;
+          for (int tq = 0; tq < 4 * NKB; ++tq) {
+            const uint32_t src = sb + OFF_STG + tq * 4096;
+            const int v0 = (tq / NKB) * 32, k0 = (tq % NKB) * KB;
+            if (snap_dst >= 0) tma_store_4d(&tmap_state, src, k0, v0, h, snap_dst);
+            if (last) tma_store_4d(&tmap_state, src, k0, v0, h, slot);
+          }
+        }
+        bulk_commit();
+      }
     }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
   }
 
-  // ---- teardown
+  // ---- teardown: every TMA store issued here has completed before exit
+  if (tid == 0) bulk_wait_all();
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 0) umma::tmem_dealloc(tm, TMEM_COLS);
@@ -872,13 +993,44 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // state tiles: [slot][H][V][K] of this layer, box 32 rows x 128 bytes
+  CUtensorMap tmap_state;
+  {
+    const int es = ST == LIN_BF16 ? 2 : 4;
+    char* base = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride;
+    const cuuint64_t d[4] = {DH, DH, static_cast<cuuint64_t>(pool.num_heads),
+                             static_cast<cuuint64_t>(pool.num_slots)};
+    const cuuint64_t st[3] = {static_cast<cuuint64_t>(DH) * es, static_cast<cuuint64_t>(DH) * DH * es,
+                              static_cast<cuuint64_t>(pool.temporal_slot_stride)};
+    const cuuint32_t bx[4] = {static_cast<cuuint32_t>(128 / es), 32, 1, 1};
+    const cuuint32_t es4[4] = {1, 1, 1, 1};
+    cr = enc(&tmap_state, ST == LIN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             4, base, d, st, bx, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  // output tiles: [T][H][V], box 64 tokens x 1 head x 128
+  CUtensorMap tmap_out;
+  {
+    const int es = a.out_dtype == LIN_BF16 ? 2 : 4;
+    const cuuint64_t d[3] = {DH, static_cast<cuuint64_t>(pool.num_heads),
+                             static_cast<cuuint64_t>(a.total_tokens)};
+    const cuuint64_t st[2] = {static_cast<cuuint64_t>(DH) * es,
+                              static_cast<cuuint64_t>(DH) * pool.num_heads * es};
+    const cuuint32_t bx[3] = {DH, 1, CH};
+    const cuuint32_t es3[3] = {1, 1, 1};
+    cr = enc(&tmap_out, a.out_dtype == LIN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+             3, a.out, d, st, bx, es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   auto kern = chunked_prefill_kernel<KDA, ST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   ChunkParams p{pool, a};
   const unsigned grid = static_cast<unsigned>(a.batch) * static_cast<unsigned>(pool.num_heads);
-  kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, p);
+  kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_state, tmap_out, p);
   return cudaGetLastError();
 }
 
