@@ -95,7 +95,47 @@ constexpr uint32_t TMEM_COLS = 256;
 struct ChunkParams {
   lin_state_pool_t pool;
   lin_prefill_args_t a;
+  const int32_t* order;  // requests longest first (nullptr: batch order)
 };
+
+// Longest-first order of a varlen batch: the sequential chunk chain of the
+// longest request bounds the call, so its CTAs are dispatched first. One CTA
+// bitonic-sorts (length, index) keys in shared memory.
+constexpr int kOrderMax = 4096;
+
+__global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__ cu, int batch,
+                                                     int32_t* __restrict__ order) {
+  __shared__ uint64_t key[kOrderMax];
+  int n2 = 1;
+  while (n2 < batch) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    if (i < batch) {
+      const int64_t len = int64_t(cu[i + 1]) - int64_t(cu[i]);
+      const uint32_t l = len < 0 ? 0u : (len > 0x7fffffff ? 0x7fffffffu : static_cast<uint32_t>(len));
+      key[i] = (static_cast<uint64_t>(0x7fffffffu - l) << 32) | static_cast<uint32_t>(i);
+    } else {
+      key[i] = ~0ull;
+    }
+  }
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ix = i ^ jj;
+        if (ix > i) {
+          const uint64_t a = key[i], b = key[ix];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            key[i] = b;
+            key[ix] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < batch; i += blockDim.x) order[i] = static_cast<int32_t>(key[i] & 0xffffffffu);
+}
 
 __device__ __forceinline__ int head_channel(int cl, int h, int H) {
   const int part = cl >> 7, c = cl & 127;
@@ -271,7 +311,8 @@ __global__ void __launch_bounds__(NT, 1)
   const lin_state_pool_t& pool = p.pool;
   const lin_prefill_args_t& a = p.a;
   const int H = pool.num_heads;
-  const int r = blockIdx.x / H, h = blockIdx.x % H;
+  const int r = p.order ? p.order[blockIdx.x / H] : blockIdx.x / H;
+  const int h = blockIdx.x % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, slice = warp >> 2;  // four warps share each lane quarter
   const int vrow = quarter * 32 + lane;             // TMEM lane owned in the epilogues
@@ -980,7 +1021,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <bool KDA, int ST>
-cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, cudaStream_t s) {
+cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
+                     cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmap;
@@ -1028,7 +1070,12 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  ChunkParams p{pool, a};
+  if (order) {
+    order_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.batch, order);
+    cudaError_t e2 = cudaGetLastError();
+    if (e2 != cudaSuccess) return e2;
+  }
+  ChunkParams p{pool, a, order};
   const unsigned grid = static_cast<unsigned>(a.batch) * static_cast<unsigned>(pool.num_heads);
   kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_state, tmap_out, p);
   return cudaGetLastError();
@@ -1043,14 +1090,23 @@ bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_a
          (reinterpret_cast<uintptr_t>(a.g) & 15) == 0 && encode_fn() != nullptr;
 }
 
-size_t chunked_prefill_workspace(const lin_state_pool_t&, const lin_prefill_args_t&) { return 0; }
+// Workspace: the longest-first order of the batch (int32 per request) when
+// the batch has more than one request and fits the sorting kernel.
+size_t chunked_prefill_workspace(const lin_state_pool_t&, const lin_prefill_args_t& a) {
+  if (a.batch <= 1 || a.batch > kOrderMax) return 0;
+  return (static_cast<size_t>(a.batch) * sizeof(int32_t) + 255) & ~size_t(255);
+}
 
-cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a, void*,
-                                   size_t, cudaStream_t stream) {
+cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int32_t* order = nullptr;
+  if (chunked_prefill_workspace(pool, a) > 0 && workspace &&
+      workspace_bytes >= chunked_prefill_workspace(pool, a))
+    order = static_cast<int32_t*>(workspace);
   const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
   const bool bf = pool.state_dtype == LIN_BF16;
-  if (kda) return bf ? launch_t<true, LIN_BF16>(pool, a, stream) : launch_t<true, LIN_F32>(pool, a, stream);
-  return bf ? launch_t<false, LIN_BF16>(pool, a, stream) : launch_t<false, LIN_F32>(pool, a, stream);
+  if (kda) return bf ? launch_t<true, LIN_BF16>(pool, a, order, stream) : launch_t<true, LIN_F32>(pool, a, order, stream);
+  return bf ? launch_t<false, LIN_BF16>(pool, a, order, stream) : launch_t<false, LIN_F32>(pool, a, order, stream);
 }
 
 }  // namespace lin
