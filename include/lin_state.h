@@ -165,6 +165,22 @@ LIN_API size_t lin_state_prefill_workspace(const lin_state_pool_t* pool,
 LIN_API int lin_state_prefill(const lin_state_pool_t* pool, const lin_prefill_args_t* args,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Prefill that allocates nothing and takes no workspace. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory during a step: serving engines that give all device memory to their
+ * own pools at start-up (so an extra allocation fails or fragments it) and
+ * loops that must not pay the device-wide synchronisation of cudaMalloc /
+ * cudaFree. Same arguments and results as lin_state_prefill. Its scratch (the
+ * longest-first order of the batch) is a fixed array in the library's device
+ * memory, held by every GPU that loads the library until the process exits:
+ *   - batches above 4096 requests are rejected with LIN_EINVAL;
+ *   - the first call on a device looks up that array's device address (with
+ *     the device current), so make the first call before any stream capture;
+ *   - all calls share the array, so calls that overlap on the GPU (different
+ *     streams, no ordering between them) race on it. */
+LIN_API int lin_state_prefill_noalloc(const lin_state_pool_t* pool,
+                                      const lin_prefill_args_t* args, void* stream);
+
 /* ---- speculative per-step buffer ([MRC] 8.4) ----------------------------
  * temporal: [layers][max_batch][max_draft][H][V][K] in the pool's state
  * dtype; conv: [layers][max_batch][max_draft][C][3] in the pool's conv

@@ -30,7 +30,7 @@ LIN_ST_COPY_ALIAS, LIN_ST_TIMEOUT, LIN_ST_BAD_ACCEPT = 16, 32, 64
 LIN_KERNEL_RECURRENT, LIN_KERNEL_CHUNKED = 0, 1
 
 EXPORTED = (
-    "lin_state_prefill_kernel", "lin_state_prefill_workspace", "lin_state_prefill", "lin_state_decode",
+    "lin_state_prefill_kernel", "lin_state_prefill_workspace", "lin_state_prefill_noalloc", "lin_state_prefill", "lin_state_decode",
     "lin_state_spec_commit", "lin_state_copy_slots", "lin_state_restore",
     "lin_state_slot_bytes", "lin_state_read_status", "lin_state_strerror",
     "lin_state_last_error", "lin_state_version", "lin_state_selftest_mma",
@@ -118,6 +118,8 @@ def _load():
     lib.lin_state_prefill_workspace.restype = ctypes.c_size_t
     lib.lin_state_prefill.argtypes = [P(PoolT), P(PrefillArgsT), vp, ctypes.c_size_t, vp]
     lib.lin_state_prefill.restype = ctypes.c_int
+    lib.lin_state_prefill_noalloc.argtypes = [P(PoolT), P(PrefillArgsT), vp]
+    lib.lin_state_prefill_noalloc.restype = ctypes.c_int
     lib.lin_state_decode.argtypes = [P(PoolT), P(DecodeArgsT), vp]
     lib.lin_state_decode.restype = ctypes.c_int
     lib.lin_state_spec_commit.argtypes = [P(PoolT), P(CommitArgsT), vp]
@@ -300,6 +302,21 @@ def lin_state_prefill(pool: StatePool, *, layer: int, x, conv_w, g, beta, out, c
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.lin_state_prefill(ctypes.byref(pd), ctypes.byref(a), _ptr(workspace), nbytes,
                                  _stream(stream)), "lin_state_prefill")
+
+
+def lin_state_prefill_noalloc(pool: StatePool, *, layer: int, x, conv_w, g, beta, out,
+                              cu_seqlens, prefix_len, slot, has_initial_state, track_slots=None,
+                              cu_track=None, track_stride: int = 0,
+                              gate_mode: int = LIN_GATE_PER_KEY,
+                              flags: int = LIN_QK_L2NORM | LIN_CONV_SILU, q_scale: float = 1.0,
+                              status=None, stream=None) -> None:
+    """Calls lin_state_prefill_noalloc: the same prefill with no workspace and
+    no allocation (its scratch is a fixed array inside the library)."""
+    a = _prefill_args(layer, x, conv_w, g, beta, out, cu_seqlens, prefix_len, slot,
+                      has_initial_state, track_slots, cu_track, track_stride, gate_mode,
+                      flags, q_scale, status)
+    _check(lib.lin_state_prefill_noalloc(ctypes.byref(pool.desc()), ctypes.byref(a),
+                                         _stream(stream)), "lin_state_prefill_noalloc")
 
 
 def lin_state_decode(pool: StatePool, *, layer: int, x, conv_w, g, beta, out, slot, pos,

@@ -205,6 +205,19 @@ int lin_state_prefill(const lin_state_pool_t* pool, const lin_prefill_args_t* a,
   return ok();
 }
 
+int lin_state_prefill_noalloc(const lin_state_pool_t* pool, const lin_prefill_args_t* a,
+                              void* stream) {
+  int rc = check_prefill(pool, a);
+  if (rc) return rc;
+  if (a->batch > lin::noalloc_max_batch())
+    return fail(LIN_EINVAL, "prefill_noalloc: batch %d above the fixed scratch of %d requests",
+                a->batch, lin::noalloc_max_batch());
+  if (a->batch == 0) return ok();
+  cudaError_t e = lin::launch_prefill_noalloc(*pool, *a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lin_state_prefill_noalloc launch");
+  return ok();
+}
+
 int lin_state_decode(const lin_state_pool_t* pool, const lin_decode_args_t* a, void* stream) {
   int rc = check_pool(pool);
   if (rc) return rc;

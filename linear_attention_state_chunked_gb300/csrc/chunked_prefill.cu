@@ -36,6 +36,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "umma.cuh"
@@ -1107,6 +1109,42 @@ cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefi
   const bool bf = pool.state_dtype == LIN_BF16;
   if (kda) return bf ? launch_t<true, LIN_BF16>(pool, a, order, stream) : launch_t<true, LIN_F32>(pool, a, order, stream);
   return bf ? launch_t<false, LIN_BF16>(pool, a, order, stream) : launch_t<false, LIN_F32>(pool, a, order, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free prefill: the order scratch lives in a fixed device array of
+// this file instead of a caller workspace. Every GPU that loads the library
+// holds the array until exit. Calls share it, so calls that overlap on the GPU
+// race on it; each call rewrites every entry it reads (nothing needs clearing).
+// ---------------------------------------------------------------------------
+constexpr int kNoAllocMaxBatch = kOrderMax;  // 4096 requests
+static __device__ __align__(256) int32_t g_noalloc_order[kNoAllocMaxBatch];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int32_t*> g_noalloc_ptr[kMaxDevices];
+}  // namespace
+
+int noalloc_max_batch() { return kNoAllocMaxBatch; }
+
+cudaError_t launch_prefill_noalloc(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
+                                   cudaStream_t stream) {
+  if (!chunked_prefill_supported(pool, a) || (a.flags & LIN_PREFILL_RECURRENT))
+    return launch_prefill_recurrent(pool, a, stream);  // needs no scratch
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int32_t* ptr = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    // Set-up, once per device with that device current: in host code the
+    // array's name is only a stand-in, so its device address is looked up.
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_order);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev].store(ptr, std::memory_order_release);
+  }
+  const size_t need = chunked_prefill_workspace(pool, a);
+  return launch_prefill_chunked(pool, a, need ? ptr : nullptr, need, stream);
 }
 
 }  // namespace lin

@@ -34,6 +34,11 @@ cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefi
                                    void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
 
+// Prefill whose scratch is a fixed device array (chunked_prefill.cu).
+int noalloc_max_batch();
+cudaError_t launch_prefill_noalloc(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
+                                   cudaStream_t stream);
+
 // Tensor-core layout self-test (selftest.cu).
 cudaError_t launch_mma_selftest(const float* A, const float* B, float* D, int N, int K, int flags,
                                 int32_t* status, cudaStream_t stream);
