@@ -28,8 +28,8 @@
  *     nothing. Byte strides must be multiples of 16.
  *   - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).
  *     All calls only enqueue work on it; none synchronises, except
- *     lin_state_read_status. Index arrays live on the device, so every call
- *     can be captured in a CUDA graph.
+ *     lin_state_read_status. Index arrays live on the device and are never
+ *     copied to the host.
  *   - Errors: a call returns LIN_OK (0) or a negative LIN_E* code when a host
  *     check fails; on failure nothing is enqueued and lin_state_last_error()
  *     gives the reason (thread-local). Errors only a kernel can see (a slot id
