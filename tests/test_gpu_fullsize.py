@@ -1,0 +1,151 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times: the whole workload runs on the GPU, and sampled (request, head) slices
+are recomputed by the oracle. Heads are independent, so the oracle runs on the
+slice's own channels, gates and state rows."""
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import linear_attention_state_chunked_gb300 as L
+import workloads as W
+from oracle import lin_state_oracle as O
+from tests.helpers import TOL_BF16, TOL_F32, np64, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+FLAGS = O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU
+
+
+def head_channels(H, D, heads):
+    idx = []
+    for part in range(3):
+        for h in heads:
+            idx.extend(range(part * H * D + h * D, part * H * D + (h + 1) * D))
+    return np.array(idx)
+
+
+def oracle_slice_prefill(wl, req, heads, pool_before_t, pool_before_c):
+    """Run the oracle for one request on the given heads of a PrefillWorkload."""
+    b = wl.b
+    H, D = b.dims.num_heads, b.dims.head_k
+    ch = head_channels(H, D, heads)
+    a, e = int(b.cu_seqlens[req]), int(b.cu_seqlens[req + 1])
+    x = np64(b.x[a:e])[:, ch]
+    w = np64(b.conv_w)[ch]
+    g = np64(b.g[a:e])[:, heads]
+    beta = np64(b.beta[a:e])[:, heads]
+    slot = int(wl.slot[req])
+    cu_tr = wl.cu_track.cpu().tolist()
+    tracks = wl.track.cpu().tolist()[cu_tr[req]:cu_tr[req + 1]]
+    S = pool_before_t.shape[1]
+    sd = "bf16" if wl.pool.temporal.dtype == torch.bfloat16 else "f32"
+    pool = {"temporal": np.zeros((1, S, len(heads), D, D)), "conv": np.zeros((1, S, len(ch), 3)),
+            "state_dtype": sd, "conv_dtype": "bf16"}
+    pool["temporal"][0, slot] = np64(pool_before_t[0, slot][heads])
+    pool["conv"][0, slot] = np64(pool_before_c[0, slot][ch])
+    od = "bf16" if wl.out.dtype == torch.bfloat16 else "f32"
+    out, st = O.prefill(pool, 0, x, w, g, beta, [0, e - a], [int(b.prefix_len[req])], [slot],
+                        [int(b.has_initial_state[req])], tracks, [0, len(tracks)],
+                        wl.track_stride, b.gate_mode, FLAGS, 1.0, od)
+    assert st == 0
+    return out, pool, slot, tracks, (a, e), ch
+
+
+def check_prefill_slice(wl, req, heads, tol):
+    before_t = wl.pool.temporal.clone().cpu()
+    before_c = wl.pool.conv.clone().cpu()
+    wl.step(0)
+    torch.cuda.synchronize()
+    out, op, slot, tracks, (a, e), ch = oracle_slice_prefill(wl, req, heads, before_t, before_c)
+    got = np64(wl.out[a:e][:, heads])
+    for k in range(len(heads)):
+        assert rel_l2(got[:, k], out[:, k]) <= tol, (req, heads[k], rel_l2(got[:, k], out[:, k]))
+    for s in [slot] + [t for t in tracks if t >= 0]:
+        gt = np64(wl.pool.temporal[0, s][heads])
+        for k in range(len(heads)):
+            assert rel_l2(gt[k], op["temporal"][0, s, k]) <= tol, (s, heads[k])
+        assert np.array_equal(np64(wl.pool.conv[0, s])[ch], op["conv"][0, s])
+
+
+def test_qwen35_gdn_prefill_full_size_sampled():
+    wl = bench.make_workload("qwen35_gdn_prefill", L, DEV)
+    check_prefill_slice(wl, 5, [0, 31], TOL_F32)
+
+
+def test_kimi_k3_kda_varlen_full_size_sampled():
+    wl = bench.make_workload("kimi_k3_kda_varlen_prefill", L, DEV)
+    lens = (wl.b.cu_seqlens[1:] - wl.b.cu_seqlens[:-1]).cpu()
+    longest = int(torch.argmax(lens))
+    warm = [r for r in range(wl.B) if int(wl.b.has_initial_state[r])]
+    check_prefill_slice(wl, longest, [3, 11], TOL_BF16)
+    # a warm request on a fresh copy of the workload (the step above moved the pool on)
+    wl2 = bench.make_workload("kimi_k3_kda_varlen_prefill", L, DEV)
+    check_prefill_slice(wl2, warm[0], [0], TOL_BF16)
+
+
+def test_long_single_request_full_size_snapshots():
+    """131,072 tokens, 12 heads, snapshots every 64 into 2,048 distinct slots:
+    every snapshot's conv window equals the 3 inputs before its boundary (bit for
+    bit, so every snapshot sits in the right slot), and one head's outputs and
+    states at sampled boundaries match the oracle."""
+    wl = bench.make_workload("kda_long_prefill_131k", L, DEV)
+    before_t = wl.pool.temporal.clone().cpu()
+    before_c = wl.pool.conv.clone().cpu()
+    wl.step(0)
+    torch.cuda.synchronize()
+    b = wl.b
+    H, D = 12, 128
+    tracks = wl.track.cpu().tolist()
+    assert len(tracks) == 2048
+    conv = wl.pool.conv[0].cpu()
+    xs = b.x.cpu()
+    for i, s in enumerate(tracks):
+        bnd = 64 * (i + 1)
+        assert torch.equal(conv[s].view(torch.int16), xs[bnd - 3:bnd].T.contiguous().view(torch.int16))
+    out, op, slot, _, (a, e), ch = oracle_slice_prefill(wl, 0, [7], before_t, before_c)
+    got = np64(wl.out[:, 7])
+    assert rel_l2(got, out[:, 0]) <= TOL_BF16
+    for i in [0, 1, 1023, 2047]:
+        s = tracks[i]
+        assert rel_l2(np64(wl.pool.temporal[0, s, 7]), op["temporal"][0, s, 0]) <= TOL_BF16
+
+
+def test_kda_decode_full_size_sampled():
+    """The decode workload (2000-slot pools, 256 requests, track interval 256):
+    eight steps as bench.py runs them (rotating 4 pool replicas), then two
+    requests x two heads of replica 0 against the oracle."""
+    wl = bench.make_workload("kda_decode", L, DEV)
+    rep0_t = wl.pools[0].temporal.clone().cpu()
+    rep0_c = wl.pools[0].conv.clone().cpu()
+    outs = []
+    for i in range(8):
+        wl.step(i)
+        if i % 4 == 0:
+            outs.append(wl.out.clone())
+        torch.cuda.synchronize()
+    dims = W.KIMI_K3_TP8
+    heads = [2, 9]
+    ch = head_channels(12, 128, heads)
+    for req in [0, 200]:
+        slot = int(wl.slot[req])
+        ts = int(wl.track[req])
+        pool = {"temporal": np.zeros((1, 2000, 2, 128, 128)), "conv": np.zeros((1, 2000, len(ch), 3)),
+                "state_dtype": "bf16", "conv_dtype": "bf16"}
+        pool["temporal"][0, slot] = np64(rep0_t[0, slot][heads])
+        pool["conv"][0, slot] = np64(rep0_c[0, slot][ch])
+        for n, i in enumerate([0, 4]):
+            x, g, beta = wl.inputs[i % len(wl.inputs)]
+            pos = int(wl.pos0[req]) + i // 4
+            o, st = O.decode(pool, 0, np64(x[req:req + 1])[:, :, ch], np64(wl.conv_w)[ch],
+                             np64(g[req:req + 1])[:, :, heads], np64(beta[req:req + 1])[:, :, heads],
+                             [slot], [pos], [ts], 256, O.GATE_PER_KEY, FLAGS, 1.0, "bf16")
+            assert st == 0
+            got = np64(outs[n][req][:, heads])
+            for k in range(2):
+                assert rel_l2(got[0, k], o[0, 0, k]) <= TOL_BF16
+        gt = np64(wl.pools[0].temporal[0, slot][heads])
+        for k in range(2):
+            assert rel_l2(gt[k], pool["temporal"][0, slot, k]) <= TOL_BF16
+        assert np.array_equal(np64(wl.pools[0].conv[0, slot])[ch], pool["conv"][0, slot])
