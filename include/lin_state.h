@@ -210,7 +210,13 @@ typedef struct {
  * Inputs (device): x [batch][n_draft][C] io_dtype, g [batch][n_draft][H]
  * or [..][H][K] fp32, beta [batch][n_draft][H] fp32, out
  * [batch][n_draft][H][V] out_dtype; slot, pos [batch] int32; track_slot
- * [batch] int32 or NULL. Live slots must be distinct within the batch. */
+ * [batch] int32 or NULL. Live slots must be distinct within the batch.
+ * x, conv_w, g and out move by bulk async copies and must be 16-byte
+ * aligned (LIN_EINVAL otherwise).
+ * One (request, head) stages its state block, conv window, taps and n_draft
+ * x (and per-key g) rows in shared memory; past 110 KB of staging the call
+ * returns LIN_EUNSUPPORTED (head 128, fp32 state, conv and io, per-key
+ * gates: n_draft <= 17). */
 typedef struct {
   int32_t layer;
   int32_t batch;

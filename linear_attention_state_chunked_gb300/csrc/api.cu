@@ -234,10 +234,15 @@ int lin_state_decode(const lin_state_pool_t* pool, const lin_decode_args_t* a, v
   if (a->batch == 0) return ok();
   if (!a->x || !a->conv_w || !a->g || !a->beta || !a->out || !a->slot || !a->pos)
     return fail(LIN_EINVAL, "decode: x / conv_w / g / beta / out / slot / pos is NULL");
+  if (!aligned16(a->x) || !aligned16(a->conv_w) || !aligned16(a->g) || !aligned16(a->out))
+    return fail(LIN_EINVAL, "decode: x, conv_w, g and out must be 16-byte aligned");
   if (a->n_draft > 1) {
     rc = check_spec(pool, a->spec, a->batch, a->n_draft, a->layer + 1);
     if (rc) return rc;
   }
+  if (lin::decode_stage_bytes(*pool, *a) > lin::kDecodeMaxStage)
+    return fail(LIN_EUNSUPPORTED, "decode: n_draft %d stages %d bytes per (request, head), over %d",
+                a->n_draft, lin::decode_stage_bytes(*pool, *a), lin::kDecodeMaxStage);
   cudaError_t e = lin::launch_decode(*pool, *a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lin_state_decode launch");
   return ok();

@@ -70,9 +70,10 @@ struct Vec8<LIN_BF16> {
   static __device__ __forceinline__ void store(void* p, const float (&v)[8]) {
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(v[2 * i])) |
-             (static_cast<uint32_t>(f32_to_bf16_bits(v[2 * i + 1])) << 16);
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);  // .x = low half
+      w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
     *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   static __device__ __forceinline__ void round(float (&v)[8]) {

@@ -22,6 +22,10 @@ cudaError_t launch_spec_commit(const lin_state_pool_t& pool, const lin_commit_ar
                                cudaStream_t stream);
 
 // Token-by-token kernels (token_kernels.cu).
+// Bytes one decode item stages in shared memory (state block, conv window,
+// taps, n_draft x rows and per-key g rows, 128-aligned); the kernel holds two.
+int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a);
+constexpr int kDecodeMaxStage = 110 * 1024;
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,

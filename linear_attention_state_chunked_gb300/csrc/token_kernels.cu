@@ -181,12 +181,13 @@ __device__ __forceinline__ void load_rows(const char* base, float (&s)[TokCfg<D>
     Vec8<ST>::load(base + (int64_t(row0 + i * C::RSTEP) * D + lr * 8) * ES, s[i]);
 }
 
-template <int CPT, int D>
+// NS: threads that share the channels (0: the whole block).
+template <int CPT, int D, int NS = 0>
 __device__ __forceinline__ void store_window(void* conv_base, int conv_dtype, const int (&chan)[CPT],
                                              const float (&win)[CPT][3]) {
 #pragma unroll
   for (int i = 0; i < CPT; ++i) {
-    const int cl = threadIdx.x + i * blockDim.x;
+    const int cl = threadIdx.x + i * (NS ? NS : static_cast<int>(blockDim.x));
     if (cl < 3 * D) {
 #pragma unroll
       for (int j = 0; j < 3; ++j) store_elem(conv_base, int64_t(chan[i]) * 3 + j, conv_dtype, win[i][j]);
@@ -195,13 +196,13 @@ __device__ __forceinline__ void store_window(void* conv_base, int conv_dtype, co
 }
 
 // ---------------------------------------------------------------------------
-// Decode / verify. One CTA per (request, head). Everything the head needs --
-// its state block, the conv window and taps of its q|k|v channels, and the
-// step's x (and per-key g) rows -- is staged into shared memory by bulk async
-// copies on one mbarrier, issued before any other work, so loads in flight
-// cost no registers and the CTA stays small. Each thread then updates its
-// rows from shared memory (8 key channels per lane, D/8 lanes per row) and
-// writes them straight to their destinations.
+// Decode / verify. The unit of work is one (request, head) item. Everything
+// an item needs -- its state block, the conv window and taps of its q|k|v
+// channels, and the step's x (and per-key g) rows -- is staged into shared
+// memory by bulk async copies completing on one mbarrier, so loads in flight
+// cost no registers. Each thread then updates its rows from shared memory
+// (8 key channels per lane, D/8 lanes per row) and writes them straight to
+// their destinations.
 // ---------------------------------------------------------------------------
 struct DecodeParams {
   lin_state_pool_t pool;
@@ -210,27 +211,17 @@ struct DecodeParams {
 
 constexpr uint32_t kDecWaitTries = 1u << 24;
 
-template <int D>
-struct DecCfg {
-  static constexpr int LPR = D / 8;
-  static constexpr int NT = (D * LPR) < 128 ? ((D * LPR) < 32 ? 32 : D * LPR) : 128;
-  static constexpr int RSTEP = NT / LPR;
-  static constexpr int RPT = D / RSTEP;
-  static constexpr int CH = 3 * D;
-  static constexpr int CPT = (CH + NT - 1) / NT;
-  static_assert(RPT * RSTEP == D, "rows");
-};
-
-// Shared-memory layout of one decode CTA (byte offsets; every piece 16-aligned).
+// Shared-memory layout of one decode stage (byte offsets; every piece
+// 16-aligned); the producer's bulk loads fill all of it.
 struct DecSmem {
-  int state, conv, w, x, g, total;
+  int state, conv, w, x, g, load;
   __host__ __device__ DecSmem(int D, int es_state, int es_conv, int es_io, int nd, bool per_key) {
     state = 0;
     conv = state + D * D * es_state;
     w = conv + 3 * D * 3 * es_conv;
     x = w + 3 * D * 4 * es_io;
     g = x + nd * 3 * D * es_io;
-    total = g + (per_key ? nd * D * 4 : 0);
+    load = g + (per_key ? nd * D * 4 : 0);
   }
 };
 
@@ -241,210 +232,401 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Warp-specialised persistent form. Each CTA walks the (request, head) items
+// i = blockIdx.x, blockIdx.x + gridDim.x, ... through a ring of `stages`
+// shared-memory buffers (two CTAs share an SM). One producer warp looks up each
+// item's slot, writes the item's metadata and issues the stage's bulk loads,
+// up to `stages` items ahead. The NC consumer threads (8 warps at head 128)
+// wait for a stage warp by warp, so a warp that is done with one item starts
+// the conv of the next while others still update rows; the only CTA-wide
+// barrier is the one per token that publishes the conv outputs. Each warp
+// hands the stage back as soon as its own reads of it are done.
+//
+// Row arithmetic: with A = Diag(alpha), the output needs no second pass over
+// the updated row, since  o_r = sum_c S'[r,c] q_c = (S A q)_r + u_r (k . q):
+// the two reductions (S A k)_r and (S A q)_r of up to four of a thread's rows
+// are summed across the row's lanes together by a transposing butterfly (each
+// exchange halves the values a lane still carries), then each row's u_r is
+// taken from the lane that ends up holding (S A k)_r.
+template <int D>
+struct DecPCfg {
+  static constexpr int LPR = D / 8;  // lanes per row, 8 key channels each
+  static constexpr int NC = (D * LPR) < 256 ? ((D * LPR) < 32 ? 32 : D * LPR) : 256;
+  static constexpr int NCW = NC / 32;   // consumer warps
+  static constexpr int NT = NC + 32;    // + one producer warp
+  static constexpr int RSTEP = NC / LPR;
+  static constexpr int RPT = D / RSTEP;        // rows per consumer thread
+  static constexpr int RB = RPT < 4 ? RPT : 4;  // rows reduced together
+  static constexpr int NV = 2 * RB;             // values reduced per lane group
+  static_assert(RPT * RSTEP == D && RPT % RB == 0, "rows");
+  static_assert(NV <= LPR, "one reduced value per lane");
+  static_assert(2 * D <= NC, "conv and gate threads");
+};
+
+constexpr int kDecMaxStages = 4;
+
+struct DecMeta {
+  int r, h, slot, ts, pos, valid;
+};
+
+__device__ __forceinline__ bool mbar_try(uint32_t sb, uint32_t par) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(sb), "r"(par)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t sb, uint32_t par) {
+  for (uint32_t it = 0; it < kDecWaitTries; ++it)
+    if (mbar_try(sb, par)) return true;
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t sb) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sb) : "memory");
+}
+// Named barrier over the consumer threads that also ORs a predicate across them.
+__device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(res)
+      : "r"(pred ? 1u : 0u), "r"(nthreads)
+      : "memory");
+  return res != 0;
+}
+
 template <int D, int ST>
-__global__ void __launch_bounds__(DecCfg<D>::NT) decode_kernel(DecodeParams p) {
-  using C = DecCfg<D>;
+__global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
+    decode_kernel(DecodeParams p, int n_items, int stage_bytes, int stages) {
+  using C = DecPCfg<D>;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
-  extern __shared__ __align__(16) uint8_t dsm[];
-  __shared__ float ysm[2][3 * D + 2];
-  __shared__ uint64_t bar;
-  __shared__ int abort_sh;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ float ysm[2][3 * D];                      // post-conv q | k | v, by token parity
+  __shared__ float agsm[2][D];                         // per-key decay factors
+  __shared__ float normsm[2][D < 32 ? 1 : D / 32][3];  // q.q, k.k, q.k partials per conv warp
+  __shared__ uint64_t full[kDecMaxStages], empty[kDecMaxStages];
+  __shared__ DecMeta meta[kDecMaxStages];
   const lin_state_pool_t& pool = p.pool;
   const lin_decode_args_t& a = p.a;
-  const int r = blockIdx.x, h = blockIdx.y;
   const int H = pool.num_heads;
-  const int ns = pool.num_slots;
-  const int slot = a.slot[r];
-  if (slot < 0) return;
-  const bool rep = (h == 0 && threadIdx.x == 0);
-  if (slot >= ns) {
-    if (rep) report(a.status, LIN_ST_BAD_SLOT);
-    return;
-  }
-  const int ts = a.track_slot ? a.track_slot[r] : -1;
-  if (ts >= ns) {
-    if (rep) report(a.status, LIN_ST_BAD_SLOT);
-    return;
-  }
-  if (ts == slot) {
-    if (rep) report(a.status, LIN_ST_TRACK_ALIAS);
-    return;
-  }
   const int ND = a.n_draft;
   const bool per_key = a.gate_mode == LIN_GATE_PER_KEY;
   const int esc = pool.conv_dtype == LIN_BF16 ? 2 : 4;
   const int esi = a.io_dtype == LIN_BF16 ? 2 : 4;
   const DecSmem L(D, ES, esc, esi, ND, per_key);
   const int64_t head_bytes = int64_t(D) * D * ES;
-  char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
-                 slot * pool.temporal_slot_stride + h * head_bytes;
-  char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
-                 slot * pool.conv_slot_stride;
   const int C_all = pool.conv_channels;
-  const uint32_t s0 = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
-  const uint32_t sbar = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&full[s])); };
+  auto empty_bar = [&](int s) { return static_cast<uint32_t>(__cvta_generic_to_shared(&empty[s])); };
+
   if (threadIdx.x == 0) {
-    abort_sh = 0;
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sbar) : "memory");
+    for (int s = 0; s < stages; ++s) {
+      meta[s].valid = 0;
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full_bar(s)) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty_bar(s)), "r"(C::NCW) : "memory");
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sbar),
-                 "r"(static_cast<uint32_t>(L.total))
-                 : "memory");
-    bulk_g2s(s0 + L.state, slot_t, D * D * ES, sbar);
-    for (int part = 0; part < 3; ++part) {
-      const int64_t ch0 = int64_t(part) * H * D + int64_t(h) * D;  // first channel of the part
-      bulk_g2s(s0 + L.conv + part * D * 3 * esc, static_cast<const char*>(slot_c) + ch0 * 3 * esc,
-               D * 3 * esc, sbar);
-      bulk_g2s(s0 + L.w + part * D * 4 * esi, static_cast<const char*>(a.conv_w) + ch0 * 4 * esi,
-               D * 4 * esi, sbar);
-      for (int j = 0; j < ND; ++j) {
-        const int64_t tok = int64_t(r) * ND + j;
-        bulk_g2s(s0 + L.x + (j * 3 + part) * D * esi,
-                 static_cast<const char*>(a.x) + (tok * C_all + ch0) * esi, D * esi, sbar);
-      }
-    }
-    if (per_key)
-      for (int j = 0; j < ND; ++j) {
-        const int64_t tok = int64_t(r) * ND + j;
-        bulk_g2s(s0 + L.g + j * D * 4, a.g + (tok * H + h) * D, D * 4, sbar);
-      }
-    bool ok = false;
-    for (uint32_t it = 0; it < kDecWaitTries && !ok; ++it) {
-      uint32_t done;
-      asm volatile(
-          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
-          "selp.u32 %0, 1, 0, p;\n\t}"
-          : "=r"(done)
-          : "r"(sbar)
-          : "memory");
-      ok = done != 0;
-    }
-    if (!ok) {
-      abort_sh = 1;
-      report(a.status, LIN_ST_TIMEOUT);
-    }
   }
   __syncthreads();
-  if (abort_sh) return;  // the copies were given up on; nothing is written
 
-  const uint8_t* sconv = dsm + L.conv;
-  const uint8_t* sw = dsm + L.w;
-  // conv channels: local cl in [0, 3D), part = cl / D
-  int chan[C::CPT];
-  float win[C::CPT][3], w[C::CPT][4];
+  if (warp == C::NCW) {
+    // ---------------- producer warp ----------------
+    int issued_n[kDecMaxStages];
 #pragma unroll
-  for (int i = 0; i < C::CPT; ++i) {
-    const int cl = threadIdx.x + i * C::NT;
-    chan[i] = cl < C::CH ? head_channel(cl, h, H, D) : 0;
-    if (cl < C::CH) {
-#pragma unroll
-      for (int q = 0; q < 3; ++q) win[i][q] = load_elem(sconv, cl * 3 + q, pool.conv_dtype);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) w[i][q] = load_elem(sw, cl * 4 + q, a.io_dtype);
+    for (int s = 0; s < kDecMaxStages; ++s) issued_n[s] = -1;
+    int n = 0;
+    bool abort = false;
+    for (int base = blockIdx.x; base < n_items && !abort; base += 32 * gridDim.x) {
+      // lane l looks up item base + l * gridDim.x, so 32 lookups overlap
+      const int item = base + lane * gridDim.x;
+      DecMeta m{0, 0, -1, -1, 0, 0};
+      if (item < n_items) {
+        m.r = item / H;
+        m.h = item % H;
+        m.slot = a.slot[m.r];
+        m.ts = a.track_slot ? a.track_slot[m.r] : -1;
+        m.pos = ND == 1 ? a.pos[m.r] : 0;
+        if (m.slot >= 0) {
+          if (m.slot >= pool.num_slots || m.ts >= pool.num_slots) {
+            if (m.h == 0) report(a.status, LIN_ST_BAD_SLOT);
+          } else if (m.ts == m.slot) {
+            if (m.h == 0) report(a.status, LIN_ST_TRACK_ALIAS);
+          } else {
+            m.valid = 1;
+          }
+        }
+      }
+      const int left = (n_items - base + gridDim.x - 1) / gridDim.x;
+      const int cnt = left < 32 ? left : 32;
+      for (int j = 0; j < cnt; ++j, ++n) {
+        DecMeta mj;
+        mj.r = __shfl_sync(0xffffffffu, m.r, j);
+        mj.h = __shfl_sync(0xffffffffu, m.h, j);
+        mj.slot = __shfl_sync(0xffffffffu, m.slot, j);
+        mj.ts = __shfl_sync(0xffffffffu, m.ts, j);
+        mj.pos = __shfl_sync(0xffffffffu, m.pos, j);
+        mj.valid = __shfl_sync(0xffffffffu, m.valid, j);
+        const int s = n % stages;
+        if (lane == 0) {
+          if (n >= stages && !mbar_wait_bounded(empty_bar(s), ((n / stages) - 1) & 1)) {
+            report(a.status, LIN_ST_TIMEOUT);
+            abort = true;
+          } else {
+            meta[s] = mj;
+            if (mj.valid) {
+              const uint32_t sf = full_bar(s);
+              const uint32_t s0 = s_base + s * stage_bytes;
+              const char* st = static_cast<const char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                               mj.slot * pool.temporal_slot_stride + mj.h * head_bytes;
+              const char* sc = static_cast<const char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                               mj.slot * pool.conv_slot_stride;
+              asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sf),
+                           "r"(static_cast<uint32_t>(L.load))
+                           : "memory");
+              bulk_g2s(s0 + L.state, st, D * D * ES, sf);
+              for (int part = 0; part < 3; ++part) {
+                const int64_t ch0 = int64_t(part) * H * D + int64_t(mj.h) * D;
+                bulk_g2s(s0 + L.conv + part * D * 3 * esc, sc + ch0 * 3 * esc, D * 3 * esc, sf);
+                bulk_g2s(s0 + L.w + part * D * 4 * esi, static_cast<const char*>(a.conv_w) + ch0 * 4 * esi,
+                         D * 4 * esi, sf);
+                for (int t = 0; t < ND; ++t) {
+                  const int64_t tok = int64_t(mj.r) * ND + t;
+                  bulk_g2s(s0 + L.x + (t * 3 + part) * D * esi,
+                           static_cast<const char*>(a.x) + (tok * C_all + ch0) * esi, D * esi, sf);
+                }
+              }
+              if (per_key)
+                for (int t = 0; t < ND; ++t) {
+                  const int64_t tok = int64_t(mj.r) * ND + t;
+                  bulk_g2s(s0 + L.g + t * D * 4, a.g + (tok * H + mj.h) * D, D * 4, sf);
+                }
+            } else {
+              mbar_arrive(full_bar(s));
+            }
+            issued_n[s] = n;
+          }
+        }
+        abort = __shfl_sync(0xffffffffu, abort, 0);
+        if (abort) break;
+      }
     }
+    // no bulk copy may still be landing in shared memory when the CTA exits
+    if (lane == 0)
+      for (int s = 0; s < stages; ++s)
+        if (issued_n[s] >= 0) mbar_wait_bounded(full_bar(s), (issued_n[s] / stages) & 1);
+    return;
   }
+
+  // ---------------- consumer warps ----------------
+  // Thread t < D runs the conv of key channel t of q, k and v (local channels
+  // t, D + t, 2D + t); threads D..2D-1 turn the per-key gates into decay
+  // factors meanwhile.
   const bool silu_on = a.flags & LIN_CONV_SILU;
-  const int lr = threadIdx.x % C::LPR, row0 = threadIdx.x / C::LPR;
-  for (int j = 0; j < ND; ++j) {
-    float* ys = ysm[j & 1];
-    const int64_t tok = int64_t(r) * ND + j;
-    const uint8_t* sx = dsm + L.x + j * 3 * D * esi;
+  const bool l2 = a.flags & LIN_QK_L2NORM;
+  const int t = threadIdx.x;
+  const int lr = lane % C::LPR;           // lane within the row group
+  const int gbase = lane - lr;            // first lane of the row group
+  const int row0 = t / C::LPR;            // first row of this thread
+  constexpr int VSTEP = C::LPR / C::NV;   // lanes per reduced value
+  constexpr int NPW = D < 32 ? 1 : D / 32;  // warps holding conv channels
+  const int my_v = lr / VSTEP;            // value this lane ends up holding
+  int tc = 0;                             // tokens done (parity of the scratch)
+  int n = 0;
+  bool abort = false;
+  for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x, ++n) {
+    const int s = n % stages;
+    // each warp waits for the stage itself
+    bool got = true;
+    if (lane == 0) got = mbar_wait_bounded(full_bar(s), (n / stages) & 1);
+    got = __shfl_sync(0xffffffffu, got, 0);
+    DecMeta m = meta[s];
+    if (!got) m.valid = 0;
+    uint8_t* buf = dsm + s * stage_bytes;
+    char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                   int64_t(m.slot) * pool.temporal_slot_stride + m.h * head_bytes;
+    char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                   int64_t(m.slot) * pool.conv_slot_stride;
+    // every item runs ND token steps (with no work when it is empty), so all
+    // consumers meet the same number of barriers whatever they saw
+    for (int j = 0; j < ND; ++j, ++tc) {
+      float* ys = ysm[tc & 1];
+      const int64_t tok = int64_t(m.r) * ND + j;
+      float beta = 0.f, gh = 0.f;
+      char* dt = nullptr;
+      char* dc = nullptr;
+      char* tt = nullptr;
+      char* tcv = nullptr;
+      float pqq = 0.f, pkk = 0.f, pqk = 0.f;
+      if (m.valid) {
+        beta = a.beta[tok * H + m.h];
+        if (!per_key) gh = a.g[tok * H + m.h];
+        if (ND == 1) {
+          dt = slot_t;
+          dc = slot_c;
+          if (m.ts >= 0 && a.track_interval > 0 && (m.pos + 1) % a.track_interval == 0) {
+            tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                 int64_t(m.ts) * pool.temporal_slot_stride + m.h * head_bytes;
+            tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                  int64_t(m.ts) * pool.conv_slot_stride;
+          }
+        } else {
+          dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
+               m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
+          dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
+               m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
+        }
+        if (t < D) {
+          const uint8_t* sx = buf + L.x + j * 3 * D * esi;
+          float y3[3];
 #pragma unroll
-    for (int i = 0; i < C::CPT; ++i) {
-      const int cl = threadIdx.x + i * C::NT;
-      if (cl < C::CH) {
-        const float xin = load_elem(sx, cl, a.io_dtype);
-        float y = w[i][0] * win[i][0] + w[i][1] * win[i][1] + w[i][2] * win[i][2] + w[i][3] * xin;
-        win[i][0] = win[i][1];
-        win[i][1] = win[i][2];
-        win[i][2] = xin;
+          for (int pt = 0; pt < 3; ++pt) {
+            const int cl = pt * D + t;
+            float win[3], w[4];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) win[i][q] = round_to_dtype(win[i][q], pool.conv_dtype);
-        ys[cl] = silu_on ? silu(y) : y;
+            for (int q = 0; q < 3; ++q) win[q] = load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = load_elem(buf + L.w, cl * 4 + q, a.io_dtype);
+            const float xin = load_elem(sx, cl, a.io_dtype);
+            const float y = w[0] * win[0] + w[1] * win[1] + w[2] * win[2] + w[3] * xin;
+            const float nw[3] = {win[1], win[2], round_to_dtype(xin, pool.conv_dtype)};
+            const int64_t ch = int64_t(pt) * H * D + int64_t(m.h) * D + t;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+              if (ND > 1) store_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype, nw[q]);  // next draft's window
+              store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
+              if (tcv) store_elem(tcv, ch * 3 + q, pool.conv_dtype, nw[q]);
+            }
+            y3[pt] = silu_on ? silu(y) : y;
+            ys[cl] = y3[pt];
+          }
+          pqq = y3[0] * y3[0];
+          pkk = y3[1] * y3[1];
+          pqk = y3[0] * y3[1];
+        } else if (per_key && t < 2 * D) {
+          const float* sg = reinterpret_cast<const float*>(buf + L.g) + j * D;
+          agsm[tc & 1][t - D] = expf(sg[t - D]);
+        }
+        if (warp < NPW) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            pqq += __shfl_xor_sync(0xffffffffu, pqq, o);
+            pkk += __shfl_xor_sync(0xffffffffu, pkk, o);
+            pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+          }
+          if (lane == 0) {
+            normsm[tc & 1][warp][0] = pqq;
+            normsm[tc & 1][warp][1] = pkk;
+            normsm[tc & 1][warp][2] = pqk;
+          }
+        }
       }
-    }
-    __syncthreads();
-    {
-      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-      constexpr int NWp = C::NT / 32;
-      for (int part = (NWp >= 2 ? warp : 0); part < 2; part += (NWp >= 2 ? 2 : 1)) {
-        if (NWp >= 2 && warp >= 2) break;
-        float ss = 0.f;
-        for (int i = lane; i < D; i += 32) ss += ys[part * D + i] * ys[part * D + i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) ys[3 * D + part] = (a.flags & LIN_QK_L2NORM) ? rsqrtf(ss + kL2Eps) : 1.f;
+      // conv outputs published; also agrees on whether any consumer's wait gave up
+      if (consumers_sync_or(C::NC, !got)) {
+        abort = true;
+        break;
       }
-    }
-    __syncthreads();
-    float a8[8];
-    if (per_key) {
-      const float* sg = reinterpret_cast<const float*>(dsm + L.g) + j * D + lr * 8;
+      if (!m.valid) continue;
+      float sqq = 0.f, skk = 0.f, sqk = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) a8[e] = expf(sg[e]);
-    } else {
-      const float av = expf(a.g[tok * H + h]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) a8[e] = av;
-    }
-    const float beta = a.beta[tok * H + h];
-    const float rq = ys[3 * D] * a.q_scale, rk = ys[3 * D + 1];
-    float q8[8], k8[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      q8[e] = ys[lr * 8 + e] * rq;
-      k8[e] = ys[D + lr * 8 + e] * rk;
-    }
-    char* dt;
-    char* dc;
-    char* tt = nullptr;
-    char* tc = nullptr;
-    if (ND == 1) {
-      dt = slot_t;
-      dc = slot_c;
-      const int n = a.pos[r] + 1;
-      if (ts >= 0 && a.track_interval > 0 && n % a.track_interval == 0) {
-        tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
-             ts * pool.temporal_slot_stride + h * head_bytes;
-        tc = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
-             ts * pool.conv_slot_stride;
+      for (int pw = 0; pw < NPW; ++pw) {
+        sqq += normsm[tc & 1][pw][0];
+        skk += normsm[tc & 1][pw][1];
+        sqk += normsm[tc & 1][pw][2];
       }
-    } else {
-      dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
-           r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + h * head_bytes;
-      dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
-           r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
-    }
-    uint8_t* sst = dsm + L.state;
-#pragma unroll 4
-    for (int i = 0; i < C::RPT; ++i) {
-      const int row = row0 + i * C::RSTEP;
-      const int64_t off = (int64_t(row) * D + lr * 8) * ES;
-      float sv[8];
-      Vec8<ST>::load(sst + off, sv);
-      float dot = 0.f;
+      const float rq = (l2 ? rsqrtf(sqq + kL2Eps) : 1.f) * a.q_scale;
+      const float rk = l2 ? rsqrtf(skk + kL2Eps) : 1.f;
+      const float kq = sqk * rq * rk;
+      float a8[8], q8[8], k8[8];
+      if (per_key) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a8[e] = agsm[tc & 1][lr * 8 + e];
+      } else {
+        const float av = expf(gh);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a8[e] = av;
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        sv[e] *= a8[e];
-        dot = fmaf(sv[e], k8[e], dot);
+        q8[e] = ys[lr * 8 + e] * rq;
+        k8[e] = ys[D + lr * 8 + e] * rk;
       }
-      dot = row_sum<C::LPR>(dot);
-      const float u = beta * (ys[2 * D + row] - dot);
-      float o = 0.f;
+      uint8_t* sst = buf + L.state;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sv[e] = fmaf(u, k8[e], sv[e]);
-        o = fmaf(sv[e], q8[e], o);
+      for (int rb = 0; rb < C::RPT; rb += C::RB) {
+        float sv[C::RB][8];
+        float red[C::NV];
+#pragma unroll
+        for (int i = 0; i < C::RB; ++i) {
+          const int row = row0 + (rb + i) * C::RSTEP;
+          Vec8<ST>::load(sst + (int64_t(row) * D + lr * 8) * ES, sv[i]);
+          float dk = 0.f, dq = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sv[i][e] *= a8[e];
+            dk = fmaf(sv[i][e], k8[e], dk);
+            dq = fmaf(sv[i][e], q8[e], dq);
+          }
+          red[2 * i] = dk;
+          red[2 * i + 1] = dq;
+        }
+        // transposing butterfly: after the exchange at distance d the lane
+        // keeps the half of its values selected by (lr & d)
+#pragma unroll
+        for (int d = C::LPR / 2, nv = C::NV; d > 0; d >>= 1) {
+          if (nv > 1) {
+            const bool up = lr & d;
+            nv >>= 1;
+#pragma unroll
+            for (int v = 0; v < C::NV / 2; ++v) {
+              if (v < nv) {
+                const float keep = up ? red[v + nv] : red[v];
+                const float send = up ? red[v] : red[v + nv];
+                red[v] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+              }
+            }
+          } else {
+            red[0] += __shfl_xor_sync(0xffffffffu, red[0], d);
+          }
+        }
+        float u[C::RB];
+#pragma unroll
+        for (int i = 0; i < C::RB; ++i) {
+          const float dk = __shfl_sync(0xffffffffu, red[0], gbase + (2 * i) * VSTEP);
+          u[i] = beta * (ys[2 * D + row0 + (rb + i) * C::RSTEP] - dk);
+        }
+        if ((my_v & 1) && (lr % VSTEP) == 0) {
+          float ui = 0.f;
+#pragma unroll
+          for (int i = 0; i < C::RB; ++i)
+            if (i == (my_v >> 1)) ui = u[i];
+          const int row = row0 + (rb + (my_v >> 1)) * C::RSTEP;
+          store_elem(a.out, (tok * H + m.h) * D + row, a.out_dtype, fmaf(ui, kq, red[0]));
+        }
+#pragma unroll
+        for (int i = 0; i < C::RB; ++i) {
+          const int64_t off = (int64_t(row0 + (rb + i) * C::RSTEP) * D + lr * 8) * ES;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sv[i][e] = fmaf(u[i], k8[e], sv[i][e]);
+          Vec8<ST>::store(dt + off, sv[i]);
+          if (tt) Vec8<ST>::store(tt + off, sv[i]);
+          if (ND > 1) {
+            Vec8<ST>::round(sv[i]);  // the next draft starts from the stored state
+            Vec8<ST>::store(sst + off, sv[i]);
+          }
+        }
       }
-      o = row_sum<C::LPR>(o);
-      if (lr == 0) store_elem(a.out, (tok * H + h) * D + row, a.out_dtype, o);
-      Vec8<ST>::round(sv);  // the stored state is what the next token starts from
-      Vec8<ST>::store(dt + off, sv);
-      if (tt) Vec8<ST>::store(tt + off, sv);
-      if (ND > 1) Vec8<ST>::store(sst + off, sv);
     }
-    store_window<DecCfg<D>::CPT, D>(dc, pool.conv_dtype, chan, win);
-    if (tc) store_window<DecCfg<D>::CPT, D>(tc, pool.conv_dtype, chan, win);
+    if (abort) break;
+    // this warp's reads (and, in verify, writes) of the stage are done
+    __syncwarp();
+    if (ND > 1) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive(empty_bar(s));
   }
 }
 
@@ -565,13 +747,25 @@ template <int D, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           cudaStream_t stream) {
   DecodeParams p{pool, a};
-  const DecSmem L(D, ST == LIN_BF16 ? 2 : 4, dtype_size(pool.conv_dtype), dtype_size(a.io_dtype),
-                  a.n_draft, a.gate_mode == LIN_GATE_PER_KEY);
-  if (L.total > 200 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, ST>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  const int stage = decode_stage_bytes(pool, a);
+  if (stage > kDecodeMaxStage) return cudaErrorInvalidValue;
+  // two CTAs per SM when two stages each fit, else one CTA with two stages
+  int stages = (100 * 1024) / stage;
+  if (stages > kDecMaxStages) stages = kDecMaxStages;
+  if (stages < 2) stages = 2;
+  const int smem = stages * stage;
+  auto kern = decode_kernel<D, ST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, ST><<<dim3(a.batch, pool.num_heads), DecCfg<D>::NT, L.total, stream>>>(p);
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DecPCfg<D>::NT, smem)) != cudaSuccess)
+    return e;
+  const int items = a.batch * pool.num_heads;
+  int grid = sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > items) grid = items;
+  kern<<<grid, DecPCfg<D>::NT, smem, stream>>>(p, items, stage, stages);
   return cudaGetLastError();
 }
 
@@ -596,6 +790,12 @@ cudaError_t prefill_launch(const lin_state_pool_t& pool, const lin_prefill_args_
       default: return cudaErrorInvalidValue;                                \
     }                                                                       \
   } while (0)
+
+int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a) {
+  const DecSmem L(pool.head_k, dtype_size(pool.state_dtype), dtype_size(pool.conv_dtype),
+                  dtype_size(a.io_dtype), a.n_draft, a.gate_mode == LIN_GATE_PER_KEY);
+  return (L.load + 127) & ~127;
+}
 
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           cudaStream_t stream) {

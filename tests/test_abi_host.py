@@ -130,6 +130,32 @@ def test_decode_and_copy_reject_bad_args_on_host():
     assert L.lib.lin_state_restore(ctypes.byref(p), None, 0, None, None, None) == 0
 
 
+def test_decode_rejects_drafts_past_the_staging_limit():
+    """Head 128 with fp32 state, conv and io and per-key gates stages
+    76,288 + 2,048 bytes per draft (state 64 KB, conv window, taps; x and g
+    rows per draft) per (request, head): 17 drafts fit in 110 KB, 18 do not,
+    and the host says so before any launch."""
+    p = fake_pool(num_layers=2, st=L.LIN_F32, ct=L.LIN_F32)
+    d = L.DecodeArgsT()
+    d.layer, d.batch, d.n_draft = 0, 4, 18
+    d.io_dtype = d.out_dtype = L.LIN_F32
+    d.gate_mode, d.flags, d.q_scale = L.LIN_GATE_PER_KEY, 3, 1.0
+    for f in ("x", "conv_w", "g", "beta", "out", "slot", "pos"):
+        setattr(d, f, 0x300000)
+    sp = d.spec
+    sp.num_layers, sp.max_batch, sp.max_draft = 2, 4, 32
+    sp.temporal, sp.conv = 0x400000, 0x500000
+    blk = p.temporal_slot_stride
+    sp.temporal_step_stride, sp.temporal_req_stride = blk, 32 * blk
+    sp.temporal_layer_stride = 4 * 32 * blk
+    sp.conv_step_stride = p.conv_slot_stride
+    sp.conv_req_stride = 32 * p.conv_slot_stride
+    sp.conv_layer_stride = 4 * 32 * p.conv_slot_stride
+    d.spec = sp
+    assert L.lib.lin_state_decode(ctypes.byref(p), ctypes.byref(d), None) == L.LIN_EUNSUPPORTED
+    assert "n_draft 18" in L.lib.lin_state_last_error().decode()
+
+
 def test_strerror_and_version():
     assert L.lib.lin_state_strerror(L.LIN_EINVAL) == b"invalid argument"
     assert L.lin_state_version() >> 16 == 1

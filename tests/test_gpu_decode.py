@@ -41,7 +41,7 @@ def _decode_both(pool, op, dims, conv_w, slots, pos, track, interval, gate, seed
 
 
 @pytest.mark.parametrize("gate", [L.LIN_GATE_PER_HEAD, L.LIN_GATE_PER_KEY])
-@pytest.mark.parametrize("D", [16, 64])
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
 def test_decode_fp32_state_vs_oracle(gate, D):
     dims = W.LayerDims(num_heads=3, head_k=D, head_v=D)
     pool = L.StatePool(1, 20, 3, D, state_dtype=torch.float32, conv_dtype=torch.float32, device=DEV)
@@ -168,6 +168,40 @@ def test_verify_commit_vs_oracle_and_linear_chain(sdt):
     L.lin_state_spec_commit(pool, spec=spec, slot=_i32([3]), pos=_i32([0]), accept_len=_i32([5]),
                             n_draft=D, status=st)
     assert L.lin_state_read_status(st) == L.LIN_ST_BAD_ACCEPT
+
+
+def test_decode_and_verify_many_items_per_cta():
+    """Enough (request, head) items that every CTA of the persistent decode runs
+    several of them and wraps its ring of stages; empty slots (-1) sit between
+    live ones. One tracked decode step, then a 3-draft verify, against the oracle."""
+    H, D, B, S = 4, 64, 300, 400
+    dims = W.LayerDims(num_heads=H, head_k=D, head_v=D)
+    pool = L.StatePool(1, S, H, D, state_dtype=torch.float32, conv_dtype=torch.bfloat16, device=DEV)
+    fill_pool(pool, 21, std=0.1)
+    op = oracle_pool(pool)
+    perm = W.randperm(S, 21, "many.perm").tolist()
+    slots = [(-1 if r % 7 == 3 else perm[r]) for r in range(B)]
+    track = [(perm[B + r // 3] if r % 3 == 0 else -1) for r in range(B)]
+    pos = [255 if r % 5 == 0 else 17 + r for r in range(B)]
+    conv_w = W.randn((dims.conv_channels, 4), 21, "many.w", std=0.5).to(torch.bfloat16)
+    o, oo = _decode_both(pool, op, dims, conv_w, slots, pos, track, 256, L.LIN_GATE_PER_KEY, 21, 0,
+                         torch.float32)
+    live = [r for r in range(B) if slots[r] >= 0]
+    assert max_rel_per_head(o[live], oo[live], 2) < TOL_F32
+    pos = [p + 1 for p in pos]
+    spec = L.SpecBuffer(pool, B, 3)
+    ospec = O.make_spec_buffer(1, B, 3, H, D, D, dims.conv_channels)
+    o, oo = _decode_both(pool, op, dims, conv_w, slots, pos, None, 0, L.LIN_GATE_PER_KEY, 21, 1,
+                         torch.float32, n_draft=3, spec=spec, ospec=ospec)
+    assert max_rel_per_head(o[live], oo[live], 2) < TOL_F32
+    t = np64(pool.temporal[0])
+    for s_ in range(S):
+        assert max_rel_per_head(t[s_], op["temporal"][0, s_], 0) < TOL_F32
+    assert np.array_equal(np64(pool.conv), op["conv"])
+    st = np64(spec.temporal)
+    for r in live[::10]:
+        for j in range(3):
+            assert max_rel_per_head(st[0, r, j], ospec["temporal"][0, r, j], 0) < TOL_F32
 
 
 def test_decode_status_bits():
