@@ -1121,7 +1121,6 @@ constexpr int kNoAllocMaxBatch = kOrderMax;  // 4096 requests
 static __device__ __align__(256) int32_t g_noalloc_order[kNoAllocMaxBatch];
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::atomic<int32_t*> g_noalloc_ptr[kMaxDevices];
 }  // namespace
 

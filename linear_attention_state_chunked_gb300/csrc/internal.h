@@ -10,6 +10,12 @@ namespace lin {
 
 inline int dtype_size(int dt) { return dt == LIN_BF16 ? 2 : 4; }
 
+// Devices a process may address through the per-device caches below.
+constexpr int kMaxDevices = 64;
+// Streaming multiprocessors of device `dev` (queried once per device; 0 when
+// the query fails or dev is out of range).
+int device_sm_count(int dev);
+
 // Slot copy family (copy_kernels.cu).
 cudaError_t launch_copy_slots(const lin_state_pool_t& pool, const int32_t* src,
                               const int32_t* dst, int32_t n, int32_t layer_begin,

@@ -15,6 +15,8 @@
 // q|k|v channels runs first; each conv channel is owned by one thread, which
 // keeps its 3-input window in registers (Kimi-K3 notes, "Conv state").
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -743,9 +745,18 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
   store_window<TokCfg<D>::CPT, D>(slot_c, pool.conv_dtype, chan, win);
 }
 
+// Per device: the dynamic shared memory the kernel instance was last opened
+// up to, and the CTAs per SM at that size (set-up calls are not repeated on
+// every launch).
+struct DecodeLaunchCache {
+  std::atomic<int> smem_set[kMaxDevices];
+  std::atomic<int64_t> occupancy[kMaxDevices];  // (smem << 32) | CTAs per SM
+};
+
 template <int D, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           cudaStream_t stream) {
+  static DecodeLaunchCache cache;
   DecodeParams p{pool, a};
   const int stage = decode_stage_bytes(pool, a);
   if (stage > kDecodeMaxStage) return cudaErrorInvalidValue;
@@ -755,15 +766,31 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (stages < 2) stages = 2;
   const int smem = stages * stage;
   auto kern = decode_kernel<D, ST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DecPCfg<D>::NT, smem)) != cudaSuccess)
-    return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (cache.smem_set[dev].load() < smem) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+      return e;
+    int cur = cache.smem_set[dev].load();
+    while (cur < smem && !cache.smem_set[dev].compare_exchange_weak(cur, smem)) {
+    }
+  }
+  int per_sm = 0;
+  const int64_t occ = cache.occupancy[dev].load();
+  if ((occ >> 32) == smem && (occ & 0xffffffff) > 0) {
+    per_sm = static_cast<int>(occ & 0xffffffff);
+  } else {
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DecPCfg<D>::NT, smem)) != cudaSuccess)
+      return e;
+    if (per_sm < 1) per_sm = 1;
+    cache.occupancy[dev].store((int64_t(smem) << 32) | per_sm);
+  }
   const int items = a.batch * pool.num_heads;
-  int grid = sms * (per_sm > 0 ? per_sm : 1);
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  int grid = sms * per_sm;
   if (grid > items) grid = items;
   kern<<<grid, DecPCfg<D>::NT, smem, stream>>>(p, items, stage, stages);
   return cudaGetLastError();
@@ -790,6 +817,16 @@ cudaError_t prefill_launch(const lin_state_pool_t& pool, const lin_prefill_args_
       default: return cudaErrorInvalidValue;                                \
     }                                                                       \
   } while (0)
+
+int device_sm_count(int dev) {
+  static std::atomic<int> cache[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  int v = cache[dev].load();
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev].store(v);
+  return v;
+}
 
 int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a) {
   const DecSmem L(pool.head_k, dtype_size(pool.state_dtype), dtype_size(pool.conv_dtype),
