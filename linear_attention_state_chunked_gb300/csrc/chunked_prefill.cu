@@ -65,8 +65,12 @@ constexpr uint32_t OFF_PPL = OFF_KQ + 24576;    //   after MMA1: P (low part, GD
 constexpr uint32_t OFF_KQL = 65536;             // [K; Q] low part (GDN), 128 rows x 128
 constexpr int AXS = 68;                         // row stride (floats) of the fp32 A / X matrix
 constexpr uint32_t OFF_AX = OFF_KQL;            //   after MMA1: fp32 A / X [64][AXS]
-constexpr uint32_t OFF_XD = OFF_KQL + 64 * AXS * 4;  // after MMA1: fp32 diagonal inverses [4][16][16]
-constexpr uint32_t OFF_YB = OFF_XD + 4096;      //   after MMA1: fp32 M blocks X_aa A_ac [6][16][16]
+constexpr int XDS = 20;                         // row stride (floats) of a 16 x 16 solve block
+constexpr int XBS = 16 * XDS;                   // floats per 16 x 16 solve block
+constexpr int ZS = 36;                          // row stride (floats) of the 32 x 32 solve block
+constexpr uint32_t OFF_XD = OFF_KQL + 64 * AXS * 4;  // after MMA1: fp32 diagonal inverses [4][16][XDS]
+constexpr uint32_t OFF_YB = OFF_XD + 4 * XBS * 4;    //   after MMA1: fp32 A_10 X_00, A_32 X_22 [2][16][XDS]
+constexpr uint32_t OFF_ZB = OFF_YB + 2 * XBS * 4;    //   after MMA1: fp32 A_BA X_A [32][ZS]
 constexpr uint32_t OFF_OSTG = 98304;            // epilogue: output tile for a TMA store (32 KB)
 constexpr uint32_t OFF_KR = 98304;              // K_r (KDA), 64 x 128
 constexpr uint32_t OFF_UTL = OFF_KR;            //   after MMA2: U^T low part (GDN), rows v
@@ -85,7 +89,7 @@ constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
 constexpr uint32_t SMEM_USED = OFF_GLAST + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_YB + 6 * 1024 <= OFF_KR, "solve scratch inside the low-part region");
+static_assert(OFF_ZB + 32 * ZS * 4 <= OFF_KR, "solve scratch inside the low-part region");
 
 // Tensor-memory columns (256 allocated).
 constexpr uint32_t COL_S = 0;    // state, fp32, lanes v
@@ -377,6 +381,7 @@ __global__ void __launch_bounds__(NT, 1)
   float* AX = reinterpret_cast<float*>(sm + OFF_AX);
   float* XD = reinterpret_cast<float*>(sm + OFF_XD);
   float* YB = reinterpret_cast<float*>(sm + OFF_YB);
+  float* ZB = reinterpret_cast<float*>(sm + OFF_ZB);
 
   if (tid == 0) prefetch_x_tile(&tmap_x, bos, h, H);
   for (int i = tid; i < 384 * 4; i += NT)
@@ -691,82 +696,134 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncthreads();
 
-    // ---- T = (I + A)^-1 Diag(beta), blocked over 16 x 16 tiles a, c:
-    //   X_aa = (I + A_aa)^-1 (unit lower triangular, forward substitution),
-    //   M_ac = X_aa A_ac for c < a (all six at once),
-    //   X_ab = -sum_{c=b}^{a-1} M_ac X_cb, by levels a - b = 1, 2, 3.
-    // Off-diagonal X blocks overwrite the A blocks in AX once those are used.
-    if (tid < 256) {
-      // one 4-lane group per (block, column); lane q of the group holds rows q, q+4, q+8, q+12
-      const int grp = tid >> 2, q = tid & 3;
-      const int blk = grp >> 4, jj = grp & 15, base = blk * 16;
-      float x[4];
+    // ---- T = (I + A)^-1 Diag(beta). X = (I + A)^-1 (unit lower triangular) is
+    // built in three levels: its four 16 x 16 diagonal blocks X_aa by forward
+    // substitution (one thread per column); the two 32 x 32 diagonal blocks,
+    // X_10 = -X_11 (A_10 X_00) and X_32 = -X_33 (A_32 X_22); then the lower-left
+    // 32 x 32 quarter X_BA = -X_B (A_BA X_A), A and B the two halves. Each
+    // off-diagonal X block overwrites its A block in AX once that is used;
+    // above the diagonal AX holds zeros throughout.
+    static_assert(NT == 512, "solve thread mapping");
+    if (tid < 64) {
+      const int blk = tid >> 4, jj = tid & 15, base = blk * 16;
+      float x[16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) x[u] = (4 * u + q == jj) ? 1.f : 0.f;
+      for (int r = 0; r < 16; ++r) {
+        float av[16];
+        const float4* ar4 = reinterpret_cast<const float4*>(AX + (base + r) * AXS + base);
 #pragma unroll
-      for (int t = 1; t < 16; ++t) {
-        float part = 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 4 * u + q;
-          if (i < t) part = fmaf(AX[(base + t) * AXS + base + i], x[u], part);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          if (4 * q4 < r) {
+            const float4 f = ar4[q4];
+            av[4 * q4] = f.x;
+            av[4 * q4 + 1] = f.y;
+            av[4 * q4 + 2] = f.z;
+            av[4 * q4 + 3] = f.w;
+          }
         }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if ((t & 3) == q && t > jj) x[t >> 2] = -part;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) {
+          if (i & 1)
+            s1 = fmaf(av[i], x[i], s1);
+          else
+            s0 = fmaf(av[i], x[i], s0);
+        }
+        // x[i] = 0 for i < jj, so the sum is 0 at and above the diagonal
+        x[r] = (r == jj) ? 1.f : -(s0 + s1);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) XD[blk * 256 + (4 * u + q) * 16 + jj] = x[u];
+      for (int r = 0; r < 16; ++r) XD[blk * XBS + r * XDS + jj] = x[r];
     }
     __syncthreads();
     {
-      // M_ac = X_aa A_ac, blocks (a, c) in order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2);
-      // each thread: one row, four consecutive columns
-      for (int item = tid; item < 6 * 64; item += NT) {
-        const int mb = item >> 6, t = (item >> 2) & 15, j4 = (item & 3) * 4;
-        const int a_ = mb < 1 ? 1 : (mb < 3 ? 2 : 3);
-        const int c_ = mb - (a_ * (a_ - 1)) / 2;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // Y_s = A_{2s+1,2s} X_{2s,2s}
+      const int s2 = tid >> 8, r = (tid >> 4) & 15, c = tid & 15;
+      const float* arow = AX + (32 * s2 + 16 + r) * AXS + 32 * s2;
+      const float* xd = XD + (2 * s2) * XBS + c;
+      float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float xd = XD[a_ * 256 + t * 16 + m];
-          const float4 av = *reinterpret_cast<const float4*>(AX + (a_ * 16 + m) * AXS + c_ * 16 + j4);
-          acc[0] = fmaf(xd, av.x, acc[0]);
-          acc[1] = fmaf(xd, av.y, acc[1]);
-          acc[2] = fmaf(xd, av.z, acc[2]);
-          acc[3] = fmaf(xd, av.w, acc[3]);
-        }
-        *reinterpret_cast<float4*>(YB + mb * 256 + t * 16 + j4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      for (int m = 0; m < 16; m += 2) {
+        acc0 = fmaf(arow[m], xd[m * XDS], acc0);
+        acc1 = fmaf(arow[m + 1], xd[(m + 1) * XDS], acc1);
       }
+      YB[s2 * XBS + r * XDS + c] = acc0 + acc1;
     }
     __syncthreads();
-#pragma unroll 1
-    for (int lev = 1; lev < 4; ++lev) {
-      // blocks (a, b) with a - b = lev
-      for (int item = tid; item < (4 - lev) * 64; item += NT) {
-        const int b_ = item >> 6, a_ = b_ + lev, t = (item >> 2) & 15, j4 = (item & 3) * 4;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int c_ = b_; c_ < a_; ++c_) {
-          const int mb = (a_ * (a_ - 1)) / 2 + c_;
+    {
+      // X_{2s+1,2s} = -X_{2s+1,2s+1} Y_s, over A_{2s+1,2s}
+      const int s2 = tid >> 8, r = (tid >> 4) & 15, c = tid & 15;
+      const float* xr = XD + (2 * s2 + 1) * XBS + r * XDS;
+      const float* yb = YB + s2 * XBS + c;
+      float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float mv = YB[mb * 256 + t * 16 + m];
-            float4 xv;
-            if (c_ == b_)
-              xv = *reinterpret_cast<const float4*>(XD + b_ * 256 + m * 16 + j4);
-            else
-              xv = *reinterpret_cast<const float4*>(AX + (c_ * 16 + m) * AXS + b_ * 16 + j4);
-            acc[0] = fmaf(mv, xv.x, acc[0]);
-            acc[1] = fmaf(mv, xv.y, acc[1]);
-            acc[2] = fmaf(mv, xv.z, acc[2]);
-            acc[3] = fmaf(mv, xv.w, acc[3]);
-          }
-        }
-        *reinterpret_cast<float4*>(AX + (a_ * 16 + t) * AXS + b_ * 16 + j4) =
-            make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+      for (int m = 0; m < 16; m += 2) {
+        acc0 = fmaf(xr[m], yb[m * XDS], acc0);
+        acc1 = fmaf(xr[m + 1], yb[(m + 1) * XDS], acc1);
       }
-      __syncthreads();
+      AX[(32 * s2 + 16 + r) * AXS + 32 * s2 + c] = -(acc0 + acc1);
     }
+    __syncthreads();
+    {
+      // Z = A_BA X_A (rows 32.., cols 0..31); a warp keeps to one column half
+      const int chalf = tid >> 8, r = (tid >> 3) & 31, c = chalf * 16 + 2 * (tid & 7);
+      const float* arow = AX + (32 + r) * AXS;
+      float z0 = 0.f, z1 = 0.f;
+      if (chalf == 0) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {  // X_00
+          const float2 xv = *reinterpret_cast<const float2*>(XD + m * XDS + c);
+          z0 = fmaf(arow[m], xv.x, z0);
+          z1 = fmaf(arow[m], xv.y, z1);
+        }
+#pragma unroll
+        for (int m = 16; m < 32; ++m) {  // X_10
+          const float2 xv = *reinterpret_cast<const float2*>(AX + m * AXS + c);
+          z0 = fmaf(arow[m], xv.x, z0);
+          z1 = fmaf(arow[m], xv.y, z1);
+        }
+      } else {
+#pragma unroll
+        for (int m = 16; m < 32; ++m) {  // X_11
+          const float2 xv = *reinterpret_cast<const float2*>(XD + XBS + (m - 16) * XDS + (c - 16));
+          z0 = fmaf(arow[m], xv.x, z0);
+          z1 = fmaf(arow[m], xv.y, z1);
+        }
+      }
+      *reinterpret_cast<float2*>(ZB + r * ZS + c) = make_float2(z0, z1);
+    }
+    __syncthreads();
+    {
+      // X_BA = -X_B Z, over A_BA; a warp keeps to one row half of X_B
+      const int rhalf = tid >> 8, rl = (tid >> 4) & 15, c = 2 * (tid & 15);
+      float o0 = 0.f, o1 = 0.f;
+      if (rhalf == 0) {
+        const float* xr = XD + 2 * XBS + rl * XDS;  // X_22 row rl
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 zv = *reinterpret_cast<const float2*>(ZB + m * ZS + c);
+          o0 = fmaf(xr[m], zv.x, o0);
+          o1 = fmaf(xr[m], zv.y, o1);
+        }
+      } else {
+        const float* xr1 = AX + (48 + rl) * AXS + 32;  // X_32 row rl
+        const float* xr2 = XD + 3 * XBS + rl * XDS;    // X_33 row rl
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 zv = *reinterpret_cast<const float2*>(ZB + m * ZS + c);
+          o0 = fmaf(xr1[m], zv.x, o0);
+          o1 = fmaf(xr1[m], zv.y, o1);
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 zv = *reinterpret_cast<const float2*>(ZB + (16 + m) * ZS + c);
+          o0 = fmaf(xr2[m], zv.x, o0);
+          o1 = fmaf(xr2[m], zv.y, o1);
+        }
+      }
+      *reinterpret_cast<float2*>(AX + (32 + rhalf * 16 + rl) * AXS + c) = make_float2(-o0, -o1);
+    }
+    __syncthreads();
     {
       const int t = tid >> 3, c0 = (tid & 7) * 8;
       float tv[8];
@@ -775,7 +832,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int i = c0 + m;
         float xvv;
         if ((i >> 4) == (t >> 4))
-          xvv = XD[(t >> 4) * 256 + (t & 15) * 16 + (i & 15)];
+          xvv = XD[(t >> 4) * XBS + (t & 15) * XDS + (i & 15)];
         else
           xvv = AX[t * AXS + i];  // zero above the diagonal blocks
         tv[m] = xvv * SBETA[i];
