@@ -82,6 +82,74 @@ struct Vec8<LIN_BF16> {
   }
 };
 
+// ---- packed fp32 pairs (two lanes of fp32 arithmetic per instruction) ----
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2sum(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 8 consecutive elements as 4 packed fp32 pairs, element 2i in the low half.
+template <int DT>
+struct Pair8;
+
+template <>
+struct Pair8<LIN_F32> {
+  static __device__ __forceinline__ void load(const void* p, uint64_t (&v)[4]) {
+    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p);
+    const ulonglong2 a = q[0], b = q[1];
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  }
+  static __device__ __forceinline__ void store(void* p, const uint64_t (&v)[4]) {
+    ulonglong2* q = reinterpret_cast<ulonglong2*>(p);
+    q[0] = make_ulonglong2(v[0], v[1]);
+    q[1] = make_ulonglong2(v[2], v[3]);
+  }
+  static __device__ __forceinline__ void round(uint64_t (&)[4]) {}
+};
+
+template <>
+struct Pair8<LIN_BF16> {
+  static __device__ __forceinline__ void load(const void* p, uint64_t (&v)[4]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = f2pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  }
+  static __device__ __forceinline__ uint32_t pack(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));  // hi -> upper half
+    return r;
+  }
+  static __device__ __forceinline__ void store(void* p, const uint64_t (&v)[4]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3]));
+  }
+  static __device__ __forceinline__ void round(uint64_t (&v)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t b = pack(v[i]);
+      v[i] = f2pack(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
+    }
+  }
+};
+
 __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

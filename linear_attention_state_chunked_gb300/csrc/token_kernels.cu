@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
   using C = DecPCfg<D>;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ float ysm[2][3 * D];                      // post-conv q | k | v, by token parity
-  __shared__ float agsm[2][D];                         // per-key decay factors
+  __shared__ __align__(16) float ysm[2][3 * D];        // post-conv q | k | v, by token parity
+  __shared__ __align__(16) float agsm[2][D];           // per-key decay factors
   __shared__ float normsm[2][D < 32 ? 1 : D / 32][3];  // q.q, k.k, q.k partials per conv warp
   __shared__ uint64_t full[kDecMaxStages], empty[kDecMaxStages];
   __shared__ DecMeta meta[kDecMaxStages];
@@ -544,38 +544,52 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
       const float rq = (l2 ? rsqrtf(sqq + kL2Eps) : 1.f) * a.q_scale;
       const float rk = l2 ? rsqrtf(skk + kL2Eps) : 1.f;
       const float kq = sqk * rq * rk;
-      float a8[8], q8[8], k8[8];
-      if (per_key) {
+      // this lane's 8 key channels as 4 packed pairs
+      uint64_t a2[4], q2[4], k2[4];
+      {
+        const float4* yq4 = reinterpret_cast<const float4*>(ys + lr * 8);
+        const float4* yk4 = reinterpret_cast<const float4*>(ys + D + lr * 8);
+        const uint64_t rq2 = f2pack(rq, rq), rk2 = f2pack(rk, rk);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a8[e] = agsm[tc & 1][lr * 8 + e];
-      } else {
-        const float av = expf(gh);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float4 fq = yq4[h2], fk = yk4[h2];
+          q2[2 * h2] = fmul2(f2pack(fq.x, fq.y), rq2);
+          q2[2 * h2 + 1] = fmul2(f2pack(fq.z, fq.w), rq2);
+          k2[2 * h2] = fmul2(f2pack(fk.x, fk.y), rk2);
+          k2[2 * h2 + 1] = fmul2(f2pack(fk.z, fk.w), rk2);
+        }
+        if (per_key) {
+          const float4* ag4 = reinterpret_cast<const float4*>(agsm[tc & 1] + lr * 8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a8[e] = av;
-      }
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float4 fa = ag4[h2];
+            a2[2 * h2] = f2pack(fa.x, fa.y);
+            a2[2 * h2 + 1] = f2pack(fa.z, fa.w);
+          }
+        } else {
+          const float av = expf(gh);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        q8[e] = ys[lr * 8 + e] * rq;
-        k8[e] = ys[D + lr * 8 + e] * rk;
+          for (int e2 = 0; e2 < 4; ++e2) a2[e2] = f2pack(av, av);
+        }
       }
       uint8_t* sst = buf + L.state;
 #pragma unroll
       for (int rb = 0; rb < C::RPT; rb += C::RB) {
-        float sv[C::RB][8];
+        uint64_t sv[C::RB][4];
         float red[C::NV];
 #pragma unroll
         for (int i = 0; i < C::RB; ++i) {
           const int row = row0 + (rb + i) * C::RSTEP;
-          Vec8<ST>::load(sst + (int64_t(row) * D + lr * 8) * ES, sv[i]);
-          float dk = 0.f, dq = 0.f;
+          Pair8<ST>::load(sst + (int64_t(row) * D + lr * 8) * ES, sv[i]);
+          uint64_t dk2 = 0ull, dq2 = 0ull;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            sv[i][e] *= a8[e];
-            dk = fmaf(sv[i][e], k8[e], dk);
-            dq = fmaf(sv[i][e], q8[e], dq);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            sv[i][e2] = fmul2(sv[i][e2], a2[e2]);
+            dk2 = ffma2(sv[i][e2], k2[e2], dk2);
+            dq2 = ffma2(sv[i][e2], q2[e2], dq2);
           }
-          red[2 * i] = dk;
-          red[2 * i + 1] = dq;
+          red[2 * i] = f2sum(dk2);
+          red[2 * i + 1] = f2sum(dq2);
         }
         // transposing butterfly: after the exchange at distance d the lane
         // keeps the half of its values selected by (lr & d)
@@ -613,13 +627,14 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
 #pragma unroll
         for (int i = 0; i < C::RB; ++i) {
           const int64_t off = (int64_t(row0 + (rb + i) * C::RSTEP) * D + lr * 8) * ES;
+          const uint64_t u2 = f2pack(u[i], u[i]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sv[i][e] = fmaf(u[i], k8[e], sv[i][e]);
-          Vec8<ST>::store(dt + off, sv[i]);
-          if (tt) Vec8<ST>::store(tt + off, sv[i]);
+          for (int e2 = 0; e2 < 4; ++e2) sv[i][e2] = ffma2(u2, k2[e2], sv[i][e2]);
+          Pair8<ST>::store(dt + off, sv[i]);
+          if (tt) Pair8<ST>::store(tt + off, sv[i]);
           if (ND > 1) {
-            Vec8<ST>::round(sv[i]);  // the next draft starts from the stored state
-            Vec8<ST>::store(sst + off, sv[i]);
+            Pair8<ST>::round(sv[i]);  // the next draft starts from the stored state
+            Pair8<ST>::store(sst + off, sv[i]);
           }
         }
       }
