@@ -86,7 +86,8 @@ constexpr uint32_t OFF_WTOT = OFF_HALO + 4608;  // per-warp gate sums, fp32 [16]
 constexpr uint32_t OFF_SBETA = OFF_WTOT + 8192; // beta_t, fp32 [64]
 constexpr uint32_t OFF_SB = OFF_SBETA + 256;    // GDN b_t, fp32 [64]
 constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
-constexpr uint32_t SMEM_USED = OFF_GLAST + 512;
+constexpr uint32_t OFF_CF = OFF_GLAST + 512;    // GDN column decay factors, fp32 [64]
+constexpr uint32_t SMEM_USED = OFF_CF + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_ZB + 32 * ZS * 4 <= OFF_KR, "solve scratch inside the low-part region");
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(NT, 1)
   float* SBETA = reinterpret_cast<float*>(sm + OFF_SBETA);
   float* SB = reinterpret_cast<float*>(sm + OFF_SB);
   float* GLAST = reinterpret_cast<float*>(sm + OFF_GLAST);
+  float* CF = reinterpret_cast<float*>(sm + OFF_CF);
   float* AX = reinterpret_cast<float*>(sm + OFF_AX);
   float* XD = reinterpret_cast<float*>(sm + OFF_XD);
   float* YB = reinterpret_cast<float*>(sm + OFF_YB);
@@ -658,6 +660,14 @@ __global__ void __launch_bounds__(NT, 1)
       }
       umma::mma_commit(&bar_mma);
     }
+    if (!KDA && tid >= 32 && tid < 96) {
+      // GDN: the in-chunk decay exp(b_t - b_i) factors as exp(b_t - b_s) exp(b_s - b_i),
+      // s the first column of i's 16-wide slice; the second factor per column here
+      // (-1 where it would leave fp32 range: those columns take the direct exponential)
+      const int i = tid - 32;
+      const float d = SB[i & ~15] - SB[i];
+      CF[i] = d <= 80.f ? __expf(d) : -1.f;
+    }
     if (j + 1 < nch) {
       const int n2 = (L - (j + 1) * CH) < CH ? (L - (j + 1) * CH) : CH;
       load_gates<KDA>(a, row0 + CH, n2, h, H, warp, lane, gk, bt);
@@ -668,24 +678,35 @@ __global__ void __launch_bounds__(NT, 1)
     {
       float v[16];
       umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R1 + slice * 16), v);
+      const int s0 = slice * 16;
       if (quarter < 2) {
         const int t = vrow;
         const float bet = SBETA[t];
         const float bt_ = SB[t];
+        const float rfac = (KDA || s0 > t) ? 1.f : __expf(bt_ - SB[s0]);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const int i = slice * 16 + k;
-          const float dec = KDA ? 1.f : __expf(bt_ - SB[i < t ? i : t]);
+          const int i = s0 + k;
+          float dec = 1.f;
+          if (!KDA) {
+            const float cf = CF[i];
+            dec = cf >= 0.f ? rfac * cf : __expf(bt_ - SB[i < t ? i : t]);
+          }
           AX[t * AXS + i] = (i < t) ? bet * v[k] * dec : 0.f;
         }
       } else {
         const int t = vrow - 64;
         const float bt_ = SB[t];
+        const float rfac = (KDA || s0 > t) ? 1.f : __expf(bt_ - SB[s0]);
         float pv[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const int i = slice * 16 + k;
-          const float dec = KDA ? 1.f : __expf(bt_ - SB[i <= t ? i : t]);
+          const int i = s0 + k;
+          float dec = 1.f;
+          if (!KDA) {
+            const float cf = CF[i];
+            dec = cf >= 0.f ? rfac * cf : __expf(bt_ - SB[i <= t ? i : t]);
+          }
           pv[k] = (i <= t) ? v[k] * dec : 0.f;
         }
         if (SPLIT)

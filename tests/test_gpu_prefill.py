@@ -105,6 +105,24 @@ def test_qwen35_gdn_reduced(path):
 
 
 @pytest.mark.parametrize("path", list(PATHS))
+def test_gdn_strong_decay(path):
+    """GDN with log-decay U[-12, 0] per (token, head): 16 consecutive tokens can
+    decay by far more than e^80, so the chunked kernel's separable decay factors
+    must fall back to the direct exponential on those columns; ragged requests."""
+    dims = W.LayerDims(num_heads=4, head_k=128, head_v=128)
+    b = W.make_prefill_batch(dims, [300, 130], W.GATE_PER_HEAD, dtype=torch.bfloat16, seed=3,
+                             gate="uniform", tag="sd")
+    b.g = b.g * 120.0
+    b.g[5:9] = 0.0  # a few tokens with no decay
+    pool = L.StatePool(1, 8, 4, 128, state_dtype=torch.float32, conv_dtype=torch.bfloat16,
+                       device=DEV)
+    op = oracle_pool(pool)
+    out, oo = run_both(pool, op, b, [1, 2], [3, 4, 5, 6], [0, 2, 4], 64, path)
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), TOL_F32)
+    compare_slots(pool, op, [1, 2, 3, 4, 5, 6], TOL_F32)
+
+
+@pytest.mark.parametrize("path", list(PATHS))
 def test_kimi_k3_kda_varlen_reduced(path):
     """Kimi-K3 TP8 KDA varlen prefill at reduced size: 12 heads, bf16 inputs and
     state, per-key decay exp(-softplus(N(0,1))), three requests (two warm from a
