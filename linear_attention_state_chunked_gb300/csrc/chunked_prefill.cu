@@ -87,7 +87,8 @@ constexpr uint32_t OFF_SBETA = OFF_WTOT + 8192; // beta_t, fp32 [64]
 constexpr uint32_t OFF_SB = OFF_SBETA + 256;    // GDN b_t, fp32 [64]
 constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
 constexpr uint32_t OFF_CF = OFF_GLAST + 512;    // GDN column decay factors, fp32 [64]
-constexpr uint32_t SMEM_USED = OFF_CF + 256;
+constexpr uint32_t OFF_WIN = OFF_CF + 256;      // the chunk's last 3 inputs, fp32 [3][384]
+constexpr uint32_t SMEM_USED = OFF_WIN + 3 * 384 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_ZB + 32 * ZS * 4 <= OFF_KR, "solve scratch inside the low-part region");
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(NT, 1)
   float* SB = reinterpret_cast<float*>(sm + OFF_SB);
   float* GLAST = reinterpret_cast<float*>(sm + OFF_GLAST);
   float* CF = reinterpret_cast<float*>(sm + OFF_CF);
+  float* WIN = reinterpret_cast<float*>(sm + OFF_WIN);
   float* AX = reinterpret_cast<float*>(sm + OFF_AX);
   float* XD = reinterpret_cast<float*>(sm + OFF_XD);
   float* YB = reinterpret_cast<float*>(sm + OFF_YB);
@@ -491,6 +493,34 @@ __global__ void __launch_bounds__(NT, 1)
         xr[m][part] = from_x ? *reinterpret_cast<const uint2*>(
                                    xg + (row0 + rel) * C_all + part * H * DH + h * DH + lane * 4)
                              : make_uint2(0u, 0u);
+    }
+
+    // the chunk's last 3 inputs, kept for a conv-state snapshot or the final
+    // write-back: each row is written by the warp that holds it (rows before
+    // the chunk by warp 0), so the epilogue need not read x again
+    {
+      const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
+      const bool need_win = (j == nch - 1) || (ntr > 0 && n == CH && (end_pos % a.track_stride) == 0);
+      if (need_win) {
+#pragma unroll
+        for (int m = 0; m < TPW + 3; ++m) {
+          const int rel = tfirst - 3 + m;
+          if (rel >= n - 3 && rel < n && (rel >= tfirst || (warp == 0 && rel < 0))) {
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+              float4 wv;
+              if (j == 0 && rel < 0) {
+                wv = *reinterpret_cast<const float4*>(HALO + (rel + 3) * 384 + part * 128 + lane * 4);
+              } else {
+                const uint2 u2 = xr[m][part];
+                wv = make_float4(__uint_as_float(u2.x << 16), __uint_as_float(u2.x & 0xffff0000u),
+                                 __uint_as_float(u2.y << 16), __uint_as_float(u2.y & 0xffff0000u));
+              }
+              *reinterpret_cast<float4*>(WIN + (rel - n + 3) * 384 + part * 128 + lane * 4) = wv;
+            }
+          }
+        }
+      }
     }
 
     // the previous chunk's TMA stores must have read their staging tiles
@@ -1047,11 +1077,8 @@ __global__ void __launch_bounds__(NT, 1)
                                      : nullptr;
         for (int idx = tid; idx < 3 * 384; idx += NT) {
           const int cl = idx / 3, m = idx % 3;
-          const int rel = n - 3 + m;
           const int ch = head_channel(cl, h, H);
-          const float wv = (j == 0 && rel < 0)
-                               ? HALO[(rel + 3) * 384 + cl]
-                               : bf16_bits_to_f32(xg[(row0 + rel) * C_all + ch]);
+          const float wv = WIN[m * 384 + cl];
           const int64_t off = int64_t(ch) * 3 + m;
           if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
           if (last) store_elem(slot_c, off, pool.conv_dtype, wv);
