@@ -87,8 +87,13 @@ constexpr uint32_t OFF_SBETA = OFF_WTOT + 8192; // beta_t, fp32 [64]
 constexpr uint32_t OFF_SB = OFF_SBETA + 256;    // GDN b_t, fp32 [64]
 constexpr uint32_t OFF_GLAST = OFF_SB + 256;    // exp(b_last), fp32 [128]
 constexpr uint32_t OFF_CF = OFF_GLAST + 512;    // GDN column decay factors, fp32 [64]
-constexpr uint32_t OFF_WIN = OFF_CF + 256;      // the chunk's last 3 inputs, fp32 [3][384]
-constexpr uint32_t SMEM_USED = OFF_WIN + 3 * 384 * 4;
+constexpr uint32_t OFF_WIN = OFF_CF + 256;      // last 3 inputs of chunks j even / odd, fp32 [2][3][384]
+constexpr uint32_t SMEM_USED = OFF_WIN + 2 * 3 * 384 * 4;
+// The next chunk's x tile (q | k | v parts of this head, 64 rows x 128 bf16
+// each, row-major) lands in the V / gamma.Q / K-tilde operand regions, which
+// are free once a chunk's last MMA has completed.
+constexpr uint32_t OFF_XT = OFF_VV;
+static_assert(OFF_QH == OFF_VV + 16384 && OFF_KT == OFF_QH + 16384, "x tile spans three regions");
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_ZB + 32 * ZS * 4 <= OFF_KR, "solve scratch inside the low-part region");
@@ -227,6 +232,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tmap, uint32_t s
       "r"(c0), "r"(c1), "r"(c2), "r"(src)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* tmap, uint32_t dst, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -305,6 +317,7 @@ __device__ __forceinline__ void put16_split(uint32_t hi_buf, uint32_t lo_buf, in
 template <bool KDA, int ST>
 __global__ void __launch_bounds__(NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                           const __grid_constant__ CUtensorMap tmap_xt,
                            const __grid_constant__ CUtensorMap tmap_state,
                            const __grid_constant__ CUtensorMap tmap_out, const ChunkParams p) {
   // GDN: fp16 operands with high / low splits on the products that set the
@@ -313,6 +326,7 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr bool SPLIT = !KDA;
   extern __shared__ uint8_t dsm[];
   __shared__ uint64_t bar_mma;
+  __shared__ uint64_t bar_x;  // x tile of the next chunk landed
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -368,9 +382,6 @@ __global__ void __launch_bounds__(NT, 1)
                  slot * pool.temporal_slot_stride + h * head_bytes;
   char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                  slot * pool.conv_slot_stride;
-  const int C_all = pool.conv_channels;
-  const uint16_t* xg = static_cast<const uint16_t*>(a.x);
-
   const uint32_t raw = umma::smem_u32(dsm);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sm = dsm + (sb - raw);
@@ -408,6 +419,7 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (tid == 0) {
     umma::mbar_init(&bar_mma, 1);
+    umma::mbar_init(&bar_x, 1);
     umma::mbar_fence_init();
     abort_sh = 0;
   }
@@ -476,54 +488,78 @@ __global__ void __launch_bounds__(NT, 1)
     return abort_sh == 0;
   };
 
+  // The x tile of the chunk starting at token r0 (thread 0): one TMA load per
+  // q | k | v part, completing on bar_x.
+  int x_issued = 0;
+  auto issue_x_tile = [&](int64_t r0) {
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar_x));
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(3 * CH * DH * 2)
+                 : "memory");
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+      tma_load_2d(&tmap_xt, sb + OFF_XT + part * (CH * DH * 2), part * H * DH + h * DH, static_cast<int>(r0), b);
+    ++x_issued;
+  };
+  if (tid == 0) issue_x_tile(bos);
+
+  const int tfirst = warp * TPW;
   for (int j = 0; j < nch; ++j) {
     const int n = (L - j * CH) < CH ? (L - j * CH) : CH;
     const int64_t row0 = bos + int64_t(j) * CH;
 
-    // ---- x rows of this warp's tokens (and the 3 before them), straight from
-    // global memory (L2, prefetched): 8 bytes = 4 channels per lane and part.
-    const int tfirst = warp * TPW;
+    // this chunk's x tile must have landed
+    if (tid == 0) {
+      if (!umma::mbar_wait(&bar_x, static_cast<uint32_t>(j & 1), kWaitTries)) {
+        abort_sh = 1;
+        report(a.status, LIN_ST_TIMEOUT);
+      }
+    }
+    __syncthreads();
+    if (abort_sh) break;
+
+    // ---- x rows of this warp's tokens from the tile (8 bytes = 4 channels per
+    // lane and part); rows before the chunk come from the previous window, rows
+    // past its end are zero
     uint2 xr[TPW + 3][3];
 #pragma unroll
     for (int m = 0; m < TPW + 3; ++m) {
       const int rel = tfirst - 3 + m;  // row relative to the chunk start
-      const bool from_x = (rel < n) && (j > 0 || rel >= 0);
 #pragma unroll
       for (int part = 0; part < 3; ++part)
-        xr[m][part] = from_x ? *reinterpret_cast<const uint2*>(
-                                   xg + (row0 + rel) * C_all + part * H * DH + h * DH + lane * 4)
-                             : make_uint2(0u, 0u);
+        xr[m][part] = (rel >= 0 && rel < n)
+                          ? *reinterpret_cast<const uint2*>(sm + OFF_XT + part * (CH * DH * 2) + rel * (DH * 2) + lane * 8)
+                          : make_uint2(0u, 0u);
     }
+    // the window before this chunk (its last 3 inputs): the initial conv state
+    // for the first chunk, else the previous chunk's window
+    const float* wprev = j == 0 ? HALO : WIN + ((j - 1) & 1) * 1152;
 
-    // the chunk's last 3 inputs, kept for a conv-state snapshot or the final
-    // write-back: each row is written by the warp that holds it (rows before
-    // the chunk by warp 0), so the epilogue need not read x again
+    // the chunk's last 3 inputs, for the next chunk and for a conv-state
+    // snapshot or the final write-back: each row is written by the warp that
+    // holds it (rows before the chunk by warp 0)
     {
-      const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
-      const bool need_win = (j == nch - 1) || (ntr > 0 && n == CH && (end_pos % a.track_stride) == 0);
-      if (need_win) {
+      float* wcur = WIN + (j & 1) * 1152;
 #pragma unroll
-        for (int m = 0; m < TPW + 3; ++m) {
-          const int rel = tfirst - 3 + m;
-          if (rel >= n - 3 && rel < n && (rel >= tfirst || (warp == 0 && rel < 0))) {
+      for (int m = 0; m < TPW + 3; ++m) {
+        const int rel = tfirst - 3 + m;
+        if (rel >= n - 3 && rel < n && (rel >= tfirst || (warp == 0 && rel < 0))) {
 #pragma unroll
-            for (int part = 0; part < 3; ++part) {
-              float4 wv;
-              if (j == 0 && rel < 0) {
-                wv = *reinterpret_cast<const float4*>(HALO + (rel + 3) * 384 + part * 128 + lane * 4);
-              } else {
-                const uint2 u2 = xr[m][part];
-                wv = make_float4(__uint_as_float(u2.x << 16), __uint_as_float(u2.x & 0xffff0000u),
-                                 __uint_as_float(u2.y << 16), __uint_as_float(u2.y & 0xffff0000u));
-              }
-              *reinterpret_cast<float4*>(WIN + (rel - n + 3) * 384 + part * 128 + lane * 4) = wv;
+          for (int part = 0; part < 3; ++part) {
+            float4 wv;
+            if (rel < 0) {
+              wv = *reinterpret_cast<const float4*>(wprev + (rel + 3) * 384 + part * 128 + lane * 4);
+            } else {
+              const uint2 u2 = xr[m][part];
+              wv = make_float4(__uint_as_float(u2.x << 16), __uint_as_float(u2.x & 0xffff0000u),
+                               __uint_as_float(u2.y << 16), __uint_as_float(u2.y & 0xffff0000u));
             }
+            *reinterpret_cast<float4*>(wcur + (rel - n + 3) * 384 + part * 128 + lane * 4) = wv;
           }
         }
       }
     }
-
-    // the previous chunk's TMA stores must have read their staging tiles
+    // the previous chunk's TMA stores must have read their staging tiles before
+    // the conv writes operands over them (after the barrier in the gate sums)
     if (tid == 0) bulk_wait_read();
 
     // ---- gates: in-chunk inclusive sums b_t (rows past n carry log-decay 0)
@@ -588,7 +624,7 @@ __global__ void __launch_bounds__(NT, 1)
       // x value of window row m (chunk row tfirst - 3 + m), part, channel lane*4+e
       auto xv = [&](int m, int part, int e) -> float {
         const int rel = tfirst - 3 + m;
-        if (j == 0 && rel < 0) return HALO[(rel + 3) * 384 + part * 128 + lane * 4 + e];
+        if (rel < 0) return wprev[(rel + 3) * 384 + part * 128 + lane * 4 + e];
         const uint32_t w = (e < 2) ? xr[m][part].x : xr[m][part].y;
         return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
       };
@@ -991,6 +1027,8 @@ __global__ void __launch_bounds__(NT, 1)
       umma::mma_commit(&bar_mma);
     }
     if (!wait_mma()) break;
+    // every MMA of this chunk is done: the next chunk's x tile may land now
+    if (tid == 0 && j + 1 < nch) issue_x_tile(row0 + CH);
 
     // ---- outputs, state operand for the next chunk, snapshots, final state.
     // Full-chunk outputs and every stored state go through swizzled staging
@@ -1078,7 +1116,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int idx = tid; idx < 3 * 384; idx += NT) {
           const int cl = idx / 3, m = idx % 3;
           const int ch = head_channel(cl, h, H);
-          const float wv = WIN[m * 384 + cl];
+          const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
           const int64_t off = int64_t(ch) * 3 + m;
           if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
           if (last) store_elem(slot_c, off, pool.conv_dtype, wv);
@@ -1104,8 +1142,14 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
 
-  // ---- teardown: every TMA store issued here has completed before exit
-  if (tid == 0) bulk_wait_all();
+  // ---- teardown: every TMA store issued here has completed, and no x tile is
+  // still landing, before exit
+  if (tid == 0) {
+    bulk_wait_all();
+    // after an early exit the last x tile issued may not have been waited for
+    // (each chunk j waited for x tile j, phase j & 1)
+    if (abort_sh) umma::mbar_wait(&bar_x, static_cast<uint32_t>((x_issued - 1) & 1), kWaitTries);
+  }
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 0) umma::tmem_dealloc(tm, TMEM_COLS);
@@ -1142,6 +1186,15 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // x tiles loaded into shared memory: 64 rows x 128 channels, row-major
+  CUtensorMap tmap_xt;
+  {
+    const cuuint32_t bxt[2] = {static_cast<cuuint32_t>(DH), static_cast<cuuint32_t>(CH)};
+    cr = enc(&tmap_xt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.x), dims, strides, bxt,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   // state tiles: [slot][H][V][K] of this layer, box 32 rows x 128 bytes
   CUtensorMap tmap_state;
   {
@@ -1184,7 +1237,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
   }
   ChunkParams p{pool, a, order};
   const unsigned grid = static_cast<unsigned>(a.batch) * static_cast<unsigned>(pool.num_heads);
-  kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_state, tmap_out, p);
+  kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p);
   return cudaGetLastError();
 }
 
