@@ -81,7 +81,9 @@ enum {
   LIN_QK_L2NORM = 1u,        /* L2-normalise q and k per head, eps 1e-6 inside the sqrt */
   LIN_CONV_SILU = 2u,        /* SiLU on the conv output                        */
   LIN_VALIDATE = 4u,         /* extra device checks (copy aliasing)            */
-  LIN_PREFILL_RECURRENT = 8u /* prefill: force the token-by-token kernel       */
+  LIN_PREFILL_RECURRENT = 8u, /* prefill: force the token-by-token kernel      */
+  LIN_PREFILL_SEGMENTED = 16u /* prefill: run a batch of one request in segments
+                                 even when it is short (see lin_state_prefill) */
 };
 
 /* ---- the state pool ([MRC] 1.3; [K3] shapes) ----------------------------
@@ -127,7 +129,18 @@ typedef struct {
  * A negative entry in a track list skips that snapshot. Requests must use
  * distinct live slots; a track slot equal to the live slot is rejected
  * (LIN_ST_TRACK_ALIAS). Workspace: lin_state_prefill_workspace() bytes of
- * device memory (may be 0 -> workspace may be NULL). */
+ * device memory (may be 0 -> workspace may be NULL).
+ * Long single requests: with the chunked kernel, a batch of one request
+ * whose heads alone cannot fill the GPU (heads x 4 <= SMs, >= 4096 tokens
+ * by total_tokens; any request of >= 8 chunks with LIN_PREFILL_SEGMENTED)
+ * runs in segments: the state after a segment is affine in the state before
+ * it (S M + B), so every segment's offset B (from a zero state) and
+ * transition M (from the identity, with zero values) are computed in
+ * parallel, a scan carries the true state across segments (fp32), and every
+ * segment then runs in parallel from its true initial state. The workspace
+ * then holds 2 fp32 states per (segment, head); with less workspace than
+ * the query reports, or in lin_state_prefill_noalloc, the request runs in
+ * one piece. */
 typedef struct {
   int32_t layer;
   int32_t batch;
@@ -153,7 +166,7 @@ typedef struct {
 } lin_prefill_args_t;
 
 /* Which kernel lin_state_prefill would run for these arguments:
- * LIN_KERNEL_CHUNKED (the tensor-core chunked kernel: head_k == 128 or 64)
+ * LIN_KERNEL_CHUNKED (the tensor-core chunked kernel: head_k == 128, bf16 x)
  * or LIN_KERNEL_RECURRENT (token by token; any supported head dim, or when
  * LIN_PREFILL_RECURRENT is set). A negative LIN_E* code for invalid args. */
 #define LIN_KERNEL_RECURRENT 0

@@ -105,10 +105,26 @@ constexpr uint32_t COL_R2 = 192; // W^T -> O^T
 constexpr uint32_t TMEM_COLS = 256;
 
 
+// Segmented run of one long request (batch of 1). The state after a chunk is
+// affine in the state before it, S' = S A_c + (U'^T K-tilde) with
+// A_c = Gamma - W^T K-tilde, so a segment of chunks maps S to S M + B. Mode 1
+// runs each segment from a zero state (its B; segment 0 from the request's
+// own initial state, giving the true state after it), mode 2 runs segments >= 1
+// from the identity with zero values (their M: rows evolve independently, and a
+// zero value input drops the U' term), both writing only the fp32 state at the
+// segment's end; after the scan S_{k+1} = S_k M_k + B_k, mode 3 runs every
+// segment from its true initial state with outputs and snapshots.
+enum SegMode { kSegOff = 0, kSegOffset = 1, kSegTransition = 2, kSegFinal = 3 };
+
 struct ChunkParams {
   lin_state_pool_t pool;
   lin_prefill_args_t a;
   const int32_t* order;  // requests longest first (nullptr: batch order)
+  int seg_mode;          // SegMode
+  int seg_len;           // tokens per segment (multiple of 64)
+  int seg_first;         // segment of blockIdx.x < H
+  float* seg_state_out;        // modes 1, 2: fp32 state after the segment, [seg][H][V][K]
+  const float* seg_state_in;   // mode 3: fp32 state before segment k >= 1 at index k - 1
 };
 
 // Longest-first order of a varlen batch: the sequential chunk chain of the
@@ -333,7 +349,9 @@ __global__ void __launch_bounds__(NT, 1)
   const lin_state_pool_t& pool = p.pool;
   const lin_prefill_args_t& a = p.a;
   const int H = pool.num_heads;
-  const int r = p.order ? p.order[blockIdx.x / H] : blockIdx.x / H;
+  const int seg_mode = p.seg_mode;
+  const int seg = seg_mode ? p.seg_first + static_cast<int>(blockIdx.x) / H : 0;
+  const int r = seg_mode ? 0 : (p.order ? p.order[blockIdx.x / H] : blockIdx.x / H);
   const int h = blockIdx.x % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, slice = warp >> 2;  // four warps share each lane quarter
@@ -347,34 +365,50 @@ __global__ void __launch_bounds__(NT, 1)
     if (rep) report(a.status, LIN_ST_BAD_SLOT);
     return;
   }
-  const int64_t bos = a.cu_seqlens[r], eos = a.cu_seqlens[r + 1];
-  if (bos < 0 || eos < bos || eos > a.total_tokens) {
-    if (rep) report(a.status, LIN_ST_BAD_SEQLEN);
+  const int64_t bos_r = a.cu_seqlens[r], eos = a.cu_seqlens[r + 1];
+  if (bos_r < 0 || eos < bos_r || eos > a.total_tokens) {
+    if (rep && seg == 0) report(a.status, LIN_ST_BAD_SEQLEN);
     return;
   }
-  const int P = a.prefix_len[r];
-  if (P < 0 || (P & 63)) {
-    if (rep) report(a.status, LIN_ST_BAD_PREFIX);
+  const int P_r = a.prefix_len[r];
+  if (P_r < 0 || (P_r & 63)) {
+    if (rep && seg == 0) report(a.status, LIN_ST_BAD_PREFIX);
     return;
   }
+  // the tokens this CTA runs: the request, or one segment of it
+  int64_t bos = bos_r, eos_c = eos;
+  if (seg_mode) {
+    bos = bos_r + int64_t(seg) * p.seg_len;
+    if (bos >= eos) return;
+    eos_c = (eos - bos) < p.seg_len ? eos : bos + p.seg_len;
+  }
+  const int P = P_r + static_cast<int>(bos - bos_r);  // tokens before bos in absolute positions
+  const bool seg_last = (eos_c == eos);               // this CTA ends the request
+  const bool outputs_on = seg_mode == kSegOff || seg_mode == kSegFinal;
+  const bool state_to_ws = seg_mode == kSegOffset || seg_mode == kSegTransition;
   int t0 = 0, ntr = 0;
-  if (a.track_stride > 0 && a.cu_track) {
+  if (outputs_on && a.track_stride > 0 && a.cu_track) {
     t0 = a.cu_track[r];
     ntr = a.cu_track[r + 1] - t0;
     for (int i = 0; i < ntr; ++i) {
       const int t = a.track_slots[t0 + i];
       if (t >= pool.num_slots) {
-        if (rep) report(a.status, LIN_ST_BAD_SLOT);
+        if (rep && seg == 0) report(a.status, LIN_ST_BAD_SLOT);
         return;
       }
       if (t == slot) {
-        if (rep) report(a.status, LIN_ST_TRACK_ALIAS);
+        if (rep && seg == 0) report(a.status, LIN_ST_TRACK_ALIAS);
         return;
       }
     }
   }
-  const bool warm = a.has_initial_state[r] != 0;
-  const int L = static_cast<int>(eos - bos);
+  // initial state: 0 zeros, 1 the slot, 2 identity, 3 the segment workspace
+  const bool warm_r = a.has_initial_state[r] != 0;
+  int init_kind = warm_r ? 1 : 0;
+  if (seg > 0) init_kind = seg_mode == kSegOffset ? 0 : (seg_mode == kSegTransition ? 2 : 3);
+  const bool warm = init_kind == 1;
+  const bool zero_v = seg_mode == kSegTransition;  // transition runs take no value input
+  const int L = static_cast<int>(eos_c - bos);
   const int nch = (L + CH - 1) / CH;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
   const int64_t head_bytes = int64_t(DH) * DH * ES;
@@ -404,7 +438,10 @@ __global__ void __launch_bounds__(NT, 1)
         load_elem(a.conv_w, int64_t(head_channel(i >> 2, h, H)) * 4 + (i & 3), a.io_dtype);
   for (int i = tid; i < 3 * 384; i += NT) {
     const int rr = i / 384, cl = i % 384;
-    HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
+    if (seg > 0)  // the 3 inputs before the segment
+      HALO[i] = load_elem(a.x, (bos - 3 + rr) * int64_t(pool.conv_channels) + head_channel(cl, h, H), LIN_BF16);
+    else
+      HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
   }
 
   if (nch == 0) {
@@ -454,9 +491,16 @@ __global__ void __launch_bounds__(NT, 1)
           s[4 * m] = u.x; s[4 * m + 1] = u.y; s[4 * m + 2] = u.z; s[4 * m + 3] = u.w;
         }
       }
+    } else if (init_kind == 3) {
+      const float* src = p.seg_state_in + ((int64_t(seg - 1) * H + h) * DH + vrow) * DH + cc;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float4 u = *reinterpret_cast<const float4*>(src + 4 * m);
+        s[4 * m] = u.x; s[4 * m + 1] = u.y; s[4 * m + 2] = u.z; s[4 * m + 3] = u.w;
+      }
     } else {
 #pragma unroll
-      for (int m = 0; m < 32; ++m) s[m] = 0.f;
+      for (int m = 0; m < 32; ++m) s[m] = (init_kind == 2 && cc + m == vrow) ? 1.f : 0.f;
     }
     umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), s);
     put32<BF>(sb + OFF_SOP, 128, vrow, cc, s, 1.f);
@@ -470,7 +514,8 @@ __global__ void __launch_bounds__(NT, 1)
   load_gates<KDA>(a, bos, L < CH ? L : CH, h, H, warp, lane, gk, bt);
 
   uint32_t ph_mma = 0;
-  int snap = 0;
+  // boundaries snapshotted before bos by earlier segments of this request
+  int snap = (ntr > 0 && seg > 0) ? static_cast<int>(P / a.track_stride - P_r / a.track_stride) : 0;
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2_on = a.flags & LIN_QK_L2NORM;
 
@@ -672,7 +717,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int e = 0; e < 4; ++e) {
           kn[e] = ok ? yk[i][e] * rk[i] : 0.f;
           qn[e] = ok ? yq[i][e] * rq[i] : 0.f;
-          vv[e] = ok ? yv[i][e] : 0.f;
+          vv[e] = (ok && !zero_v) ? yv[i][e] : 0.f;
         }
         float eL[4], eR[4], eH[4], eT[4];
 #pragma unroll
@@ -1037,7 +1082,7 @@ __global__ void __launch_bounds__(NT, 1)
     {
       const bool full = (n == CH);
       const int oes = a.out_dtype == LIN_BF16 ? 2 : 4;
-      {
+      if (outputs_on) {
         float o16[16];
         umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), o16);
         if (full) {
@@ -1077,12 +1122,21 @@ __global__ void __launch_bounds__(NT, 1)
         ++snap;
       }
       const bool last = (j == nch - 1);
-      const bool store_state = snap_dst >= 0 || last;
+      // the final state goes to the slot when this CTA ends the request (and
+      // runs with outputs); segment state runs write it to the workspace
+      const bool last_to_slot = last && outputs_on && seg_last;
+      const bool store_state = snap_dst >= 0 || last_to_slot;
       {
         float v[32];
         const int cc = slice * 32;
         umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
-        put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
+        if (!last) put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
+        if (last && state_to_ws) {
+          float* dst = p.seg_state_out + ((int64_t(seg) * H + h) * DH + vrow) * DH + cc;
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+        }
         if (store_state) {
           // state tile of 32 rows x 128 bytes, 128-byte swizzle (chunk m of row r at m ^ (r % 8))
           if (ST == LIN_BF16) {
@@ -1119,14 +1173,14 @@ __global__ void __launch_bounds__(NT, 1)
           const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
           const int64_t off = int64_t(ch) * 3 + m;
           if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
-          if (last) store_elem(slot_c, off, pool.conv_dtype, wv);
+          if (last_to_slot) store_elem(slot_c, off, pool.conv_dtype, wv);
         }
       }
       umma::fence_smem_to_async();
       umma::fence_before_sync();
       __syncthreads();
       if (tid == 0) {
-        if (full) tma_store_3d(&tmap_out, sb + OFF_OSTG, 0, h, static_cast<int>(row0));
+        if (full && outputs_on) tma_store_3d(&tmap_out, sb + OFF_OSTG, 0, h, static_cast<int>(row0));
         if (store_state) {
           constexpr int KB = ST == LIN_BF16 ? 64 : 32;  // key channels per tile
           constexpr int NKB = DH / KB;
@@ -1134,7 +1188,7 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t src = sb + OFF_STG + tq * 4096;
             const int v0 = (tq / NKB) * 32, k0 = (tq % NKB) * KB;
             if (snap_dst >= 0) tma_store_4d(&tmap_state, src, k0, v0, h, snap_dst);
-            if (last) tma_store_4d(&tmap_state, src, k0, v0, h, slot);
+            if (last_to_slot) tma_store_4d(&tmap_state, src, k0, v0, h, slot);
           }
         }
         bulk_commit();
@@ -1171,9 +1225,93 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Carries the true state across the segments of a long request:
+// S_{k+1} = S_k M_k + B_k for k = 1 .. nseg - 2, where buf[k] holds B_k on entry
+// (buf[0] holds S_1, the offset run of segment 0 from the request's own initial
+// state) and S_{k+1} on exit, and mbuf[k] holds M_k. Rows of S evolve
+// independently, so CTA (head, 16-row block) runs the whole scan for its rows.
+constexpr int kScanRows = 16;
+constexpr int kScanThreads = 256;
+constexpr size_t kScanSmem = (size_t(DH) * DH + size_t(kScanRows) * DH) * sizeof(float);
+
+__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(float* buf, const float* mbuf, int nseg, int H) {
+  extern __shared__ __align__(16) float ssm[];
+  float* Msh = ssm;             // M_k, 128 x 128
+  float* Ssh = ssm + DH * DH;   // this CTA's rows of S_k, 16 x 128
+  const int h = blockIdx.x / (DH / kScanRows), rb = blockIdx.x % (DH / kScanRows);
+  const int tid = threadIdx.x;
+  const int row = tid / 16, c0 = (tid % 16) * 8;  // one row, 8 columns per thread
+  const int64_t head_elems = int64_t(DH) * DH;
+  auto at = [&](const float* base, int k) { return base + (int64_t(k) * H + h) * head_elems; };
+  auto atw = [&](float* base, int k) { return base + (int64_t(k) * H + h) * head_elems; };
+  for (int i = tid; i < kScanRows * DH / 4; i += kScanThreads)
+    reinterpret_cast<float4*>(Ssh)[i] = reinterpret_cast<const float4*>(at(buf, 0) + int64_t(rb) * kScanRows * DH)[i];
+  for (int k = 1; k + 1 < nseg; ++k) {
+    const float4* msrc = reinterpret_cast<const float4*>(at(mbuf, k));
+    for (int i = tid; i < DH * DH / 4; i += kScanThreads) reinterpret_cast<float4*>(Msh)[i] = msrc[i];
+    float* brow = atw(buf, k) + int64_t(rb * kScanRows + row) * DH + c0;
+    const float4 b0 = reinterpret_cast<const float4*>(brow)[0], b1 = reinterpret_cast<const float4*>(brow)[1];
+    float acc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    __syncthreads();
+#pragma unroll 4
+    for (int m = 0; m < DH; ++m) {
+      const float sv = Ssh[row * DH + m];
+      const float4 m0 = *reinterpret_cast<const float4*>(Msh + m * DH + c0);
+      const float4 m1 = *reinterpret_cast<const float4*>(Msh + m * DH + c0 + 4);
+      acc[0] = fmaf(sv, m0.x, acc[0]);
+      acc[1] = fmaf(sv, m0.y, acc[1]);
+      acc[2] = fmaf(sv, m0.z, acc[2]);
+      acc[3] = fmaf(sv, m0.w, acc[3]);
+      acc[4] = fmaf(sv, m1.x, acc[4]);
+      acc[5] = fmaf(sv, m1.y, acc[5]);
+      acc[6] = fmaf(sv, m1.z, acc[6]);
+      acc[7] = fmaf(sv, m1.w, acc[7]);
+    }
+    __syncthreads();  // every read of S_k and M_k is done
+    reinterpret_cast<float4*>(Ssh + row * DH + c0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4*>(Ssh + row * DH + c0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    reinterpret_cast<float4*>(brow)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4*>(brow)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncthreads();
+  }
+}
+
+// Segments for one long request: enough (segment, head) CTAs to fill every SM
+// about six times, each segment a whole number of chunks (at least 4).
+struct SegPlan {
+  int nseg = 0, seg_len = 0;
+};
+
+SegPlan segment_plan(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
+  SegPlan sp;
+  if (a.batch != 1 || (a.flags & LIN_PREFILL_RECURRENT)) return sp;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return sp;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return sp;
+  const int64_t nch = (a.total_tokens + CH - 1) / CH;
+  const bool forced = (a.flags & LIN_PREFILL_SEGMENTED) != 0;
+  const bool want = forced ? nch >= 8 : (int64_t(pool.num_heads) * 4 <= sms && nch >= 64);
+  if (!want) return sp;
+  const int64_t target = int64_t(6) * sms;
+  int64_t seg_ch = (nch * pool.num_heads + target - 1) / target;
+  if (seg_ch < 4) seg_ch = 4;
+  const int64_t nseg = (nch + seg_ch - 1) / seg_ch;
+  if (nseg < 2 || nseg * pool.num_heads >= (int64_t(1) << 31) || seg_ch * CH >= (int64_t(1) << 30))
+    return sp;
+  sp.nseg = static_cast<int>(nseg);
+  sp.seg_len = static_cast<int>(seg_ch * CH);
+  return sp;
+}
+
+size_t segment_workspace(const lin_state_pool_t& pool, const SegPlan& sp) {
+  if (sp.nseg < 2) return 0;
+  return 2 * size_t(sp.nseg) * pool.num_heads * DH * DH * sizeof(float);
+}
+
 template <bool KDA, int ST>
 cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
-                     cudaStream_t s) {
+                     const SegPlan& sp, float* seg_buf, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmap;
@@ -1235,8 +1373,31 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
     cudaError_t e2 = cudaGetLastError();
     if (e2 != cudaSuccess) return e2;
   }
-  ChunkParams p{pool, a, order};
-  const unsigned grid = static_cast<unsigned>(a.batch) * static_cast<unsigned>(pool.num_heads);
+  const unsigned H = static_cast<unsigned>(pool.num_heads);
+  if (sp.nseg >= 2 && seg_buf) {
+    // one long request in segments: offset runs (segments 0 .. n-2) and
+    // transition runs (1 .. n-2), the scan, then the final runs (all)
+    float* bbuf = seg_buf;
+    float* mbuf = seg_buf + size_t(sp.nseg) * H * DH * DH;
+    ChunkParams p1{pool, a, nullptr, kSegOffset, sp.seg_len, 0, bbuf, nullptr};
+    kern<<<unsigned(sp.nseg - 1) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (sp.nseg > 2) {
+      ChunkParams p2{pool, a, nullptr, kSegTransition, sp.seg_len, 1, mbuf, nullptr};
+      kern<<<unsigned(sp.nseg - 2) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p2);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kScanSmem))) != cudaSuccess)
+        return e;
+      seg_scan_kernel<<<H * (DH / kScanRows), kScanThreads, kScanSmem, s>>>(bbuf, mbuf, sp.nseg, int(H));
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    ChunkParams p3{pool, a, nullptr, kSegFinal, sp.seg_len, 0, nullptr, bbuf};
+    kern<<<unsigned(sp.nseg) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p3);
+    return cudaGetLastError();
+  }
+  ChunkParams p{pool, a, order, kSegOff, 0, 0, nullptr, nullptr};
+  const unsigned grid = static_cast<unsigned>(a.batch) * H;
   kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p);
   return cudaGetLastError();
 }
@@ -1250,23 +1411,44 @@ bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_a
          (reinterpret_cast<uintptr_t>(a.g) & 15) == 0 && encode_fn() != nullptr;
 }
 
-// Workspace: the longest-first order of the batch (int32 per request) when
-// the batch has more than one request and fits the sorting kernel.
-size_t chunked_prefill_workspace(const lin_state_pool_t&, const lin_prefill_args_t& a) {
+namespace {
+// The longest-first order of the batch (int32 per request) when the batch has
+// more than one request and fits the sorting kernel.
+size_t order_workspace(const lin_prefill_args_t& a) {
   if (a.batch <= 1 || a.batch > kOrderMax) return 0;
   return (static_cast<size_t>(a.batch) * sizeof(int32_t) + 255) & ~size_t(255);
 }
 
-cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
-                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  int32_t* order = nullptr;
-  if (chunked_prefill_workspace(pool, a) > 0 && workspace &&
-      workspace_bytes >= chunked_prefill_workspace(pool, a))
-    order = static_cast<int32_t*>(workspace);
+cudaError_t launch_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
+                           const SegPlan& sp, float* seg_buf, cudaStream_t stream) {
   const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
   const bool bf = pool.state_dtype == LIN_BF16;
-  if (kda) return bf ? launch_t<true, LIN_BF16>(pool, a, order, stream) : launch_t<true, LIN_F32>(pool, a, order, stream);
-  return bf ? launch_t<false, LIN_BF16>(pool, a, order, stream) : launch_t<false, LIN_F32>(pool, a, order, stream);
+  if (kda)
+    return bf ? launch_t<true, LIN_BF16>(pool, a, order, sp, seg_buf, stream)
+              : launch_t<true, LIN_F32>(pool, a, order, sp, seg_buf, stream);
+  return bf ? launch_t<false, LIN_BF16>(pool, a, order, sp, seg_buf, stream)
+            : launch_t<false, LIN_F32>(pool, a, order, sp, seg_buf, stream);
+}
+}  // namespace
+
+// Workspace: the batch order (varlen batches), or the per-segment states of a
+// long single request run in segments.
+size_t chunked_prefill_workspace(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
+  return order_workspace(a) + segment_workspace(pool, segment_plan(pool, a));
+}
+
+cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const size_t ow = order_workspace(a);
+  int32_t* order = (ow > 0 && workspace && workspace_bytes >= ow) ? static_cast<int32_t*>(workspace) : nullptr;
+  SegPlan sp = segment_plan(pool, a);
+  float* seg_buf = nullptr;
+  const size_t sw = segment_workspace(pool, sp);
+  if (sw > 0 && workspace && workspace_bytes >= ow + sw)
+    seg_buf = reinterpret_cast<float*>(static_cast<char*>(workspace) + ow);
+  else
+    sp = SegPlan{};  // too little workspace: run the request in one piece
+  return launch_chunked(pool, a, order, sp, seg_buf, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1300,8 +1482,8 @@ cudaError_t launch_prefill_noalloc(const lin_state_pool_t& pool, const lin_prefi
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev].store(ptr, std::memory_order_release);
   }
-  const size_t need = chunked_prefill_workspace(pool, a);
-  return launch_prefill_chunked(pool, a, need ? ptr : nullptr, need, stream);
+  const size_t need = order_workspace(a);
+  return launch_chunked(pool, a, need ? ptr : nullptr, SegPlan{}, nullptr, stream);
 }
 
 }  // namespace lin

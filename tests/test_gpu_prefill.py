@@ -104,6 +104,42 @@ def test_qwen35_gdn_reduced(path):
     compare_slots(pool, op, [1, 2, 3, 4, 5, 6], TOL_F32)
 
 
+@pytest.mark.parametrize("gate", [W.GATE_PER_KEY, W.GATE_PER_HEAD])
+def test_single_request_in_segments(gate):
+    """A batch of one long request run as parallel segments (offset and
+    transition runs, the fp32 scan, final runs) equals the oracle: a warm
+    start at a 64-multiple prefix, a ragged last segment, snapshots every 64
+    into distinct slots that cross segment boundaries, outputs, the final state
+    and conv window; and it equals the same call run in one piece."""
+    dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
+    L_, P_ = 1500, 128
+    b = W.make_prefill_batch(dims, [L_], gate, dtype=torch.bfloat16, seed=4,
+                             gate="softplus" if gate == W.GATE_PER_KEY else "uniform", tag="seg",
+                             prefixes=[P_], warm=[1])
+    sdt = torch.bfloat16 if gate == W.GATE_PER_KEY else torch.float32
+    n_tr = (P_ + L_) // 64 - P_ // 64
+    pool = L.StatePool(1, 2 + n_tr, 2, 128, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV)
+    fill_pool(pool, 4, std=0.1)
+    ref = L.StatePool(1, 2 + n_tr, 2, 128, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV,
+                      temporal=pool.temporal.clone(), conv=pool.conv.clone())
+    op = oracle_pool(pool)
+    tracks = list(range(2, 2 + n_tr))
+    tol = TOL_BF16 if gate == W.GATE_PER_KEY else TOL_F32
+    out, oo = run_both(pool, op, b, [1], tracks, [0, n_tr], 64, "chunked",
+                       out_dtype=torch.float32, flags=FLAGS | L.LIN_PREFILL_SEGMENTED)
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), tol)
+    compare_slots(pool, op, [1] + tracks, tol)
+    # one piece (no segments) on a copy: the same placement, values within rounding
+    out1 = torch.zeros_like(out)
+    kw = dict(layer=0, x=b.x.to(DEV), conv_w=b.conv_w.to(DEV), g=b.g.to(DEV), beta=b.beta.to(DEV),
+              out=out1, cu_seqlens=b.cu_seqlens.to(DEV), prefix_len=b.prefix_len.to(DEV),
+              slot=_i32([1]), has_initial_state=b.has_initial_state.to(DEV), track_slots=_i32(tracks),
+              cu_track=_i32([0, n_tr]), track_stride=64, gate_mode=gate, flags=FLAGS)
+    L.lin_state_prefill(ref, **kw)
+    assert torch.equal(pool.conv, ref.conv)  # windows are copies of inputs: bit-exact
+    assert (out - out1).norm() <= tol * out1.norm()
+
+
 @pytest.mark.parametrize("path", list(PATHS))
 def test_gdn_strong_decay(path):
     """GDN with log-decay U[-12, 0] per (token, head): 16 consecutive tokens can
