@@ -70,6 +70,12 @@ extern "C" {
 #define LIN_ST_COPY_ALIAS 16   /* LIN_VALIDATE: a copy dst is another pair's dst or src */
 #define LIN_ST_TIMEOUT 32      /* a bounded device wait gave up               */
 #define LIN_ST_BAD_ACCEPT 64   /* commit accept_len outside [0, n_draft]      */
+#define LIN_ST_DECAY_RANGE 128 /* KDA chunked prefill: some key channel decays
+                                  by more than e^80 across half a chunk (mean
+                                  log-decay below -2.5 per token), outside the
+                                  range of the chunk's factored decay; that
+                                  request's results are not valid: rerun it
+                                  with LIN_PREFILL_RECURRENT                   */
 
 /* ---- enums ------------------------------------------------------------- */
 typedef enum { LIN_F32 = 0, LIN_BF16 = 1 } lin_dtype_t;

@@ -708,6 +708,7 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
+      bool range_bad = false;
 #pragma unroll
       for (int i = 0; i < TPW; ++i) {
         const int t = tfirst + i;
@@ -728,6 +729,8 @@ __global__ void __launch_bounds__(NT, 1)
           eT[e] = __expf(blast[ee] - b);
           eL[e] = KDA ? __expf(b - bref[ee]) : 1.f;
           eR[e] = KDA ? __expf(bref[ee] - b) : 1.f;
+          // the factored decay must stay inside fp32 range (see LIN_ST_DECAY_RANGE)
+          if (KDA && ok && fabsf(b - bref[ee]) > 80.f) range_bad = true;
         }
         const int c = lane * 4;
         if (SPLIT) {
@@ -748,6 +751,7 @@ __global__ void __launch_bounds__(NT, 1)
         put4<BF>(sb + OFF_QH, 64, t, c, qn[0] * eH[0], qn[1] * eH[1], qn[2] * eH[2], qn[3] * eH[3]);
         put4<BF>(sb + OFF_KT, 64, t, c, kn[0] * eT[0], kn[1] * eT[1], kn[2] * eT[2], kn[3] * eT[3]);
       }
+      if (KDA && __any_sync(0xffffffffu, range_bad) && lane == 0) report(a.status, LIN_ST_DECAY_RANGE);
     }
     umma::fence_smem_to_async();
     __syncthreads();

@@ -140,6 +140,31 @@ def test_single_request_in_segments(gate):
     assert (out - out1).norm() <= tol * out1.norm()
 
 
+def test_kda_decay_beyond_chunk_range_is_reported():
+    """KDA with log-decay -30 * softplus(N(0,1)) per key channel: across half a
+    chunk some channel decays by far more than e^80, outside the chunked
+    kernel's factored range. The chunked call must say so in the status
+    (LIN_ST_DECAY_RANGE) rather than return silently wrong values, and the
+    recurrent kernel must still match the oracle on the same inputs."""
+    dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
+    b = W.make_prefill_batch(dims, [200], W.GATE_PER_KEY, dtype=torch.bfloat16, seed=5,
+                             gate="softplus", tag="dr")
+    b.g = b.g * 30.0
+    pool = L.StatePool(1, 4, 2, 128, state_dtype=torch.bfloat16, conv_dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.zeros((200, 2, 128), device=DEV)
+    kw = dict(layer=0, x=b.x.to(DEV), conv_w=b.conv_w.to(DEV), g=b.g.to(DEV), beta=b.beta.to(DEV),
+              out=out, cu_seqlens=b.cu_seqlens.to(DEV), prefix_len=b.prefix_len.to(DEV), slot=_i32([1]),
+              has_initial_state=b.has_initial_state.to(DEV), track_slots=None, cu_track=None,
+              track_stride=0, gate_mode=W.GATE_PER_KEY, flags=FLAGS, status=st)
+    assert L.lin_state_prefill_kernel(pool, **kw) == L.LIN_KERNEL_CHUNKED
+    L.lin_state_prefill(pool, **kw)
+    assert L.lin_state_read_status(st) & L.LIN_ST_DECAY_RANGE
+    op = oracle_pool(pool)
+    out2, oo = run_both(pool, op, b, [2], [], [0, 0], 0, "recurrent", out_dtype=torch.float32)
+    compare_outputs(out2, oo, b.cu_seqlens.tolist(), TOL_BF16)
+
+
 @pytest.mark.parametrize("path", list(PATHS))
 def test_gdn_strong_decay(path):
     """GDN with log-decay U[-12, 0] per (token, head): 16 consecutive tokens can
