@@ -442,6 +442,17 @@ def time_steps(wl, steps, warmup, stream, flush=None):
     return t0.elapsed_time(t1), per, kern
 
 
+def reduce_over_ranks(rank_ms, units_per_rank, world, device):
+    """Whole-job figures of a step that every rank ran on its own replica:
+    the time is the slowest rank's (all-reduce MAX), the work is the sum over
+    ranks. Returns (ms, units per second)."""
+    if world > 1:
+        t = torch.tensor([rank_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        rank_ms = float(t.item())
+    return rank_ms, units_per_rank * world / (rank_ms / 1e3)
+
+
 def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=False):
     wl = make_workload(name, L, dev)
     # decode rotates 4 pool replicas: a replica's 108 MB working set is never
@@ -452,13 +463,8 @@ def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=Fals
     total_ms, per, kern = time_steps(wl, steps, warmup, stream,
                                      (lambda: flush_l2(flush_buf)) if need_flush else None)
     kern_ms = statistics.mean(kern)
-    rank_ms = statistics.mean(per)
-    if dist_info["world"] > 1:
-        t = torch.tensor([rank_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        rank_ms = float(t.item())
+    rank_ms, value = reduce_over_ranks(statistics.mean(per), wl.units_per_step(), dist_info["world"], dev)
     units = wl.units_per_step() * dist_info["world"]
-    value = units / (rank_ms / 1e3)
     achieved = wl.kernel_bytes_per_launch() / (kern_ms / 1e3) / 1e9
     res = {"value": value, "unit": wl.unit, "ms_per_step": rank_ms,
            "roofline": {"bound": "hbm", "kernel": wl.kernel, "achieved": achieved,
@@ -482,12 +488,9 @@ def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=Fals
             wl.step_e2e(i)
         t1.record(stream)
         torch.cuda.synchronize()
-        e_ms = t0.elapsed_time(t1) / steps
-        if dist_info["world"] > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        res["e2e"] = {"value": units / (e_ms / 1e3), "unit": wl.unit,
+        e_ms, e_val = reduce_over_ranks(t0.elapsed_time(t1) / steps, wl.units_per_step(),
+                                        dist_info["world"], dev)
+        res["e2e"] = {"value": e_val, "unit": wl.unit,
                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
     del wl
     torch.cuda.empty_cache()
