@@ -113,8 +113,10 @@ constexpr uint32_t TMEM_COLS = 256;
 // from the identity with zero values (their M: rows evolve independently, and a
 // zero value input drops the U' term), both writing only the fp32 state at the
 // segment's end; after the scan S_{k+1} = S_k M_k + B_k, mode 3 runs every
-// segment from its true initial state with outputs and snapshots.
-enum SegMode { kSegOff = 0, kSegOffset = 1, kSegTransition = 2, kSegFinal = 3 };
+// segment from its true initial state with outputs and snapshots. Segment 0's
+// offset run starts from the true state, so it also writes its outputs and
+// snapshots; the offset and transition runs share one launch.
+enum SegMode { kSegOff = 0, kSegOffset = 1, kSegTransition = 2, kSegFinal = 3, kSegOffsetAndTransition = 4 };
 
 struct ChunkParams {
   lin_state_pool_t pool;
@@ -122,8 +124,10 @@ struct ChunkParams {
   const int32_t* order;  // requests longest first (nullptr: batch order)
   int seg_mode;          // SegMode
   int seg_len;           // tokens per segment (multiple of 64)
-  int seg_first;         // segment of blockIdx.x < H
-  float* seg_state_out;        // modes 1, 2: fp32 state after the segment, [seg][H][V][K]
+  int seg_first;         // segment of blockIdx.x < H (modes 1 - 3)
+  int seg_count;         // segments of the request (mode 4: blocks of offset runs first)
+  float* seg_state_out;        // offset runs: fp32 state after the segment, [seg][H][V][K]
+  float* seg_trans_out;        // transition runs: likewise
   const float* seg_state_in;   // mode 3: fp32 state before segment k >= 1 at index k - 1
 };
 
@@ -349,8 +353,20 @@ __global__ void __launch_bounds__(NT, 1)
   const lin_state_pool_t& pool = p.pool;
   const lin_prefill_args_t& a = p.a;
   const int H = pool.num_heads;
-  const int seg_mode = p.seg_mode;
-  const int seg = seg_mode ? p.seg_first + static_cast<int>(blockIdx.x) / H : 0;
+  int seg_mode = p.seg_mode;
+  int seg = 0;
+  if (seg_mode == kSegOffsetAndTransition) {
+    const int nb1 = (p.seg_count - 1) * H;  // offset runs of segments 0 .. n-2 first
+    if (static_cast<int>(blockIdx.x) < nb1) {
+      seg_mode = kSegOffset;
+      seg = static_cast<int>(blockIdx.x) / H;
+    } else {
+      seg_mode = kSegTransition;
+      seg = 1 + (static_cast<int>(blockIdx.x) - nb1) / H;
+    }
+  } else if (seg_mode) {
+    seg = p.seg_first + static_cast<int>(blockIdx.x) / H;
+  }
   const int r = seg_mode ? 0 : (p.order ? p.order[blockIdx.x / H] : blockIdx.x / H);
   const int h = blockIdx.x % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -384,8 +400,9 @@ __global__ void __launch_bounds__(NT, 1)
   }
   const int P = P_r + static_cast<int>(bos - bos_r);  // tokens before bos in absolute positions
   const bool seg_last = (eos_c == eos);               // this CTA ends the request
-  const bool outputs_on = seg_mode == kSegOff || seg_mode == kSegFinal;
+  const bool outputs_on = seg_mode == kSegOff || seg_mode == kSegFinal || (seg_mode == kSegOffset && seg == 0);
   const bool state_to_ws = seg_mode == kSegOffset || seg_mode == kSegTransition;
+  float* state_ws = seg_mode == kSegTransition ? p.seg_trans_out : p.seg_state_out;
   int t0 = 0, ntr = 0;
   if (outputs_on && a.track_stride > 0 && a.cu_track) {
     t0 = a.cu_track[r];
@@ -1136,7 +1153,7 @@ __global__ void __launch_bounds__(NT, 1)
         umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
         if (!last) put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
         if (last && state_to_ws) {
-          float* dst = p.seg_state_out + ((int64_t(seg) * H + h) * DH + vrow) * DH + cc;
+          float* dst = state_ws + ((int64_t(seg) * H + h) * DH + vrow) * DH + cc;
 #pragma unroll
           for (int m = 0; m < 8; ++m)
             *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
@@ -1383,24 +1400,23 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
     // transition runs (1 .. n-2), the scan, then the final runs (all)
     float* bbuf = seg_buf;
     float* mbuf = seg_buf + size_t(sp.nseg) * H * DH * DH;
-    ChunkParams p1{pool, a, nullptr, kSegOffset, sp.seg_len, 0, bbuf, nullptr};
-    kern<<<unsigned(sp.nseg - 1) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p1);
+    // offset runs of segments 0 .. n-2 (segment 0 also with its outputs and
+    // snapshots) and transition runs of segments 1 .. n-2, one launch
+    ChunkParams p1{pool, a, nullptr, kSegOffsetAndTransition, sp.seg_len, 0, sp.nseg, bbuf, mbuf, nullptr};
+    kern<<<unsigned(2 * sp.nseg - 3) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (sp.nseg > 2) {
-      ChunkParams p2{pool, a, nullptr, kSegTransition, sp.seg_len, 1, mbuf, nullptr};
-      kern<<<unsigned(sp.nseg - 2) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p2);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
       if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kScanSmem))) != cudaSuccess)
         return e;
       seg_scan_kernel<<<H * (DH / kScanRows), kScanThreads, kScanSmem, s>>>(bbuf, mbuf, sp.nseg, int(H));
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    ChunkParams p3{pool, a, nullptr, kSegFinal, sp.seg_len, 0, nullptr, bbuf};
-    kern<<<unsigned(sp.nseg) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p3);
+    ChunkParams p3{pool, a, nullptr, kSegFinal, sp.seg_len, 1, sp.nseg, nullptr, nullptr, bbuf};
+    kern<<<unsigned(sp.nseg - 1) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p3);
     return cudaGetLastError();
   }
-  ChunkParams p{pool, a, order, kSegOff, 0, 0, nullptr, nullptr};
+  ChunkParams p{pool, a, order, kSegOff, 0, 0, 0, nullptr, nullptr, nullptr};
   const unsigned grid = static_cast<unsigned>(a.batch) * H;
   kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p);
   return cudaGetLastError();
