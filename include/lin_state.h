@@ -223,7 +223,11 @@ typedef struct {
  *   "--mamba-track-interval": prompt 1000, interval 256 -> 1024, 1280, ...).
  * n_draft > 1 (verify, [MRC] 8.3): the tokens run in order from the slot
  *   state; the state after draft step j goes to spec row r, step j; the slot
- *   is not modified and nothing is tracked (commit does that).
+ *   is not modified and nothing is tracked (commit does that). With no spec
+ *   buffer (spec.temporal and spec.conv both NULL) only the outputs are
+ *   written: the replay form of speculative decoding, where
+ *   lin_state_replay_commit later re-runs the accepted prefix ([K3]
+ *   "ReplaySSM"; [MRC] 9).
  * The state is rounded to the pool dtype after every token, so a verify
  *   step equals the same number of single-token decodes bit for bit.
  * Inputs (device): x [batch][n_draft][C] io_dtype, g [batch][n_draft][H]
@@ -284,6 +288,43 @@ typedef struct {
 
 LIN_API int lin_state_spec_commit(const lin_state_pool_t* pool, const lin_commit_args_t* args,
                           void* stream);
+
+/* ---- replay commit ([K3] "ReplaySSM" exact-fold; [MRC] 9.2 - 9.10) -------
+ * The commit of a verify that kept no per-step states: for each request r,
+ * the first a = accept_len[r] (0..n_draft) of its n_draft draft tokens run
+ * again, in order, from the state in slot[r] of `layer`, with the same inputs
+ * the verify call had (x [batch][n_draft][C], g, beta as in lin_decode_args_t;
+ * only the accepted rows are read), and the state and conv window after them
+ * replace the slot's; no outputs are written. A boundary crossed on the way
+ * ((pos[r] + j + 1) % track_interval == 0, track_slot[r] >= 0) snapshots the
+ * state and window there into track_slot[r] ([MRC] 9.10), so the track slot
+ * ends up as lin_state_spec_commit leaves it. The arithmetic is the decode
+ * kernel's, token by token with the state rounded to the pool dtype after
+ * each token, so the slot equals what the per-step-state path commits, bit
+ * for bit. a == 0 leaves the slot unchanged. x, conv_w, g must be 16-byte
+ * aligned; the staging limit of lin_state_decode applies to n_draft. */
+typedef struct {
+  int32_t layer;
+  int32_t batch;
+  int32_t n_draft;
+  int32_t io_dtype;  /* x, conv_w */
+  int32_t gate_mode;
+  uint32_t flags;
+  float q_scale;
+  int32_t track_interval; /* 0 = never track */
+  const void* x;
+  const void* conv_w;
+  const float* g;
+  const float* beta;
+  const int32_t* slot;       /* device [batch] */
+  const int32_t* pos;        /* device [batch]: tokens already in the slot's state */
+  const int32_t* accept_len; /* device [batch] */
+  const int32_t* track_slot; /* device [batch] or NULL */
+  int32_t* status;
+} lin_replay_args_t;
+
+LIN_API int lin_state_replay_commit(const lin_state_pool_t* pool, const lin_replay_args_t* args,
+                                    void* stream);
 
 /* ---- batched slot copies ([MRC] 3.2 copy_from / COW; [PP] fork_from) ----
  * For i < n and every layer in [layer_begin, layer_end):

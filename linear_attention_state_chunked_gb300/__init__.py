@@ -33,7 +33,7 @@ LIN_KERNEL_RECURRENT, LIN_KERNEL_CHUNKED = 0, 1
 
 EXPORTED = (
     "lin_state_prefill_kernel", "lin_state_prefill_workspace", "lin_state_prefill_noalloc", "lin_state_prefill", "lin_state_decode",
-    "lin_state_spec_commit", "lin_state_copy_slots", "lin_state_restore",
+    "lin_state_spec_commit", "lin_state_replay_commit", "lin_state_copy_slots", "lin_state_restore",
     "lin_state_slot_bytes", "lin_state_read_status", "lin_state_strerror",
     "lin_state_last_error", "lin_state_version", "lin_state_selftest_mma",
 )
@@ -92,6 +92,17 @@ class DecodeArgsT(ctypes.Structure):
     ]
 
 
+class ReplayArgsT(ctypes.Structure):
+    _fields_ = [
+        ("layer", ctypes.c_int32), ("batch", ctypes.c_int32), ("n_draft", ctypes.c_int32),
+        ("io_dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("q_scale", ctypes.c_float), ("track_interval", ctypes.c_int32),
+        ("x", ctypes.c_void_p), ("conv_w", ctypes.c_void_p), ("g", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("slot", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+        ("accept_len", ctypes.c_void_p), ("track_slot", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
 class CommitArgsT(ctypes.Structure):
     _fields_ = [
         ("layer_begin", ctypes.c_int32), ("layer_end", ctypes.c_int32),
@@ -126,6 +137,8 @@ def _load():
     lib.lin_state_decode.restype = ctypes.c_int
     lib.lin_state_spec_commit.argtypes = [P(PoolT), P(CommitArgsT), vp]
     lib.lin_state_spec_commit.restype = ctypes.c_int
+    lib.lin_state_replay_commit.argtypes = [P(PoolT), P(ReplayArgsT), vp]
+    lib.lin_state_replay_commit.restype = ctypes.c_int
     lib.lin_state_copy_slots.argtypes = [P(PoolT), vp, vp, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_uint32, vp, vp]
     lib.lin_state_copy_slots.restype = ctypes.c_int
@@ -325,7 +338,9 @@ def lin_state_decode(pool: StatePool, *, layer: int, x, conv_w, g, beta, out, sl
                      track_slot=None, track_interval: int = 0, spec: Optional[SpecBuffer] = None,
                      gate_mode: int = LIN_GATE_PER_KEY, flags: int = LIN_QK_L2NORM | LIN_CONV_SILU,
                      q_scale: float = 1.0, status=None, stream=None) -> None:
-    """Calls lin_state_decode. x [B][n_draft][C]; n_draft > 1 needs `spec`."""
+    """Calls lin_state_decode. x [B][n_draft][C]; with n_draft > 1 the per-step
+    states go to `spec`, or, with spec None, only the outputs are written (the
+    replay form: lin_state_replay_commit then runs the accepted prefix)."""
     a = DecodeArgsT()
     a.layer, a.batch, a.n_draft = layer, x.shape[0], x.shape[1]
     a.io_dtype, a.out_dtype = dtype_code(x.dtype), dtype_code(out.dtype)
@@ -354,6 +369,25 @@ def lin_state_spec_commit(pool: StatePool, *, spec: SpecBuffer, slot, pos, accep
     a.status = status.data_ptr() if status is not None else None
     _check(lib.lin_state_spec_commit(ctypes.byref(pool.desc()), ctypes.byref(a), _stream(stream)),
            "lin_state_spec_commit")
+
+
+def lin_state_replay_commit(pool: StatePool, *, layer: int, x, conv_w, g, beta, slot, pos,
+                            accept_len, track_slot=None, track_interval: int = 0,
+                            gate_mode: int = LIN_GATE_PER_KEY,
+                            flags: int = LIN_QK_L2NORM | LIN_CONV_SILU, q_scale: float = 1.0,
+                            status=None, stream=None) -> None:
+    """Calls lin_state_replay_commit: runs the first accept_len[r] of request r's
+    n_draft tokens (x [B][n_draft][C], the verify call's inputs) into its slot."""
+    a = ReplayArgsT()
+    a.layer, a.batch, a.n_draft = layer, x.shape[0], x.shape[1]
+    a.io_dtype, a.gate_mode, a.flags = dtype_code(x.dtype), gate_mode, flags
+    a.q_scale, a.track_interval = q_scale, track_interval
+    a.x, a.conv_w, a.g, a.beta = (t.data_ptr() for t in (x, conv_w, g, beta))
+    a.slot, a.pos, a.accept_len = slot.data_ptr(), pos.data_ptr(), accept_len.data_ptr()
+    a.track_slot = track_slot.data_ptr() if track_slot is not None else None
+    a.status = status.data_ptr() if status is not None else None
+    _check(lib.lin_state_replay_commit(ctypes.byref(pool.desc()), ctypes.byref(a), _stream(stream)),
+           "lin_state_replay_commit")
 
 
 def lin_state_copy_slots(pool: StatePool, src, dst, layer_begin: int = 0,

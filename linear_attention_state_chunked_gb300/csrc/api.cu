@@ -236,15 +236,62 @@ int lin_state_decode(const lin_state_pool_t* pool, const lin_decode_args_t* a, v
     return fail(LIN_EINVAL, "decode: x / conv_w / g / beta / out / slot / pos is NULL");
   if (!aligned16(a->x) || !aligned16(a->conv_w) || !aligned16(a->g) || !aligned16(a->out))
     return fail(LIN_EINVAL, "decode: x, conv_w, g and out must be 16-byte aligned");
-  if (a->n_draft > 1) {
+  // n_draft > 1 with no spec buffer at all: a verify that writes outputs only
+  const bool spec_less = a->spec.temporal == nullptr && a->spec.conv == nullptr;
+  if (a->n_draft > 1 && !spec_less) {
     rc = check_spec(pool, a->spec, a->batch, a->n_draft, a->layer + 1);
     if (rc) return rc;
   }
   if (lin::decode_stage_bytes(*pool, *a) > lin::kDecodeMaxStage)
     return fail(LIN_EUNSUPPORTED, "decode: n_draft %d stages %d bytes per (request, head), over %d",
                 a->n_draft, lin::decode_stage_bytes(*pool, *a), lin::kDecodeMaxStage);
-  cudaError_t e = lin::launch_decode(*pool, *a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = lin::launch_decode(*pool, *a, nullptr, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lin_state_decode launch");
+  return ok();
+}
+
+int lin_state_replay_commit(const lin_state_pool_t* pool, const lin_replay_args_t* a, void* stream) {
+  int rc = check_pool(pool);
+  if (rc) return rc;
+  if (!a) return fail(LIN_EINVAL, "replay commit args is NULL");
+  if (a->layer < 0 || a->layer >= pool->num_layers)
+    return fail(LIN_EINVAL, "replay commit: layer %d outside [0, %d)", a->layer, pool->num_layers);
+  if (a->batch < 0 || a->batch > 65535) return fail(LIN_EINVAL, "replay commit: batch outside [0, 65535]");
+  if (a->n_draft < 1) return fail(LIN_EINVAL, "replay commit: n_draft must be >= 1");
+  if (!valid_dtype(a->io_dtype)) return fail(LIN_EINVAL, "replay commit: io_dtype");
+  if (a->gate_mode != LIN_GATE_PER_HEAD && a->gate_mode != LIN_GATE_PER_KEY)
+    return fail(LIN_EINVAL, "replay commit: gate_mode");
+  if (a->track_interval < 0) return fail(LIN_EINVAL, "replay commit: negative track_interval");
+  if (a->batch == 0) return ok();
+  if (!a->x || !a->conv_w || !a->g || !a->beta || !a->slot || !a->pos || !a->accept_len)
+    return fail(LIN_EINVAL, "replay commit: x / conv_w / g / beta / slot / pos / accept_len is NULL");
+  if (!aligned16(a->x) || !aligned16(a->conv_w) || !aligned16(a->g))
+    return fail(LIN_EINVAL, "replay commit: x, conv_w and g must be 16-byte aligned");
+  lin_decode_args_t d;
+  memset(&d, 0, sizeof(d));
+  d.layer = a->layer;
+  d.batch = a->batch;
+  d.n_draft = a->n_draft;
+  d.io_dtype = a->io_dtype;
+  d.out_dtype = LIN_F32;  // no outputs are written
+  d.gate_mode = a->gate_mode;
+  d.flags = a->flags;
+  d.q_scale = a->q_scale;
+  d.track_interval = a->track_interval;
+  d.x = a->x;
+  d.conv_w = a->conv_w;
+  d.g = a->g;
+  d.beta = a->beta;
+  d.out = nullptr;
+  d.slot = a->slot;
+  d.pos = a->pos;
+  d.track_slot = a->track_slot;
+  d.status = a->status;
+  if (lin::decode_stage_bytes(*pool, d) > lin::kDecodeMaxStage)
+    return fail(LIN_EUNSUPPORTED, "replay commit: n_draft %d stages %d bytes per (request, head), over %d",
+                d.n_draft, lin::decode_stage_bytes(*pool, d), lin::kDecodeMaxStage);
+  cudaError_t e = lin::launch_decode(*pool, d, a->accept_len, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lin_state_replay_commit launch");
   return ok();
 }
 

@@ -32,8 +32,10 @@ cudaError_t launch_spec_commit(const lin_state_pool_t& pool, const lin_commit_ar
 // taps, n_draft x rows and per-key g rows, 128-aligned); the kernel holds two.
 int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a);
 constexpr int kDecodeMaxStage = 110 * 1024;
+// accept: NULL for decode / verify; per-request accepted token counts for a
+// replay commit (in place, no outputs).
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
-                          cudaStream_t stream);
+                          const int32_t* accept, cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,
                                      const lin_prefill_args_t& a, cudaStream_t stream);
 

@@ -209,6 +209,7 @@ __device__ __forceinline__ void store_window(void* conv_base, int conv_dtype, co
 struct DecodeParams {
   lin_state_pool_t pool;
   lin_decode_args_t a;
+  const int32_t* accept;  // replay commit: accepted tokens per request (NULL: decode / verify)
 };
 
 constexpr uint32_t kDecWaitTries = 1u << 24;
@@ -268,7 +269,7 @@ struct DecPCfg {
 constexpr int kDecMaxStages = 4;
 
 struct DecMeta {
-  int r, h, slot, ts, pos, valid;
+  int r, h, slot, ts, pos, acc, valid;  // acc: tokens to run (n_draft, or accepted in a replay)
 };
 
 __device__ __forceinline__ bool mbar_try(uint32_t sb, uint32_t par) {
@@ -301,7 +302,12 @@ __device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
   return res != 0;
 }
 
-template <int D, int ST>
+// MODE: kDecStates (decode in place, or verify into the spec buffer),
+// kDecOutputsOnly (verify without per-step states), kDecReplay (the commit
+// form: accepted tokens per request, in place, no outputs).
+enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2 };
+
+template <int D, int ST, int MODE>
 __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
     decode_kernel(DecodeParams p, int n_items, int stage_bytes, int stages) {
   using C = DecPCfg<D>;
@@ -347,20 +353,23 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
     for (int base = blockIdx.x; base < n_items && !abort; base += 32 * gridDim.x) {
       // lane l looks up item base + l * gridDim.x, so 32 lookups overlap
       const int item = base + lane * gridDim.x;
-      DecMeta m{0, 0, -1, -1, 0, 0};
+      DecMeta m{0, 0, -1, -1, 0, 0, 0};
       if (item < n_items) {
         m.r = item / H;
         m.h = item % H;
         m.slot = a.slot[m.r];
         m.ts = a.track_slot ? a.track_slot[m.r] : -1;
-        m.pos = ND == 1 ? a.pos[m.r] : 0;
+        m.pos = (ND == 1 || MODE == kDecReplay) ? a.pos[m.r] : 0;
+        m.acc = MODE == kDecReplay ? p.accept[m.r] : ND;
         if (m.slot >= 0) {
           if (m.slot >= pool.num_slots || m.ts >= pool.num_slots) {
             if (m.h == 0) report(a.status, LIN_ST_BAD_SLOT);
           } else if (m.ts == m.slot) {
             if (m.h == 0) report(a.status, LIN_ST_TRACK_ALIAS);
+          } else if (m.acc < 0 || m.acc > ND) {
+            if (m.h == 0) report(a.status, LIN_ST_BAD_ACCEPT);
           } else {
-            m.valid = 1;
+            m.valid = m.acc > 0;  // nothing accepted: nothing to load or run
           }
         }
       }
@@ -373,6 +382,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
         mj.slot = __shfl_sync(0xffffffffu, m.slot, j);
         mj.ts = __shfl_sync(0xffffffffu, m.ts, j);
         mj.pos = __shfl_sync(0xffffffffu, m.pos, j);
+        mj.acc = __shfl_sync(0xffffffffu, m.acc, j);
         mj.valid = __shfl_sync(0xffffffffu, m.valid, j);
         const int s = n % stages;
         if (lane == 0) {
@@ -431,6 +441,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
   // factors meanwhile.
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2 = a.flags & LIN_QK_L2NORM;
+  constexpr bool REPLAY = MODE == kDecReplay;
   const int t = threadIdx.x;
   const int lr = lane % C::LPR;           // lane within the row group
   const int gbase = lane - lr;            // first lane of the row group
@@ -459,16 +470,30 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
     for (int j = 0; j < ND; ++j, ++tc) {
       float* ys = ysm[tc & 1];
       const int64_t tok = int64_t(m.r) * ND + j;
+      const bool live = REPLAY ? (m.valid && j < m.acc) : static_cast<bool>(m.valid);
       float beta = 0.f, gh = 0.f;
       char* dt = nullptr;
       char* dc = nullptr;
       char* tt = nullptr;
       char* tcv = nullptr;
       float pqq = 0.f, pkk = 0.f, pqk = 0.f;
-      if (m.valid) {
+      if (live) {
         beta = a.beta[tok * H + m.h];
         if (!per_key) gh = a.g[tok * H + m.h];
-        if (ND == 1) {
+        if (REPLAY) {
+          // in place: the slot after the last accepted token, the track slot
+          // at a boundary crossed on the way
+          if (j == m.acc - 1) {
+            dt = slot_t;
+            dc = slot_c;
+          }
+          if (m.ts >= 0 && a.track_interval > 0 && (m.pos + j + 1) % a.track_interval == 0) {
+            tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                 int64_t(m.ts) * pool.temporal_slot_stride + m.h * head_bytes;
+            tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                  int64_t(m.ts) * pool.conv_slot_stride;
+          }
+        } else if (ND == 1) {
           dt = slot_t;
           dc = slot_c;
           if (m.ts >= 0 && a.track_interval > 0 && (m.pos + 1) % a.track_interval == 0) {
@@ -477,12 +502,12 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
             tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                   int64_t(m.ts) * pool.conv_slot_stride;
           }
-        } else {
+        } else if (MODE == kDecStates) {
           dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
                m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
           dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
                m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
-        }
+        }  // kDecOutputsOnly: a verify that keeps no per-step states
         if (t < D) {
           const uint8_t* sx = buf + L.x + j * 3 * D * esi;
           float y3[3];
@@ -501,7 +526,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
               if (ND > 1) store_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype, nw[q]);  // next draft's window
-              store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
+              if (MODE == kDecStates || (MODE == kDecReplay && dc)) store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
               if (tcv) store_elem(tcv, ch * 3 + q, pool.conv_dtype, nw[q]);
             }
             y3[pt] = silu_on ? silu(y) : y;
@@ -533,7 +558,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
         abort = true;
         break;
       }
-      if (!m.valid) continue;
+      if (!live) continue;
       float sqq = 0.f, skk = 0.f, sqk = 0.f;
 #pragma unroll
       for (int pw = 0; pw < NPW; ++pw) {
@@ -616,7 +641,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           const float dk = __shfl_sync(0xffffffffu, red[0], gbase + (2 * i) * VSTEP);
           u[i] = beta * (ys[2 * D + row0 + (rb + i) * C::RSTEP] - dk);
         }
-        if ((my_v & 1) && (lr % VSTEP) == 0) {
+        if (!REPLAY && (my_v & 1) && (lr % VSTEP) == 0) {
           float ui = 0.f;
 #pragma unroll
           for (int i = 0; i < C::RB; ++i)
@@ -630,7 +655,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           const uint64_t u2 = f2pack(u[i], u[i]);
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) sv[i][e2] = ffma2(u2, k2[e2], sv[i][e2]);
-          Pair8<ST>::store(dt + off, sv[i]);
+          if (MODE == kDecStates || (MODE == kDecReplay && dt)) Pair8<ST>::store(dt + off, sv[i]);
           if (tt) Pair8<ST>::store(tt + off, sv[i]);
           if (ND > 1) {
             Pair8<ST>::round(sv[i]);  // the next draft starts from the stored state
@@ -770,9 +795,10 @@ struct DecodeLaunchCache {
 
 template <int D, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
-                          cudaStream_t stream) {
-  static DecodeLaunchCache cache;
-  DecodeParams p{pool, a};
+                          const int32_t* accept, cudaStream_t stream) {
+  static DecodeLaunchCache caches[3];  // one per DecMode
+  DecodeLaunchCache& cache = caches[accept ? kDecReplay : (a.n_draft > 1 && !a.spec.temporal ? kDecOutputsOnly : kDecStates)];
+  DecodeParams p{pool, a, accept};
   const int stage = decode_stage_bytes(pool, a);
   if (stage > kDecodeMaxStage) return cudaErrorInvalidValue;
   // two CTAs per SM when two stages each fit, else one CTA with two stages
@@ -780,7 +806,10 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (stages > kDecMaxStages) stages = kDecMaxStages;
   if (stages < 2) stages = 2;
   const int smem = stages * stage;
-  auto kern = decode_kernel<D, ST>;
+  const int mode = accept ? kDecReplay : (a.n_draft > 1 && !a.spec.temporal ? kDecOutputsOnly : kDecStates);
+  auto kern = mode == kDecReplay ? decode_kernel<D, ST, kDecReplay>
+                                 : (mode == kDecOutputsOnly ? decode_kernel<D, ST, kDecOutputsOnly>
+                                                            : decode_kernel<D, ST, kDecStates>);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -850,9 +879,9 @@ int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a)
 }
 
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
-                          cudaStream_t stream) {
+                          const int32_t* accept, cudaStream_t stream) {
   if (a.batch <= 0) return cudaSuccess;
-  LIN_DISPATCH_D_ST(decode_launch, pool.head_k, pool.state_dtype, pool, a, stream);
+  LIN_DISPATCH_D_ST(decode_launch, pool.head_k, pool.state_dtype, pool, a, accept, stream);
 }
 
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,

@@ -117,12 +117,26 @@ def test_decode_and_copy_reject_bad_args_on_host():
     d = L.DecodeArgsT()
     d.layer, d.batch, d.n_draft = 0, 4, 0
     assert L.lib.lin_state_decode(ctypes.byref(p), ctypes.byref(d), None) == L.LIN_EINVAL
-    d.n_draft = 4  # verify needs a spec buffer
+    d.n_draft = 4  # a verify with half a spec buffer (no conv part) is rejected
     d.io_dtype = d.out_dtype = L.LIN_BF16
     for f in ("x", "conv_w", "g", "beta", "out", "slot", "pos"):
         setattr(d, f, 0x300000)
+    d.spec.temporal = 0x400000
     assert L.lib.lin_state_decode(ctypes.byref(p), ctypes.byref(d), None) == L.LIN_EINVAL
     assert "spec" in L.lib.lin_state_last_error().decode()
+    # replay commit: accept_len is required, and inputs must be 16-byte aligned
+    r = L.ReplayArgsT()
+    r.layer, r.batch, r.n_draft, r.io_dtype = 0, 4, 4, L.LIN_BF16
+    r.gate_mode = L.LIN_GATE_PER_KEY
+    for f in ("x", "conv_w", "g", "beta", "slot", "pos"):
+        setattr(r, f, 0x300000)
+    assert L.lib.lin_state_replay_commit(ctypes.byref(p), ctypes.byref(r), None) == L.LIN_EINVAL
+    assert "accept_len" in L.lib.lin_state_last_error().decode()
+    r.accept_len, r.x = 0x300000, 0x300004
+    assert L.lib.lin_state_replay_commit(ctypes.byref(p), ctypes.byref(r), None) == L.LIN_EINVAL
+    assert "aligned" in L.lib.lin_state_last_error().decode()
+    r.n_draft = 0
+    assert L.lib.lin_state_replay_commit(ctypes.byref(p), ctypes.byref(r), None) == L.LIN_EINVAL
     assert L.lib.lin_state_copy_slots(ctypes.byref(p), None, None, 3, 0, 69, 0, None, None) == L.LIN_EINVAL
     assert L.lib.lin_state_copy_slots(ctypes.byref(p), 0x10, 0x10, 3, 5, 2, 0, None, None) == L.LIN_EINVAL
     # empty work is a no-op that never reaches the device

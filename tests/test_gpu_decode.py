@@ -204,6 +204,62 @@ def test_decode_and_verify_many_items_per_cta():
             assert max_rel_per_head(st[0, r, j], ospec["temporal"][0, r, j], 0) < TOL_F32
 
 
+@pytest.mark.parametrize("sdt,gate", [(torch.bfloat16, L.LIN_GATE_PER_KEY),
+                                      (torch.float32, L.LIN_GATE_PER_HEAD)])
+def test_replay_commit_equals_spec_commit(sdt, gate):
+    """The replay form of speculative decoding ([K3] ReplaySSM, [MRC] 9): a
+    verify that keeps no per-step states writes the same outputs, bit for bit,
+    as one that does, and re-running the accepted prefix into the slot leaves
+    every slot and track slot bit-identical to committing from the per-step
+    buffer; both match the oracle. Accept lengths 0 .. D, boundary crossings
+    at 256, a padding request, layer 1 of a 2-layer pool."""
+    H, D, ND, B, S = 2, 128, 4, 7, 24
+    dims = W.LayerDims(num_heads=H, head_k=D, head_v=D)
+    pa = L.StatePool(2, S, H, D, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV)
+    fill_pool(pa, 31, std=0.1)
+    pb = L.StatePool(2, S, H, D, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV,
+                     temporal=pa.temporal.clone(), conv=pa.conv.clone())
+    op = oracle_pool(pa)
+    conv_w = W.randn((dims.conv_channels, 4), 31, "rp.w", std=0.5).to(torch.bfloat16).to(DEV)
+    slots = [3, 7, -1, 11, 15, 19, 21]
+    track = [4, 8, 9, 12, 16, -1, 22]
+    pos = [254, 100, 0, 253, 255, 1, 510]
+    acc = [3, 4, 2, 0, 1, 2, 4]
+    x, g, beta = (t.to(DEV) for t in W.make_decode_inputs(dims, B, ND, gate, torch.bfloat16, 31, tag="rp"))
+    spec = L.SpecBuffer(pa, B, ND)
+    oa = torch.zeros((B, ND, H, D), device=DEV)
+    ob = torch.zeros((B, ND, H, D), device=DEV)
+    common = dict(layer=1, x=x, conv_w=conv_w, g=g, beta=beta, slot=_i32(slots), pos=_i32(pos),
+                  gate_mode=gate, flags=FLAGS)
+    L.lin_state_decode(pa, out=oa, spec=spec, **common)
+    L.lin_state_decode(pb, out=ob, **common)  # no spec buffer: outputs only
+    assert torch.equal(oa, ob)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lin_state_spec_commit(pa, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
+                            n_draft=ND, track_slot=_i32(track), track_interval=256, layer_begin=1,
+                            layer_end=2, status=st)
+    assert L.lin_state_read_status(st) == 0
+    L.lin_state_replay_commit(pb, layer=1, x=x, conv_w=conv_w, g=g, beta=beta, slot=_i32(slots),
+                              pos=_i32(pos), accept_len=_i32(acc), track_slot=_i32(track),
+                              track_interval=256, gate_mode=gate, flags=FLAGS, status=st)
+    assert L.lin_state_read_status(st) == 0
+    assert torch.equal(pa.temporal, pb.temporal)
+    assert torch.equal(pa.conv, pb.conv)
+    # the oracle: verify into its own per-step buffer, then commit
+    ospec = O.make_spec_buffer(2, B, ND, H, D, D, dims.conv_channels)
+    oo, ost = O.decode(op, 1, np64(x), np64(conv_w), np64(g), np64(beta), slots, pos, None, 0,
+                       gate, FLAGS, 1.0, "f32", spec=ospec)
+    assert ost == 0
+    live = [r for r in range(B) if slots[r] >= 0]
+    tol = TOL_F32 if sdt == torch.float32 else TOL_BF16
+    assert max_rel_per_head(np64(ob)[live], oo[live], 2) < tol
+    O.spec_commit(op, ospec, 1, 2, slots, pos, acc, track, 256, ND)
+    t = np64(pb.temporal[1])
+    for s_ in range(S):
+        assert max_rel_per_head(t[s_], op["temporal"][1, s_], 0) < tol
+    assert np.array_equal(np64(pb.conv), op["conv"])
+
+
 def test_decode_status_bits():
     dims = W.LayerDims(num_heads=1, head_k=32, head_v=32)
     pool = L.StatePool(1, 8, 1, 32, device=DEV)
