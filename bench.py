@@ -230,10 +230,12 @@ class DecodeWorkload(Workload):
     step, interval 256 with per-request track slots; the pool is rotated over 4
     replicas so the per-step working set does not stay in L2."""
 
-    def __init__(self, L, dev, n_draft=1, replicas=4, seed=0):
+    def __init__(self, L, dev, n_draft=1, replicas=4, seed=0, replay=False):
         self.L, self.dev = L, dev
         self.n_draft = n_draft
-        self.name = "kda_decode" if n_draft == 1 else f"kda_spec_verify{n_draft}_commit"
+        self.replay = replay
+        self.name = ("kda_decode" if n_draft == 1 else
+                     f"kda_spec_verify{n_draft}_replay" if replay else f"kda_spec_verify{n_draft}_commit")
         self.unit = "req-steps/s" if n_draft == 1 else "verify-rounds/s"
         self.kernel = "decode"
         dims = W.KIMI_K3_TP8
@@ -262,7 +264,8 @@ class DecodeWorkload(Workload):
         self.out = torch.empty((B, n_draft, 12, 128), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         if n_draft > 1:
-            self.specs = [L.SpecBuffer(p, B, n_draft) for p in self.pools]
+            if not replay:
+                self.specs = [L.SpecBuffer(p, B, n_draft) for p in self.pools]
             self.acc = (W.randint(1, n_draft, (B,), seed, "kd.acc")).to(torch.int32).to(dev)
             self.launches_per_step = 2
         st = W.state_bytes(dims, 2, 2)
@@ -272,6 +275,18 @@ class DecodeWorkload(Workload):
             # the amortised track copy (one per 256 steps)
             self.bytes = B * (2 * st + x_b + st / 256.0)
             self.units = B
+        elif replay:
+            # verify reads the state and writes outputs only; the commit reads
+            # and writes the state and reads the accepted tokens' inputs
+            D = n_draft
+            acc_mean = (n_draft + 1) / 2.0
+            o_b = 12 * 128 * 2
+            verify = B * (st + D * x_b)
+            commit = B * (2 * st + acc_mean * (x_b - o_b))
+            self.bytes = verify + commit
+            self.verify_bytes = verify
+            self.units = 1
+            self.acc_tokens = B * acc_mean
         else:
             D = n_draft
             acc_mean = (n_draft + 1) / 2.0
@@ -305,6 +320,17 @@ class DecodeWorkload(Workload):
                                slot=self.slot, pos=pos, track_slot=self.track, track_interval=256,
                                gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
             self._k_end()
+        elif self.replay:
+            self._k_begin()
+            L.lin_state_decode(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta, out=self.out,
+                               slot=self.slot, pos=pos, gate_mode=L.LIN_GATE_PER_KEY,
+                               status=self.status)
+            self._k_end()
+            L.lin_state_replay_commit(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta,
+                                      slot=self.slot, pos=pos, accept_len=self.acc,
+                                      track_slot=self.track, track_interval=256,
+                                      gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
+            return
         else:
             self._k_begin()
             L.lin_state_decode(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta, out=self.out,
@@ -381,6 +407,8 @@ def make_workload(name, L, dev):
         return DecodeWorkload(L, dev, 1)
     if name == "kda_spec_verify4_commit":
         return DecodeWorkload(L, dev, 4)
+    if name == "kda_spec_verify4_replay":
+        return DecodeWorkload(L, dev, 4, replay=True)
     if name == "slot_copy_kimi_k3_69l":
         return CopyWorkload(L, dev)
     raise ValueError(name)
@@ -388,6 +416,7 @@ def make_workload(name, L, dev):
 
 HEADLINE = "qwen35_gdn_prefill"
 DEFAULT_EXTRA = ["kimi_k3_kda_varlen_prefill", "kda_decode", "kda_spec_verify4_commit",
+                 "kda_spec_verify4_replay",
                  "slot_copy_kimi_k3_69l", "kda_long_prefill_131k"]
 
 CONFIG_TEXT = {
@@ -402,6 +431,8 @@ CONFIG_TEXT = {
                   "1 token per step, track interval 256, 4 pool replicas",
     "kda_spec_verify4_commit": "KDA speculative verify of 4 drafts + commit of U{1..4} accepted, "
                                "256 requests, per-step states in a spec buffer",
+    "kda_spec_verify4_replay": "KDA speculative verify of 4 drafts (outputs only) + replay commit of "
+                               "U{1..4} accepted tokens into the slot, 256 requests, no per-step buffer",
     "slot_copy_kimi_k3_69l": "checkpoint fork/restore copy: Kimi-K3 slot over 69 layers (29,039,616 B), "
                              "64 random src->dst pairs per batch in a 256-slot pool",
     "kda_long_prefill_131k": "single-request KDA prefill, 131072 tokens, 12 heads, bf16, cold, "
