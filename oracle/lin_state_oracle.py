@@ -61,6 +61,7 @@ ST_TRACK_ALIAS = 4
 ST_BAD_SEQLEN = 8
 ST_COPY_ALIAS = 16
 ST_BAD_ACCEPT = 64
+ST_BAD_TREE = 256  # a draft's parent outside [-1, j), or an accepted node outside [-1, n_draft)
 
 L2_EPS = 1e-6
 
@@ -246,14 +247,18 @@ def make_spec_buffer(num_layers, batch, n_draft, H, K, V, C, W=4, fill=0.0):
 
 def decode(pool, layer, x, conv_w, g, beta, slot, pos, track_slot,
            track_interval, gate_mode, flags, q_scale=1.0, out_dtype="f32",
-           spec=None, out=None):
+           spec=None, out=None, parent=None):
     """x [B][D][C]; g [B][D][H] or [B][D][H][K]; beta [B][D][H].
 
     D == 1: the slot is read, advanced one token and written back; when the
     state then covers a multiple of track_interval tokens it is also copied
     into track_slot[r].
     D > 1 (verify): D tokens run from the slot state; the state after step j
-    goes to spec[layer][r][j]; the slot is not modified.
+    goes to spec[layer][r][j]; the slot is not modified. With parent
+    [B][D] (a draft tree, MambaRadixCache page 8.3 and 9.6,
+    retrieve_parent_token): draft j starts from the state and conv window
+    after draft parent[r][j] (-1: the slot's), so a chain is parent[j] = j-1;
+    a parent outside [-1, j) skips the request with ST_BAD_TREE.
     The state is rounded to the pool's dtype after every token, as a decode
     that reads and writes the pool per token would.
     """
@@ -279,9 +284,20 @@ def decode(pool, layer, x, conv_w, g, beta, slot, pos, track_slot,
         if ts == s:
             status |= ST_TRACK_ALIAS
             continue
+        if parent is not None and D > 1 and any(
+                not (-1 <= int(parent[r][j]) < j) for j in range(D)):
+            status |= ST_BAD_TREE
+            continue
         S = temporal[layer, s].copy()
         cw = conv[layer, s].copy()
         for j in range(D):
+            if parent is not None and D > 1:
+                pj = int(parent[r][j])
+                if pj < 0:
+                    S, cw = temporal[layer, s].copy(), conv[layer, s].copy()
+                else:
+                    S = spec["temporal"][layer, r, pj].copy()
+                    cw = spec["conv"][layer, r, pj].copy()
             S, cw, o = token_step(S, cw, x[r, j], conv_w, g[r, j], beta[r, j],
                                   H, K, V, gate_mode, flags, q_scale)
             S = round_to(S, sd)
@@ -301,22 +317,38 @@ def decode(pool, layer, x, conv_w, g, beta, slot, pos, track_slot,
 
 
 def spec_commit(pool, spec, layer_begin, layer_end, slot, pos, accept_len,
-                track_slot, track_interval, n_draft):
+                track_slot, track_interval, n_draft, parent=None, accept_node=None):
     """main[slot] = buffer[accepted - 1] for every layer in the range; when the
     accepted tokens cross a multiple of track_interval, the state at that
     boundary (the largest one crossed) also goes to track_slot.
-    accept_len == 0 leaves everything unchanged."""
+    accept_len == 0 leaves everything unchanged.
+    A draft tree (parent [B][D], accept_node [B]): the accepted path ends at
+    node accept_node[r] (-1: nothing accepted) and runs back through its
+    parents to the root; its length plays the part of accept_len, and the
+    node at depth n - pos on it holds the boundary state."""
     temporal, conv = pool["temporal"], pool["conv"]
     num_slots = temporal.shape[1]
     status = 0
     for r in range(len(slot)):
         s = int(slot[r])
-        a = int(accept_len[r])
         if s < 0:
             continue
         if not _in_range(s, num_slots):
             status |= ST_BAD_SLOT
             continue
+        if parent is not None:
+            node = int(accept_node[r])
+            if node < -1 or node >= n_draft:
+                status |= ST_BAD_TREE
+                continue
+            path = []  # root first
+            while node >= 0:
+                path.insert(0, node)
+                node = int(parent[r][node])
+            a = len(path)
+        else:
+            a = int(accept_len[r])
+            path = list(range(a)) if 0 <= a <= n_draft else []
         if a < 0 or a > n_draft:
             status |= ST_BAD_ACCEPT
             continue
@@ -336,11 +368,11 @@ def spec_commit(pool, spec, layer_begin, layer_end, slot, pos, accept_len,
             if n > p:
                 boundary = n
         for layer in range(layer_begin, layer_end):
-            temporal[layer, s] = spec["temporal"][layer, r, a - 1]
-            conv[layer, s] = spec["conv"][layer, r, a - 1]
+            temporal[layer, s] = spec["temporal"][layer, r, path[a - 1]]
+            conv[layer, s] = spec["conv"][layer, r, path[a - 1]]
             if boundary is not None:
-                temporal[layer, ts] = spec["temporal"][layer, r, boundary - p - 1]
-                conv[layer, ts] = spec["conv"][layer, r, boundary - p - 1]
+                temporal[layer, ts] = spec["temporal"][layer, r, path[boundary - p - 1]]
+                conv[layer, ts] = spec["conv"][layer, r, path[boundary - p - 1]]
     return status
 
 

@@ -384,6 +384,108 @@ def test_spec_commit_equals_sequential_decode(dtype):
                 assert np.all(pa["temporal"][0, 3] == -1)
 
 
+# a draft tree in the shape of the MambaRadixCache page's example (9.6): two
+# roots, children of both, a grandchild; parent index per draft, -1 = the slot
+TREE_PARENT = [-1, -1, 0, 0, 1, 2, 2, 5]
+
+
+def _tree_setup(seed, dtype, D):
+    H, K, V = 2, 8, 8
+    C = 2 * H * K + H * V
+    r = rng(seed)
+    w = r.standard_normal((C, 4)) * 0.5
+    S0 = O.round_to(r.standard_normal((H, V, K)) * 0.2, dtype)
+    c0 = O.round_to(r.standard_normal((C, 3)), dtype)
+    x = O.round_to(r.standard_normal((1, D, C)), dtype)
+    g = -np.log1p(np.exp(r.standard_normal((1, D, H, K))))
+    b = 1 / (1 + np.exp(-r.standard_normal((1, D, H))))
+    pool = O.make_pool(1, 6, H, K, V, C, state_dtype=dtype, conv_dtype=dtype, fill=-1)
+    pool["temporal"][0, 1] = S0
+    pool["conv"][0, 1] = c0
+    return H, K, V, C, w, x, g, b, pool
+
+
+def _path(parent, node):
+    p = []
+    while node >= 0:
+        p.insert(0, node)
+        node = parent[node]
+    return p
+
+
+@pytest.mark.parametrize("dtype", ["f64", "bf16"])
+def test_tree_verify_paths_equal_linear_chains(dtype):
+    """MambaRadixCache page 8.3 / 9.6: each draft of a tree starts from its
+    parent's state (retrieve_parent_token). Every node's output and state
+    equal the linear chain run along its root-to-node path, and a chain given
+    as parents (j - 1) equals the plain verify exactly."""
+    D = len(TREE_PARENT)
+    H, K, V, C, w, x, g, b, pool = _tree_setup(61, dtype, D)
+    f = O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU
+    spec = O.make_spec_buffer(1, 1, D, H, K, V, C)
+    out_t, st = O.decode(pool, 0, x, w, g, b, [1], [0], None, 0, O.GATE_PER_KEY, f, spec=spec,
+                         parent=[TREE_PARENT])
+    assert st == 0
+    for node in range(D):
+        path = _path(TREE_PARENT, node)
+        pc = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in pool.items()}
+        sc = O.make_spec_buffer(1, 1, len(path), H, K, V, C)
+        if len(path) == 1:
+            out_c, _ = O.decode(pc, 0, x[:, path], w, g[:, path], b[:, path], [1], [0], None, 0,
+                                O.GATE_PER_KEY, f)
+            # a single decode writes the slot: compare against it
+            assert np.array_equal(pc["temporal"][0, 1], spec["temporal"][0, 0, node])
+        else:
+            out_c, _ = O.decode(pc, 0, x[:, path], w, g[:, path], b[:, path], [1], [0], None, 0,
+                                O.GATE_PER_KEY, f, spec=sc)
+            assert np.array_equal(sc["temporal"][0, 0, -1], spec["temporal"][0, 0, node])
+            assert np.array_equal(sc["conv"][0, 0, -1], spec["conv"][0, 0, node])
+        assert np.array_equal(out_c[0, -1], out_t[0, node])
+    # a chain written as parents is the plain verify
+    chain = [[j - 1 for j in range(D)]]
+    s1, s2 = O.make_spec_buffer(1, 1, D, H, K, V, C), O.make_spec_buffer(1, 1, D, H, K, V, C)
+    o1, _ = O.decode(pool, 0, x, w, g, b, [1], [0], None, 0, O.GATE_PER_KEY, f, spec=s1, parent=chain)
+    o2, _ = O.decode(pool, 0, x, w, g, b, [1], [0], None, 0, O.GATE_PER_KEY, f, spec=s2)
+    assert np.array_equal(o1, o2) and np.array_equal(s1["temporal"], s2["temporal"])
+
+
+def test_tree_commit_equals_chain_commit_and_rejects_bad_trees():
+    """The accepted path of a tree is a linear chain (MambaRadixCache page
+    9.9): committing node a equals committing a chain verify of a's path with
+    accept_len = its depth, boundary snapshots included; a parent outside
+    [-1, j) or an accepted node outside [-1, n_draft) is rejected."""
+    D = len(TREE_PARENT)
+    H, K, V, C, w, x, g, b, pool = _tree_setup(62, "bf16", D)
+    f = O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU
+    for pos in [100, 254, 255]:
+        for node in [-1, 0, 3, 4, 7]:
+            pa = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in pool.items()}
+            spec = O.make_spec_buffer(1, 1, D, H, K, V, C)
+            O.decode(pa, 0, x, w, g, b, [1], [pos], None, 0, O.GATE_PER_KEY, f, spec=spec,
+                     parent=[TREE_PARENT])
+            st = O.spec_commit(pa, spec, 0, 1, [1], [pos], None, [3], 256, D, parent=[TREE_PARENT],
+                               accept_node=[node])
+            assert st == 0
+            path = _path(TREE_PARENT, node)
+            pb = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in pool.items()}
+            if path:
+                sc = O.make_spec_buffer(1, 1, max(2, len(path)), H, K, V, C)
+                xp = x[:, path + path[-1:]] if len(path) == 1 else x[:, path]
+                gp = g[:, path + path[-1:]] if len(path) == 1 else g[:, path]
+                bp = b[:, path + path[-1:]] if len(path) == 1 else b[:, path]
+                O.decode(pb, 0, xp, w, gp, bp, [1], [pos], None, 0, O.GATE_PER_KEY, f, spec=sc)
+                O.spec_commit(pb, sc, 0, 1, [1], [pos], [len(path)], [3], 256, sc["temporal"].shape[2])
+            for k in ("temporal", "conv"):
+                assert np.array_equal(pa[k], pb[k]), (pos, node, k)
+    bad = [-1, 0, 2, 0, 1, 2, 2, 5]  # draft 2's parent is itself
+    st = O.decode(pool, 0, x, w, g, b, [1], [0], None, 0, O.GATE_PER_KEY, f,
+                  spec=O.make_spec_buffer(1, 1, D, H, K, V, C), parent=[bad])[1]
+    assert st == O.ST_BAD_TREE
+    st = O.spec_commit(pool, O.make_spec_buffer(1, 1, D, H, K, V, C), 0, 1, [1], [0], None, None, 0,
+                       D, parent=[TREE_PARENT], accept_node=[D])
+    assert st == O.ST_BAD_TREE
+
+
 def test_copy_slots_is_a_gather():
     r = rng(50)
     pool = O.make_pool(3, 10, 2, 4, 4, 24)
