@@ -70,6 +70,8 @@ extern "C" {
 #define LIN_ST_COPY_ALIAS 16   /* LIN_VALIDATE: a copy dst is another pair's dst or src */
 #define LIN_ST_TIMEOUT 32      /* a bounded device wait gave up               */
 #define LIN_ST_BAD_ACCEPT 64   /* commit accept_len outside [0, n_draft]      */
+#define LIN_ST_BAD_TREE 256    /* a draft's parent outside [-1, j), or an
+                                  accepted node outside [-1, n_draft)         */
 #define LIN_ST_DECAY_RANGE 128 /* KDA chunked prefill: some key channel decays
                                   by more than e^80 across half a chunk (mean
                                   log-decay below -2.5 per token), outside the
@@ -260,6 +262,12 @@ typedef struct {
   const int32_t* track_slot;
   lin_spec_buf_t spec; /* used when n_draft > 1 */
   int32_t* status;
+  /* Draft tree ([MRC] 8.3, 9.6 retrieve_parent_token): device [batch][n_draft]
+   * int32, or NULL for a linear chain. With a spec buffer and n_draft <= 32,
+   * draft j of request r starts from the state and conv window after draft
+   * parent[r][j] (-1: the slot's); parent[r][j] must lie in [-1, j), else the
+   * request is skipped with LIN_ST_BAD_TREE. */
+  const int32_t* parent;
 } lin_decode_args_t;
 
 LIN_API int lin_state_decode(const lin_state_pool_t* pool, const lin_decode_args_t* args,
@@ -284,6 +292,13 @@ typedef struct {
   const int32_t* track_slot; /* device [batch] or NULL */
   lin_spec_buf_t spec;
   int32_t* status;
+  /* Draft tree: parent as in lin_decode_args_t (device [batch][n_draft]) and
+   * accept_node (device [batch]): the last node of the accepted path (-1:
+   * nothing), whose length then plays the part of accept_len (accept_len is
+   * not read); the boundary snapshot comes from the path's node at that
+   * depth. NULL parent: the linear chain above. */
+  const int32_t* parent;
+  const int32_t* accept_node;
 } lin_commit_args_t;
 
 LIN_API int lin_state_spec_commit(const lin_state_pool_t* pool, const lin_commit_args_t* args,

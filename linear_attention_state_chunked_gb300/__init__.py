@@ -28,6 +28,7 @@ LIN_PREFILL_SEGMENTED = 16
 LIN_ST_BAD_SLOT, LIN_ST_BAD_PREFIX, LIN_ST_TRACK_ALIAS, LIN_ST_BAD_SEQLEN = 1, 2, 4, 8
 LIN_ST_COPY_ALIAS, LIN_ST_TIMEOUT, LIN_ST_BAD_ACCEPT = 16, 32, 64
 LIN_ST_DECAY_RANGE = 128
+LIN_ST_BAD_TREE = 256
 
 LIN_KERNEL_RECURRENT, LIN_KERNEL_CHUNKED = 0, 1
 
@@ -88,7 +89,7 @@ class DecodeArgsT(ctypes.Structure):
         ("x", ctypes.c_void_p), ("conv_w", ctypes.c_void_p), ("g", ctypes.c_void_p),
         ("beta", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("slot", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("track_slot", ctypes.c_void_p),
-        ("spec", SpecBufT), ("status", ctypes.c_void_p),
+        ("spec", SpecBufT), ("status", ctypes.c_void_p), ("parent", ctypes.c_void_p),
     ]
 
 
@@ -110,6 +111,7 @@ class CommitArgsT(ctypes.Structure):
         ("track_interval", ctypes.c_int32),
         ("slot", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("accept_len", ctypes.c_void_p),
         ("track_slot", ctypes.c_void_p), ("spec", SpecBufT), ("status", ctypes.c_void_p),
+        ("parent", ctypes.c_void_p), ("accept_node", ctypes.c_void_p),
     ]
 
 
@@ -337,10 +339,12 @@ def lin_state_prefill_noalloc(pool: StatePool, *, layer: int, x, conv_w, g, beta
 def lin_state_decode(pool: StatePool, *, layer: int, x, conv_w, g, beta, out, slot, pos,
                      track_slot=None, track_interval: int = 0, spec: Optional[SpecBuffer] = None,
                      gate_mode: int = LIN_GATE_PER_KEY, flags: int = LIN_QK_L2NORM | LIN_CONV_SILU,
-                     q_scale: float = 1.0, status=None, stream=None) -> None:
+                     q_scale: float = 1.0, status=None, stream=None, parent=None) -> None:
     """Calls lin_state_decode. x [B][n_draft][C]; with n_draft > 1 the per-step
     states go to `spec`, or, with spec None, only the outputs are written (the
-    replay form: lin_state_replay_commit then runs the accepted prefix)."""
+    replay form: lin_state_replay_commit then runs the accepted prefix).
+    parent [B][n_draft] int32 (with `spec`): a draft tree, draft j starting
+    from the state after draft parent[r][j] (-1: the slot's)."""
     a = DecodeArgsT()
     a.layer, a.batch, a.n_draft = layer, x.shape[0], x.shape[1]
     a.io_dtype, a.out_dtype = dtype_code(x.dtype), dtype_code(out.dtype)
@@ -351,20 +355,26 @@ def lin_state_decode(pool: StatePool, *, layer: int, x, conv_w, g, beta, out, sl
     if spec is not None:
         a.spec = spec.desc()
     a.status = status.data_ptr() if status is not None else None
+    a.parent = parent.data_ptr() if parent is not None else None
     _check(lib.lin_state_decode(ctypes.byref(pool.desc()), ctypes.byref(a), _stream(stream)),
            "lin_state_decode")
 
 
-def lin_state_spec_commit(pool: StatePool, *, spec: SpecBuffer, slot, pos, accept_len,
+def lin_state_spec_commit(pool: StatePool, *, spec: SpecBuffer, slot, pos, accept_len=None,
                           n_draft: int, track_slot=None, track_interval: int = 0,
                           layer_begin: int = 0, layer_end: Optional[int] = None,
-                          status=None, stream=None) -> None:
+                          status=None, stream=None, parent=None, accept_node=None) -> None:
+    """Calls lin_state_spec_commit: accept_len for a chain, or parent +
+    accept_node (the last accepted node) for a draft tree."""
     a = CommitArgsT()
     a.layer_begin = layer_begin
     a.layer_end = pool.num_layers if layer_end is None else layer_end
     a.batch, a.n_draft, a.track_interval = slot.numel(), n_draft, track_interval
-    a.slot, a.pos, a.accept_len = slot.data_ptr(), pos.data_ptr(), accept_len.data_ptr()
+    a.slot, a.pos = slot.data_ptr(), pos.data_ptr()
+    a.accept_len = accept_len.data_ptr() if accept_len is not None else None
     a.track_slot = track_slot.data_ptr() if track_slot is not None else None
+    a.parent = parent.data_ptr() if parent is not None else None
+    a.accept_node = accept_node.data_ptr() if accept_node is not None else None
     a.spec = spec.desc()
     a.status = status.data_ptr() if status is not None else None
     _check(lib.lin_state_spec_commit(ctypes.byref(pool.desc()), ctypes.byref(a), _stream(stream)),

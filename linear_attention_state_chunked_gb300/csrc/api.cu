@@ -242,6 +242,12 @@ int lin_state_decode(const lin_state_pool_t* pool, const lin_decode_args_t* a, v
     rc = check_spec(pool, a->spec, a->batch, a->n_draft, a->layer + 1);
     if (rc) return rc;
   }
+  if (a->parent) {
+    if (a->n_draft <= 1 || spec_less)
+      return fail(LIN_EINVAL, "decode: a draft tree needs n_draft > 1 and a spec buffer");
+    if (a->n_draft > 32)
+      return fail(LIN_EUNSUPPORTED, "decode: a draft tree holds at most 32 drafts, not %d", a->n_draft);
+  }
   if (lin::decode_stage_bytes(*pool, *a) > lin::kDecodeMaxStage)
     return fail(LIN_EUNSUPPORTED, "decode: n_draft %d stages %d bytes per (request, head), over %d",
                 a->n_draft, lin::decode_stage_bytes(*pool, *a), lin::kDecodeMaxStage);
@@ -304,7 +310,8 @@ int lin_state_spec_commit(const lin_state_pool_t* pool, const lin_commit_args_t*
   if (a->batch < 0 || a->n_draft < 1 || a->track_interval < 0)
     return fail(LIN_EINVAL, "commit: batch / n_draft / track_interval");
   if (a->batch == 0 || a->layer_begin == a->layer_end) return ok();
-  if (!a->slot || !a->pos || !a->accept_len) return fail(LIN_EINVAL, "commit: slot / pos / accept_len is NULL");
+  if (!a->slot || !a->pos || (a->parent ? !a->accept_node : !a->accept_len))
+    return fail(LIN_EINVAL, "commit: slot / pos / accept_len (accept_node with a tree) is NULL");
   rc = check_spec(pool, a->spec, a->batch, a->n_draft, a->layer_end);
   if (rc) return rc;
   cudaError_t e = lin::launch_spec_commit(*pool, *a, static_cast<cudaStream_t>(stream));

@@ -127,15 +127,37 @@ __global__ void __launch_bounds__(kCopyThreads) slot_copy_kernel(CopyParams p) {
   } else {  // kModeCommit; blockIdx.y = 0 -> live slot, 1 -> track slot
     const lin_commit_args_t& c = p.commit;
     int s = c.slot[item];
-    int a = c.accept_len[item];
     if (s < 0) return;
     if (s >= ns) {
       if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_SLOT);
       return;
     }
-    if (a < 0 || a > c.n_draft) {
-      if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_ACCEPT);
-      return;
+    // the accepted path: drafts 0 .. a-1 of a chain, or a tree node and its
+    // ancestors (each parent strictly earlier, so the walk ends in <= n_draft steps)
+    int a, last;
+    const int32_t* par = c.parent ? c.parent + int64_t(item) * c.n_draft : nullptr;
+    if (par) {
+      last = c.accept_node[item];
+      if (last < -1 || last >= c.n_draft) {
+        if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_TREE);
+        return;
+      }
+      a = 0;
+      for (int nd = last; nd >= 0; ++a) {
+        const int up = par[nd];
+        if (up < -1 || up >= nd) {
+          if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_TREE);
+          return;
+        }
+        nd = up;
+      }
+    } else {
+      a = c.accept_len[item];
+      if (a < 0 || a > c.n_draft) {
+        if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_ACCEPT);
+        return;
+      }
+      last = a - 1;
     }
     if (a == 0) return;
     int ts = c.track_slot ? c.track_slot[item] : -1;
@@ -149,14 +171,20 @@ __global__ void __launch_bounds__(kCopyThreads) slot_copy_kernel(CopyParams p) {
     }
     int step;
     if (blockIdx.y == 0) {
-      step = a - 1;
+      step = last;
       dst_slot = s;
     } else {
       if (ts < 0 || c.track_interval <= 0) return;
       const int pos = c.pos[item];
       const int nb = ((pos + a) / c.track_interval) * c.track_interval;
       if (nb <= pos) return;
+      // the path's node at depth nb - pos: nb - pos - 1 in a chain, or the
+      // accepted node's ancestor a - (nb - pos) levels up
       step = nb - pos - 1;
+      if (par) {
+        step = last;
+        for (int up = a - (nb - pos); up > 0; --up) step = par[step];
+      }
       dst_slot = ts;
     }
     src_t = static_cast<const char*>(c.spec.temporal) + layer * c.spec.temporal_layer_stride +

@@ -305,7 +305,10 @@ __device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
 // MODE: kDecStates (decode in place, or verify into the spec buffer),
 // kDecOutputsOnly (verify without per-step states), kDecReplay (the commit
 // form: accepted tokens per request, in place, no outputs).
-enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2 };
+// kDecTree: verify into the spec buffer where draft j starts from the state
+// after draft parent[r][j] (-1: the slot's).
+enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2, kDecTree = 3 };
+constexpr int kDecMaxTree = 32;  // drafts per request in a tree verify
 
 template <int D, int ST, int MODE>
 __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
   __shared__ float normsm[2][D < 32 ? 1 : D / 32][3];  // q.q, k.k, q.k partials per conv warp
   __shared__ uint64_t full[kDecMaxStages], empty[kDecMaxStages];
   __shared__ DecMeta meta[kDecMaxStages];
+  __shared__ int8_t par_sm[MODE == kDecTree ? kDecMaxStages : 1][MODE == kDecTree ? kDecMaxTree : 1];
   const lin_state_pool_t& pool = p.pool;
   const lin_decode_args_t& a = p.a;
   const int H = pool.num_heads;
@@ -370,6 +374,13 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
             if (m.h == 0) report(a.status, LIN_ST_BAD_ACCEPT);
           } else {
             m.valid = m.acc > 0;  // nothing accepted: nothing to load or run
+            if (MODE == kDecTree) {
+              for (int t = 0; t < ND; ++t) {
+                const int pt = a.parent[int64_t(m.r) * ND + t];
+                if (pt < -1 || pt >= t) m.valid = 0;
+              }
+              if (!m.valid && m.h == 0) report(a.status, LIN_ST_BAD_TREE);
+            }
           }
         }
       }
@@ -391,6 +402,8 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
             abort = true;
           } else {
             meta[s] = mj;
+            if (MODE == kDecTree && mj.valid)
+              for (int t = 0; t < ND; ++t) par_sm[s][t] = static_cast<int8_t>(a.parent[int64_t(mj.r) * ND + t]);
             if (mj.valid) {
               const uint32_t sf = full_bar(s);
               const uint32_t s0 = s_base + s * stage_bytes;
@@ -471,6 +484,22 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
       float* ys = ysm[tc & 1];
       const int64_t tok = int64_t(m.r) * ND + j;
       const bool live = REPLAY ? (m.valid && j < m.acc) : static_cast<bool>(m.valid);
+      // a tree draft whose parent is not the previous draft starts from the
+      // parent's stored state and window (the slot's for a root); each thread
+      // reads back only the rows and channels it wrote itself
+      const char* src_t = nullptr;
+      const char* src_c = nullptr;
+      if (MODE == kDecTree && live && j > 0) {
+        const int pj = par_sm[s][j];
+        if (pj != j - 1) {
+          src_t = pj < 0 ? slot_t
+                         : static_cast<const char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
+                               m.r * a.spec.temporal_req_stride + pj * a.spec.temporal_step_stride + m.h * head_bytes;
+          src_c = pj < 0 ? slot_c
+                         : static_cast<const char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
+                               m.r * a.spec.conv_req_stride + pj * a.spec.conv_step_stride;
+        }
+      }
       float beta = 0.f, gh = 0.f;
       char* dt = nullptr;
       char* dc = nullptr;
@@ -502,7 +531,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
             tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                   int64_t(m.ts) * pool.conv_slot_stride;
           }
-        } else if (MODE == kDecStates) {
+        } else if (MODE == kDecStates || MODE == kDecTree) {
           dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
                m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
           dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
@@ -516,7 +545,10 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
             const int cl = pt * D + t;
             float win[3], w[4];
 #pragma unroll
-            for (int q = 0; q < 3; ++q) win[q] = load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
+            for (int q = 0; q < 3; ++q)
+              win[q] = (MODE == kDecTree && src_c)
+                           ? load_elem(src_c, (int64_t(pt) * H * D + int64_t(m.h) * D + t) * 3 + q, pool.conv_dtype)
+                           : load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
 #pragma unroll
             for (int q = 0; q < 4; ++q) w[q] = load_elem(buf + L.w, cl * 4 + q, a.io_dtype);
             const float xin = load_elem(sx, cl, a.io_dtype);
@@ -526,7 +558,8 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
               if (ND > 1) store_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype, nw[q]);  // next draft's window
-              if (MODE == kDecStates || (MODE == kDecReplay && dc)) store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
+              if (MODE == kDecStates || MODE == kDecTree || (MODE == kDecReplay && dc))
+                store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
               if (tcv) store_elem(tcv, ch * 3 + q, pool.conv_dtype, nw[q]);
             }
             y3[pt] = silu_on ? silu(y) : y;
@@ -605,7 +638,11 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
 #pragma unroll
         for (int i = 0; i < C::RB; ++i) {
           const int row = row0 + (rb + i) * C::RSTEP;
-          Pair8<ST>::load(sst + (int64_t(row) * D + lr * 8) * ES, sv[i]);
+          const int64_t roff = (int64_t(row) * D + lr * 8) * ES;
+          if (MODE == kDecTree && src_t)
+            Pair8<ST>::load(src_t + roff, sv[i]);
+          else
+            Pair8<ST>::load(sst + roff, sv[i]);
           uint64_t dk2 = 0ull, dq2 = 0ull;
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
@@ -655,7 +692,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           const uint64_t u2 = f2pack(u[i], u[i]);
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) sv[i][e2] = ffma2(u2, k2[e2], sv[i][e2]);
-          if (MODE == kDecStates || (MODE == kDecReplay && dt)) Pair8<ST>::store(dt + off, sv[i]);
+          if (MODE == kDecStates || MODE == kDecTree || (MODE == kDecReplay && dt)) Pair8<ST>::store(dt + off, sv[i]);
           if (tt) Pair8<ST>::store(tt + off, sv[i]);
           if (ND > 1) {
             Pair8<ST>::round(sv[i]);  // the next draft starts from the stored state
@@ -796,8 +833,12 @@ struct DecodeLaunchCache {
 template <int D, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           const int32_t* accept, cudaStream_t stream) {
-  static DecodeLaunchCache caches[3];  // one per DecMode
-  DecodeLaunchCache& cache = caches[accept ? kDecReplay : (a.n_draft > 1 && !a.spec.temporal ? kDecOutputsOnly : kDecStates)];
+  const int mode = accept ? kDecReplay
+                   : (a.n_draft > 1 && a.parent && a.spec.temporal) ? kDecTree
+                   : (a.n_draft > 1 && !a.spec.temporal) ? kDecOutputsOnly
+                                                         : kDecStates;
+  static DecodeLaunchCache caches[4];  // one per DecMode
+  DecodeLaunchCache& cache = caches[mode];
   DecodeParams p{pool, a, accept};
   const int stage = decode_stage_bytes(pool, a);
   if (stage > kDecodeMaxStage) return cudaErrorInvalidValue;
@@ -806,10 +847,10 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (stages > kDecMaxStages) stages = kDecMaxStages;
   if (stages < 2) stages = 2;
   const int smem = stages * stage;
-  const int mode = accept ? kDecReplay : (a.n_draft > 1 && !a.spec.temporal ? kDecOutputsOnly : kDecStates);
   auto kern = mode == kDecReplay ? decode_kernel<D, ST, kDecReplay>
-                                 : (mode == kDecOutputsOnly ? decode_kernel<D, ST, kDecOutputsOnly>
-                                                            : decode_kernel<D, ST, kDecStates>);
+             : mode == kDecTree   ? decode_kernel<D, ST, kDecTree>
+             : mode == kDecOutputsOnly ? decode_kernel<D, ST, kDecOutputsOnly>
+                                       : decode_kernel<D, ST, kDecStates>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

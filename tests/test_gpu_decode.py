@@ -260,6 +260,85 @@ def test_replay_commit_equals_spec_commit(sdt, gate):
     assert np.array_equal(np64(pb.conv), op["conv"])
 
 
+TREES = [[-1, -1, 0, 0, 1, 2, 2, 5],   # the MambaRadixCache page's shape (9.6): two roots, depth 4
+         [-1, 0, 1, 2, 3, 4, 5, 6],     # a chain written as parents
+         [-1, -1, -1, 0, 1, 2, 3, 3],   # three roots
+         [-1, 0, 0, 2, 2, 2, 5, 1]]
+
+
+def _path(par, node):
+    p = []
+    while node >= 0:
+        p.insert(0, node)
+        node = par[node]
+    return p
+
+
+@pytest.mark.parametrize("sdt,gate", [(torch.bfloat16, L.LIN_GATE_PER_KEY),
+                                      (torch.float32, L.LIN_GATE_PER_HEAD)])
+def test_tree_verify_and_commit(sdt, gate):
+    """Draft-tree verify (MambaRadixCache page 8.3, 9.6: retrieve_parent_token):
+    every node's output and per-step state equal, bit for bit, the linear
+    verify of its root-to-node path, and match the oracle; committing an
+    accepted node equals the oracle's commit (boundaries at 256 included); a
+    request whose tree has a parent outside [-1, j) is skipped with
+    LIN_ST_BAD_TREE."""
+    H, D, ND = 2, 128, 8
+    B = len(TREES) + 1
+    dims = W.LayerDims(num_heads=H, head_k=D, head_v=D)
+    pool = L.StatePool(1, 16, H, D, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV)
+    fill_pool(pool, 41, std=0.1)
+    op = oracle_pool(pool)
+    conv_w = W.randn((dims.conv_channels, 4), 41, "tr.w", std=0.5).to(torch.bfloat16).to(DEV)
+    x, g, beta = (t.to(DEV) for t in W.make_decode_inputs(dims, B, ND, gate, torch.bfloat16, 41, tag="tr"))
+    parents = TREES + [[-1, 0, 2, 0, 1, 2, 2, 5]]  # the last tree is malformed (draft 2 is its own parent)
+    slots, pos = [1, 2, 3, 4, 5], [253, 100, 254, 7, 0]  # trees 0 and 2 cross 256 (ancestor, node)
+    spec = L.SpecBuffer(pool, B, ND)
+    out = torch.zeros((B, ND, H, D), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    par = _i32(parents).view(B, ND)
+    L.lin_state_decode(pool, layer=0, x=x, conv_w=conv_w, g=g, beta=beta, out=out, slot=_i32(slots),
+                       pos=_i32(pos), spec=spec, gate_mode=gate, flags=FLAGS, status=st, parent=par)
+    assert L.lin_state_read_status(st) == L.LIN_ST_BAD_TREE
+    ospec = O.make_spec_buffer(1, B, ND, H, D, D, dims.conv_channels)
+    oo, ost = O.decode(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots, pos, None, 0, gate,
+                       FLAGS, 1.0, "f32", spec=ospec, parent=parents)
+    assert ost == O.ST_BAD_TREE
+    tol = TOL_F32 if sdt == torch.float32 else TOL_BF16
+    good = list(range(len(TREES)))
+    assert max_rel_per_head(np64(out)[good], oo[good], 3) < tol
+    # every node equals the linear verify of its path, bit for bit
+    for r in good:
+        for node in range(ND):
+            path = _path(parents[r], node)
+            if len(path) < 2:
+                continue
+            n = len(path)
+            sp = L.SpecBuffer(pool, 1, n)
+            o1 = torch.zeros((1, n, H, D), device=DEV)
+            L.lin_state_decode(pool, layer=0, x=x[r:r + 1, path].contiguous(), conv_w=conv_w,
+                               g=g[r:r + 1, path].contiguous(), beta=beta[r:r + 1, path].contiguous(),
+                               out=o1, slot=_i32([slots[r]]), pos=_i32([pos[r]]), spec=sp,
+                               gate_mode=gate, flags=FLAGS)
+            assert torch.equal(o1[0, -1], out[r, node]), (r, node)
+            assert torch.equal(sp.temporal[0, 0, -1], spec.temporal[0, r, node]), (r, node)
+            assert torch.equal(sp.conv[0, 0, -1], spec.conv[0, r, node]), (r, node)
+    # commit an accepted node of each tree
+    track = [9, 10, 11, 12, 13]
+    acc_node = [7, 5, 4, -1, 3]
+    L.lin_state_spec_commit(pool, spec=spec, slot=_i32(slots), pos=_i32(pos), n_draft=ND,
+                            track_slot=_i32(track), track_interval=256, status=st, parent=par,
+                            accept_node=_i32(acc_node))
+    assert L.lin_state_read_status(st) == 0
+    O.spec_commit(op, ospec, 0, 1, slots[:4], pos[:4], None, track[:4], 256, ND,
+                  parent=parents[:4], accept_node=acc_node[:4])
+    t = np64(pool.temporal[0])
+    for s_ in slots[:4] + track[:4]:
+        assert max_rel_per_head(t[s_], op["temporal"][0, s_], 0) < tol
+    assert np.array_equal(np64(pool.conv)[0, slots[:4] + track[:4]],
+                          op["conv"][0, slots[:4] + track[:4]])
+
+
 def test_decode_status_bits():
     dims = W.LayerDims(num_heads=1, head_k=32, head_v=32)
     pool = L.StatePool(1, 8, 1, 32, device=DEV)
