@@ -16,6 +16,13 @@ What it computes, token by token and in the order the pages state it:
   (GDN), followed by the output o = S' q.
   -- Kimi-K3 notes, "Speculative decoding" (the recurrent update) and the
      "g" ring paragraph (GDN g is one scalar per head, KDA g has 128 values).
+* Additive (Mamba2 SSD) form, with FLAG_UPDATE_ADDITIVE: the same state,
+  pool and tracking, but the update is the plain state-space recurrence
+      S' = S Diag(alpha) + beta v k^T
+  (no delta correction). The pages write it as S_new = A x S_old + B x x
+  with activations (hidden_states, dt, B, C); in this layout alpha =
+  exp(dt A) per head, beta = dt, k = B, v = x, q = C.
+  -- MambaRadixCache page section 9.3 ("什么是输入激活值").
 * Warm or cold start from a slot: has_initial_state = 1 loads the slot,
   0 starts from zero.
   -- Qwen3.5 Linear-State Prefix Cache, section 5.1 step 5 and section 6.4.
@@ -53,6 +60,7 @@ GATE_PER_KEY = 1
 FLAG_QK_L2NORM = 1
 FLAG_CONV_SILU = 2
 FLAG_VALIDATE = 4
+FLAG_UPDATE_ADDITIVE = 32
 
 # Device status bits, as the library documents them.
 ST_BAD_SLOT = 1
@@ -147,9 +155,12 @@ def token_step(S, cw, x_t, conv_w, g_t, beta_t, H, K, V, gate_mode, flags, q_sca
         alpha = np.exp(g_t)
     # S Diag(alpha): column c of S (key channel c) scaled by alpha[c].
     S_dec = S * alpha[:, None, :]
-    # d = beta (v - (S Diag(alpha)) k)
-    pred = np.einsum("hvk,hk->hv", S_dec, k)
-    d = beta_t[:, None] * (v - pred)
+    # d = beta (v - (S Diag(alpha)) k); the additive form drops the prediction
+    if flags & FLAG_UPDATE_ADDITIVE:
+        d = beta_t[:, None] * v
+    else:
+        pred = np.einsum("hvk,hk->hv", S_dec, k)
+        d = beta_t[:, None] * (v - pred)
     # S' = S Diag(alpha) + d k^T
     S_new = S_dec + d[:, :, None] * k[:, None, :]
     # o = S' q

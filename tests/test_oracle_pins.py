@@ -169,6 +169,65 @@ def test_scalar_head_closed_form():
         np.testing.assert_allclose(S[h, 0, 0], total, rtol=1e-11)
 
 
+def _ssd_quadratic_form(S0, x, g, beta, H, K, V, gate_mode):
+    """The additive recurrence unrolled (the state-space / masked-attention
+    duality): with b_t = sum_{r<=t} log alpha_r per key channel,
+        o_t = sum_{s<=t} beta_s v_s sum_c q_tc k_sc exp(b_tc - b_sc)
+              + S_0 (exp(b_t) . q_t),
+        S_T = S_0 Diag(exp(b_T)) + sum_s beta_s v_s (exp(b_T - b_s) . k_s)^T.
+    q, k, v are the raw inputs (identity conv, no normalisation)."""
+    L = x.shape[0]
+    q = x[:, :H * K].reshape(L, H, K)
+    k = x[:, H * K:2 * H * K].reshape(L, H, K)
+    v = x[:, 2 * H * K:].reshape(L, H, V)
+    lg = np.repeat(g[:, :, None], K, axis=2) if gate_mode == O.GATE_PER_HEAD else g
+    b = np.cumsum(lg, axis=0)  # [L][H][K]
+    out = np.zeros((L, H, V))
+    for t in range(L):
+        for s_ in range(t + 1):
+            w = np.einsum("hc,hc->h", q[t] * np.exp(b[t] - b[s_]), k[s_])
+            out[t] += (beta[s_] * w)[:, None] * v[s_]
+        out[t] += np.einsum("hvk,hk->hv", S0, np.exp(b[t]) * q[t])
+    S = S0 * np.exp(b[-1])[:, None, :]
+    for s_ in range(L):
+        S += beta[s_][:, None, None] * v[s_][:, :, None] * (np.exp(b[-1] - b[s_]) * k[s_])[:, None, :]
+    return S, out
+
+
+@pytest.mark.parametrize("gate_mode", [O.GATE_PER_HEAD, O.GATE_PER_KEY])
+def test_additive_matches_ssd_quadratic_form(gate_mode):
+    """FLAG_UPDATE_ADDITIVE (S' = S Diag(alpha) + beta v k^T) against its
+    unrolled quadratic form, warm start; the delta-rule result differs."""
+    H, K, V, L = 2, 6, 5, 19
+    x, w, g, beta, S0, cw0 = _tiny_inputs(11, H, K, V, L, gate_mode)
+    w[:] = 0.0
+    w[:, 3] = 1.0
+    S, cw, out = _run_oracle_one(S0, cw0, x, w, g, beta, H, K, V, gate_mode,
+                                 O.FLAG_UPDATE_ADDITIVE)
+    Se, oute = _ssd_quadratic_form(S0, x, g, beta, H, K, V, gate_mode)
+    np.testing.assert_allclose(out, oute, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(S, Se, rtol=1e-11, atol=1e-12)
+    Sd, _, outd = _run_oracle_one(S0, cw0, x, w, g, beta, H, K, V, gate_mode, 0)
+    assert not np.allclose(outd, oute, rtol=1e-3, atol=1e-3)
+
+
+def test_additive_unit_decay_is_sum_of_outer_products():
+    """alpha = 1, S_0 = 0, any keys: S = sum_i beta_i v_i k_i^T (no interference
+    term, unlike the delta rule), through the conv and SiLU path."""
+    H, K, V, L = 1, 5, 3, 9
+    x, w, g, beta, _, _ = _tiny_inputs(12, H, K, V, L, O.GATE_PER_HEAD, warm=False)
+    g[:] = 0.0
+    S, _, _ = _run_oracle_one(np.zeros((H, V, K)), np.zeros((x.shape[1], 3)), x, w, g, beta,
+                              H, K, V, O.GATE_PER_HEAD, O.FLAG_UPDATE_ADDITIVE | O.FLAG_CONV_SILU)
+    C = x.shape[1]
+    y = np.zeros((L, C))
+    for c in range(C):
+        y[:, c] = np.convolve(np.concatenate([np.zeros(3), x[:, c]]), w[c][::-1], mode="valid")
+    y = y / (1.0 + np.exp(-y))
+    expect = sum(beta[i, 0] * np.outer(y[i, 2 * K:], y[i, K:2 * K]) for i in range(L))
+    np.testing.assert_allclose(S[0], expect, rtol=1e-12, atol=1e-13)
+
+
 def test_gdn_equals_kda_with_broadcast_gate():
     H, K, V, L = 2, 6, 6, 15
     x, w, g, beta, S0, cw0 = _tiny_inputs(6, H, K, V, L, O.GATE_PER_HEAD)
