@@ -140,7 +140,7 @@ class Workload:
 
 class PrefillWorkload(Workload):
     def __init__(self, L, dev, name, dims, lengths, prefixes, warm, gate_mode, io_dtype,
-                 out_dtype, state_dtype, track_stride, tracks_per_req, gate, seed=0):
+                 out_dtype, state_dtype, track_stride, tracks_per_req, gate, seed=0, flags=None):
         self.L, self.dev, self.name = L, dev, name
         self.unit = "tok/s"
         self.kernel = "prefill"
@@ -176,7 +176,8 @@ class PrefillWorkload(Workload):
                        cu_seqlens=b.cu_seqlens, prefix_len=b.prefix_len, slot=self.slot,
                        has_initial_state=b.has_initial_state, track_slots=self.track,
                        cu_track=self.cu_track, track_stride=track_stride, gate_mode=gate_mode,
-                       flags=L.LIN_QK_L2NORM | L.LIN_CONV_SILU, status=self.status)
+                       flags=L.LIN_QK_L2NORM | L.LIN_CONV_SILU if flags is None else flags,
+                       status=self.status)
         need = L.lin_state_prefill_workspace(self.pool, **self.kw)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.kernel_kind = L.lin_state_prefill_kernel(self.pool, **self.kw)
@@ -403,6 +404,10 @@ def make_workload(name, L, dev):
         return PrefillWorkload(L, dev, name, W.KIMI_K3_TP8, [131072], [0], [0], W.GATE_PER_KEY,
                                torch.bfloat16, torch.bfloat16, torch.bfloat16, 64, "all",
                                "softplus")
+    if name == "mamba2_ssd_prefill":
+        return PrefillWorkload(L, dev, name, W.QWEN35_GDN, [4096] * 8, [0] * 8, [0] * 8,
+                               W.GATE_PER_HEAD, torch.bfloat16, torch.float32, torch.float32,
+                               64, 2, "ssd", flags=L.LIN_CONV_SILU | L.LIN_UPDATE_ADDITIVE)
     if name == "kda_decode":
         return DecodeWorkload(L, dev, 1)
     if name == "kda_spec_verify4_commit":
@@ -417,7 +422,7 @@ def make_workload(name, L, dev):
 HEADLINE = "qwen35_gdn_prefill"
 DEFAULT_EXTRA = ["kimi_k3_kda_varlen_prefill", "kda_decode", "kda_spec_verify4_commit",
                  "kda_spec_verify4_replay",
-                 "slot_copy_kimi_k3_69l", "kda_long_prefill_131k"]
+                 "slot_copy_kimi_k3_69l", "kda_long_prefill_131k", "mamba2_ssd_prefill"]
 
 CONFIG_TEXT = {
     "qwen35_gdn_prefill": "Qwen3.5-style GDN prefill: 1 linear layer, 32 heads, K=V=128, conv 4 over "
@@ -435,6 +440,10 @@ CONFIG_TEXT = {
                                "U{1..4} accepted tokens into the slot, 256 requests, no per-step buffer",
     "slot_copy_kimi_k3_69l": "checkpoint fork/restore copy: Kimi-K3 slot over 69 layers (29,039,616 B), "
                              "64 random src->dst pairs per batch in a 256-slot pool",
+    "mamba2_ssd_prefill": "Mamba2-style SSD prefill (additive update, no delta correction): 32 heads, "
+                          "headdim = d_state = 128, conv 4 + SiLU over x|B|C, no q/k norm, "
+                          "dt = softplus(N(0,1)-3), A = -U[1,16] per head, bf16 inputs, fp32 state "
+                          "and outputs, 8 requests x 4096 tokens, snapshot every 64 (ping-pong)",
     "kda_long_prefill_131k": "single-request KDA prefill, 131072 tokens, 12 heads, bf16, cold, "
                              "snapshots every 64 into 2048 distinct track slots",
 }

@@ -90,8 +90,14 @@ enum {
   LIN_CONV_SILU = 2u,        /* SiLU on the conv output                        */
   LIN_VALIDATE = 4u,         /* extra device checks (copy aliasing)            */
   LIN_PREFILL_RECURRENT = 8u, /* prefill: force the token-by-token kernel      */
-  LIN_PREFILL_SEGMENTED = 16u /* prefill: run a batch of one request in segments
+  LIN_PREFILL_SEGMENTED = 16u, /* prefill: run a batch of one request in segments
                                  even when it is short (see lin_state_prefill) */
+  LIN_UPDATE_ADDITIVE = 32u   /* prefill, decode, verify, replay: the additive
+                                 (Mamba2 SSD) update S' = S Diag(alpha) + beta v k^T
+                                 with no delta correction ([MRC] 9.3: S_new =
+                                 A S_old + B x; alpha = exp(dt A), beta = dt,
+                                 k = B, v = x, q = C); the pool, tracking,
+                                 verify and commit work unchanged */
 };
 
 /* ---- the state pool ([MRC] 1.3; [K3] shapes) ----------------------------
@@ -145,7 +151,9 @@ typedef struct {
  * it (S M + B), so every segment's offset B (from a zero state) and
  * transition M (from the identity, with zero values) are computed in
  * parallel, a scan carries the true state across segments (fp32), and every
- * segment then runs in parallel from its true initial state. The workspace
+ * segment then runs in parallel from its true initial state; with a cycled
+ * track list only the snapshots that remain at the end in token order (the
+ * request's last n_r) are written, so the slots end up as in one piece. The workspace
  * then holds 2 fp32 states per (segment, head); with less workspace than
  * the query reports, or in lin_state_prefill_noalloc, the request runs in
  * one piece. */

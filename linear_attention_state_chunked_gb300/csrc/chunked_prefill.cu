@@ -23,6 +23,9 @@
 //     MMA3  U^T = U'^T + S0 (-W)^T                N = 64,  K = 128
 //     MMA4  O^T = S0 Qhat^T + U^T P^T             N = 64,  K = 128 + 64
 //     MMA5  S   = S0 Diag(gamma_last) + U^T Ktil  N = 128, K = 64
+// The additive (Mamba2 SSD) form S_t = S_{t-1} Diag(alpha_t) + beta_t v_t k_t^T of
+// the MambaRadixCache page (section 9.3) is the same with A = 0: T = Diag(beta),
+// U = U' (no W, no solve, no MMA3 term).
 // (KDA: K_l = k exp(b - b_ref), Q_l = q exp(b - b_ref), K_r = k exp(b_ref - b)
 // with b_ref the chunk's middle row, so no exponent leaves +-(half a chunk);
 // GDN: the scalar decay exp(b_t - b_i) is applied in fp32 to A' and P'.)
@@ -262,6 +265,7 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* tmap, uint32_t ds
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_but_one() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 
 // hi / lo fp16 split of four values: hi = fp16(x), lo = fp16(x - hi).
 __device__ __forceinline__ void split4(float a, float b, float c, float d, uint32_t (&hi)[2],
@@ -533,8 +537,14 @@ __global__ void __launch_bounds__(NT, 1)
   uint32_t ph_mma = 0;
   // boundaries snapshotted before bos by earlier segments of this request
   int snap = (ntr > 0 && seg > 0) ? static_cast<int>(P / a.track_stride - P_r / a.track_stride) : 0;
+  // Segments run in parallel, so two of them may map boundaries onto the same
+  // entry of a cycled track list: there only the snapshots that survive in
+  // token order (the request's last ntr) are written.
+  const int64_t snap_total =
+      ntr > 0 ? (int64_t(P_r) + (eos - bos_r)) / a.track_stride - int64_t(P_r) / a.track_stride : 0;
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2_on = a.flags & LIN_QK_L2NORM;
+  const bool additive = a.flags & LIN_UPDATE_ADDITIVE;  // uniform over the CTA
 
   // Waits for the MMAs committed so far (thread 0 polls, everyone syncs).
   auto wait_mma = [&]() -> bool {
@@ -857,6 +867,7 @@ __global__ void __launch_bounds__(NT, 1)
     // off-diagonal X block overwrites its A block in AX once that is used;
     // above the diagonal AX holds zeros throughout.
     static_assert(NT == 512, "solve thread mapping");
+    if (!additive) {
     if (tid < 64) {
       const int blk = tid >> 4, jj = tid & 15, base = blk * 16;
       float x[16];
@@ -977,6 +988,7 @@ __global__ void __launch_bounds__(NT, 1)
       *reinterpret_cast<float2*>(AX + (32 + rhalf * 16 + rl) * AXS + c) = make_float2(-o0, -o1);
     }
     __syncthreads();
+    }  // !additive
     {
       const int t = tid >> 3, c0 = (tid & 7) * 8;
       float tv[8];
@@ -984,7 +996,9 @@ __global__ void __launch_bounds__(NT, 1)
       for (int m = 0; m < 8; ++m) {
         const int i = c0 + m;
         float xvv;
-        if ((i >> 4) == (t >> 4))
+        if (additive)
+          xvv = (i == t) ? 1.f : 0.f;  // X = I
+        else if ((i >> 4) == (t >> 4))
           xvv = XD[(t >> 4) * XBS + (t & 15) * XDS + (i & 15)];
         else
           xvv = AX[t * AXS + i];  // zero above the diagonal blocks
@@ -1015,11 +1029,11 @@ __global__ void __launch_bounds__(NT, 1)
         const uint64_t bd = umma::desc_kmajor(sb + OFF_TT, 64, k0);
         const uint64_t akh = umma::desc_mnmajor(sb + OFF_KH, 64, k0);
         const uint64_t avv = umma::desc_mnmajor(sb + OFF_VV, 64, k0);
-        umma::mma_f16(tm + COL_R2, akh, bd, id2, k0 > 0);
+        if (!additive) umma::mma_f16(tm + COL_R2, akh, bd, id2, k0 > 0);
         umma::mma_f16(tm + COL_R1, avv, bd, id2, k0 > 0);
         if (SPLIT) {
           const uint64_t bl = umma::desc_kmajor(sb + OFF_TTL, 64, k0);
-          umma::mma_f16(tm + COL_R2, akh, bl, id2, 1);
+          if (!additive) umma::mma_f16(tm + COL_R2, akh, bl, id2, 1);
           umma::mma_f16(tm + COL_R1, avv, bl, id2, 1);
         }
       }
@@ -1029,9 +1043,11 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- -W into shared memory (rows c); S0 <- S0 Diag(gamma_last) in TMEM
     {
-      float w16[16];
-      umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), w16);
-      put16<BF>(sb + OFF_WW, 128, vrow, slice * 16, w16, -1.f);
+      if (!additive) {
+        float w16[16];
+        umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), w16);
+        put16<BF>(sb + OFF_WW, 128, vrow, slice * 16, w16, -1.f);
+      }
       float v[32];
       const int cc = slice * 32;
       umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
@@ -1051,7 +1067,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int k0 = 0; k0 < DH; k0 += 16) {
         const uint64_t ad = umma::desc_kmajor(sb + OFF_SOP, 128, k0);
-        umma::mma_f16(tm + COL_R1, ad, umma::desc_mnmajor(sb + OFF_WW, 128, k0), id3, 1);
+        if (!additive) umma::mma_f16(tm + COL_R1, ad, umma::desc_mnmajor(sb + OFF_WW, 128, k0), id3, 1);
         umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
       }
       umma::mma_commit(&bar_mma);
@@ -1139,7 +1155,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
       int snap_dst = -1;
       if (ntr > 0 && full && (end_pos % a.track_stride) == 0) {
-        snap_dst = a.track_slots[t0 + (snap % ntr)];
+        if (seg_mode == kSegOff || snap >= snap_total - ntr) snap_dst = a.track_slots[t0 + (snap % ntr)];
         ++snap;
       }
       const bool last = (j == nch - 1);
@@ -1201,6 +1217,14 @@ __global__ void __launch_bounds__(NT, 1)
       umma::fence_before_sync();
       __syncthreads();
       if (tid == 0) {
+        // bulk stores carry no order among themselves: an earlier snapshot
+        // into the same track slot must have landed before this one starts.
+        // Each chunk commits one group and a slot recurs every ntr snapshots,
+        // so all but the latest group must be complete (all of them for ntr 1).
+        if (snap_dst >= 0) {
+          if (ntr == 1) bulk_wait_all();
+          else bulk_wait_but_one();
+        }
         if (full && outputs_on) tma_store_3d(&tmap_out, sb + OFF_OSTG, 0, h, static_cast<int>(row0));
         if (store_state) {
           constexpr int KB = ST == LIN_BF16 ? 64 : 32;  // key channels per tile

@@ -5,6 +5,8 @@
 // The update is the KDA recurrence of the Kimi-K3 notes ("企业官网建设流程全解析",
 // "Speculative decoding"):
 //     S' = S Diag(alpha) + d k^T,   d = beta (v - (S Diag(alpha)) k),   o = S' q
+// or, with LIN_UPDATE_ADDITIVE, the Mamba2 SSD form d = beta v of the
+// MambaRadixCache page (section 9.3).
 // Row v of S (its K key channels) evolves on its own given (k, alpha, beta, v_v),
 // so rows are spread over threads: a row is split over D/8 lanes of one warp,
 // 8 consecutive key channels per lane, which makes every state load and store
@@ -115,8 +117,8 @@ __device__ __forceinline__ void qk_norms(float* ys, bool l2) {
 // Update this thread's rows for one token; writes o for the rows it leads.
 template <int D>
 __device__ __forceinline__ void rows_update(float (&s)[TokCfg<D>::RPT][8], const float* ys,
-                                            const float (&a8)[8], float beta, float q_scale,
-                                            void* out, int64_t orow, int out_dtype) {
+                                            const float (&a8)[8], float beta, float dmul,
+                                            float q_scale, void* out, int64_t orow, int out_dtype) {
   using C = TokCfg<D>;
   const int lr = threadIdx.x % C::LPR;
   const int row0 = threadIdx.x / C::LPR;
@@ -137,7 +139,7 @@ __device__ __forceinline__ void rows_update(float (&s)[TokCfg<D>::RPT][8], const
       dot = fmaf(s[i][e], k8[e], dot);
     }
     dot = row_sum<C::LPR>(dot);
-    const float u = beta * (ys[2 * D + row] - dot);
+    const float u = beta * fmaf(-dmul, dot, ys[2 * D + row]);  // dmul 0: additive form
     float o = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -454,6 +456,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
   // factors meanwhile.
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2 = a.flags & LIN_QK_L2NORM;
+  const float dmul = (a.flags & LIN_UPDATE_ADDITIVE) ? 0.f : 1.f;  // 0: additive form
   constexpr bool REPLAY = MODE == kDecReplay;
   const int t = threadIdx.x;
   const int lr = lane % C::LPR;           // lane within the row group
@@ -676,7 +679,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
 #pragma unroll
         for (int i = 0; i < C::RB; ++i) {
           const float dk = __shfl_sync(0xffffffffu, red[0], gbase + (2 * i) * VSTEP);
-          u[i] = beta * (ys[2 * D + row0 + (rb + i) * C::RSTEP] - dk);
+          u[i] = beta * fmaf(-dmul, dk, ys[2 * D + row0 + (rb + i) * C::RSTEP]);
         }
         if (!REPLAY && (my_v & 1) && (lr % VSTEP) == 0) {
           float ui = 0.f;
@@ -793,6 +796,7 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
     }
   }
 
+  const float dmul = (a.flags & LIN_UPDATE_ADDITIVE) ? 0.f : 1.f;
   int snap = 0;
   for (int64_t t = bos; t < eos; ++t) {
     float* ys = sm.y[(t - bos) & 1];
@@ -803,7 +807,7 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
     float a8[8];
     const int64_t gbase = a.gate_mode == LIN_GATE_PER_KEY ? (t * H + h) * D : t * H + h;
     load_alpha<D>(a8, a.g, gbase, a.gate_mode);
-    rows_update<D>(s, ys, a8, a.beta[t * H + h], a.q_scale, a.out, (t * H + h) * D, a.out_dtype);
+    rows_update<D>(s, ys, a8, a.beta[t * H + h], dmul, a.q_scale, a.out, (t * H + h) * D, a.out_dtype);
     const int64_t n = P + (t - bos) + 1;
     if (nt > 0 && n % a.track_stride == 0) {
       const int dst = a.track_slots[t0 + (snap % nt)];

@@ -48,7 +48,7 @@ def oracle_slice_prefill(wl, req, heads, pool_before_t, pool_before_c):
     od = "bf16" if wl.out.dtype == torch.bfloat16 else "f32"
     out, st = O.prefill(pool, 0, x, w, g, beta, [0, e - a], [int(b.prefix_len[req])], [slot],
                         [int(b.has_initial_state[req])], tracks, [0, len(tracks)],
-                        wl.track_stride, b.gate_mode, FLAGS, 1.0, od)
+                        wl.track_stride, b.gate_mode, wl.kw["flags"], 1.0, od)
     assert st == 0
     return out, pool, slot, tracks, (a, e), ch
 
@@ -72,6 +72,12 @@ def check_prefill_slice(wl, req, heads, tol):
 def test_qwen35_gdn_prefill_full_size_sampled():
     wl = bench.make_workload("qwen35_gdn_prefill", L, DEV)
     check_prefill_slice(wl, 5, [0, 31], TOL_F32)
+
+
+def test_mamba2_ssd_prefill_full_size_sampled():
+    wl = bench.make_workload("mamba2_ssd_prefill", L, DEV)
+    assert wl.kw["flags"] & L.LIN_UPDATE_ADDITIVE
+    check_prefill_slice(wl, 3, [7, 30], TOL_F32)
 
 
 def test_kimi_k3_kda_varlen_full_size_sampled():

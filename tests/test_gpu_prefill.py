@@ -104,13 +104,16 @@ def test_qwen35_gdn_reduced(path):
     compare_slots(pool, op, [1, 2, 3, 4, 5, 6], TOL_F32)
 
 
+@pytest.mark.parametrize("pingpong", [False, True])
 @pytest.mark.parametrize("gate", [W.GATE_PER_KEY, W.GATE_PER_HEAD])
-def test_single_request_in_segments(gate):
+def test_single_request_in_segments(gate, pingpong):
     """A batch of one long request run as parallel segments (offset and
     transition runs, the fp32 scan, final runs) equals the oracle: a warm
     start at a 64-multiple prefix, a ragged last segment, snapshots every 64
-    into distinct slots that cross segment boundaries, outputs, the final state
-    and conv window; and it equals the same call run in one piece."""
+    into distinct slots that cross segment boundaries (or into a ping-pong
+    pair, where segments share track slots and only the last two snapshots
+    may remain), outputs, the final state and conv window; and it equals the
+    same call run in one piece."""
     dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
     L_, P_ = 1500, 128
     b = W.make_prefill_batch(dims, [L_], gate, dtype=torch.bfloat16, seed=4,
@@ -123,7 +126,8 @@ def test_single_request_in_segments(gate):
     ref = L.StatePool(1, 2 + n_tr, 2, 128, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV,
                       temporal=pool.temporal.clone(), conv=pool.conv.clone())
     op = oracle_pool(pool)
-    tracks = list(range(2, 2 + n_tr))
+    tracks = [2, 3] if pingpong else list(range(2, 2 + n_tr))
+    n_tr = len(tracks)
     tol = TOL_BF16 if gate == W.GATE_PER_KEY else TOL_F32
     out, oo = run_both(pool, op, b, [1], tracks, [0, n_tr], 64, "chunked",
                        out_dtype=torch.float32, flags=FLAGS | L.LIN_PREFILL_SEGMENTED)

@@ -96,6 +96,16 @@ def beta_sigmoid(shape, seed, name, device="cpu"):
     return torch.sigmoid(randn(shape, seed, name, device))
 
 
+def ssd_gates(shape, seed, name, device="cpu"):
+    """Inputs of the additive (Mamba2 SSD) form: a step size dt = softplus(z - 3),
+    z ~ N(0, 1) (median about 0.05) per (token, head), and a per-head rate
+    A = -U[1, 16] over the last axis of `shape`. Returns (g, beta) =
+    (dt * A, dt): the log-decay and the input scale."""
+    dt = torch.nn.functional.softplus(randn(shape, seed, f"{name}.dt", device) - 3.0)
+    A = -rand((shape[-1],), seed, f"{name}.A", device, 1.0, 16.0)
+    return dt * A, dt
+
+
 def l2_normalise_heads(x: torch.Tensor, dims: LayerDims) -> torch.Tensor:
     """Normalise the q and k channel groups of x [..., C] per head (input recipe
     of the tiny workload: q, k drawn N(0,1) then L2-normalised per head)."""
@@ -138,7 +148,8 @@ def make_prefill_batch(dims: LayerDims, lengths: List[int], gate_mode: int,
                        qk_prenorm: bool = False, conv_std: float = 0.5
                        ) -> PrefillBatch:
     """Varlen prefill inputs. x ~ N(0,1); conv weights ~ N(0, conv_std^2);
-    g per the gate recipe; beta = sigmoid(N(0,1))."""
+    g per the gate recipe; beta = sigmoid(N(0,1)), except gate "ssd": g and
+    beta from ssd_gates (per-head gates only)."""
     B = len(lengths)
     T = int(sum(lengths))
     H, K = dims.num_heads, dims.head_k
@@ -150,11 +161,15 @@ def make_prefill_batch(dims: LayerDims, lengths: List[int], gate_mode: int,
     conv_w = randn((C, dims.conv_width), seed, f"{tag}.conv_w", device,
                    std=conv_std).to(dtype)
     gshape = (T, H) if gate_mode == GATE_PER_HEAD else (T, H, K)
-    if gate == "softplus":
-        g = gate_log_decay_softplus(gshape, seed, f"{tag}.g", device)
+    if gate == "ssd":
+        assert gate_mode == GATE_PER_HEAD
+        g, beta = ssd_gates((T, H), seed, f"{tag}.ssd", device)
     else:
-        g = gate_log_decay_uniform(gshape, seed, f"{tag}.g", device)
-    beta = beta_sigmoid((T, H), seed, f"{tag}.beta", device)
+        if gate == "softplus":
+            g = gate_log_decay_softplus(gshape, seed, f"{tag}.g", device)
+        else:
+            g = gate_log_decay_uniform(gshape, seed, f"{tag}.g", device)
+        beta = beta_sigmoid((T, H), seed, f"{tag}.beta", device)
     cu = torch.zeros(B + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
     pre = torch.tensor(prefixes if prefixes is not None else [0] * B, dtype=torch.int32)
@@ -165,12 +180,17 @@ def make_prefill_batch(dims: LayerDims, lengths: List[int], gate_mode: int,
 
 def make_decode_inputs(dims: LayerDims, batch: int, n_draft: int, gate_mode: int,
                        dtype=torch.bfloat16, seed: int = 0, device="cpu",
-                       tag: str = "decode", step: int = 0):
-    """One decode step's inputs for `batch` requests x `n_draft` tokens."""
+                       tag: str = "decode", step: int = 0, gate: str = "softplus"):
+    """One decode step's inputs for `batch` requests x `n_draft` tokens
+    (gate "ssd": g and beta from ssd_gates, per-head gates only)."""
     H, K = dims.num_heads, dims.head_k
     C = dims.conv_channels
     t = f"{tag}.{step}"
     x = randn((batch, n_draft, C), seed, f"{t}.x", device).to(dtype)
+    if gate == "ssd":
+        assert gate_mode == GATE_PER_HEAD
+        g, beta = ssd_gates((batch, n_draft, H), seed, f"{t}.ssd", device)
+        return x, g, beta
     gshape = (batch, n_draft, H) if gate_mode == GATE_PER_HEAD else (batch, n_draft, H, K)
     g = gate_log_decay_softplus(gshape, seed, f"{t}.g", device)
     beta = beta_sigmoid((batch, n_draft, H), seed, f"{t}.beta", device)
