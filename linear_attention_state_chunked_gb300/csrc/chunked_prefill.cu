@@ -21,6 +21,8 @@
 //     MMA1  [A';P'] = [K_l;Q_l] K_r^T            N = 64,  K = 128
 //     MMA2  W^T = Khat^T T^T,  U'^T = V^T T^T     N = 64,  K = 64
 //     MMA3  U^T = U'^T + S0 (-W)^T                N = 64,  K = 128
+// (MMA4a needs only S0 and gamma . Q, so it is issued right after MMA1 and runs
+// while the solve does; MMA4b accumulates onto it.)
 //     MMA4  O^T = S0 Qhat^T + U^T P^T             N = 64,  K = 128 + 64
 //     MMA5  S   = S0 Diag(gamma_last) + U^T Ktil  N = 128, K = 64
 // The additive (Mamba2 SSD) form S_t = S_{t-1} Diag(alpha_t) + beta_t v_t k_t^T of
@@ -101,11 +103,12 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_ZB + 32 * ZS * 4 <= OFF_KR, "solve scratch inside the low-part region");
 
-// Tensor-memory columns (256 allocated).
+// Tensor-memory columns (all 512 of the SM; the kernel runs one CTA per SM).
 constexpr uint32_t COL_S = 0;    // state, fp32, lanes v
 constexpr uint32_t COL_R1 = 128; // [A';P'] -> U'^T -> U^T
-constexpr uint32_t COL_R2 = 192; // W^T -> O^T
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t COL_R2 = 192; // W^T
+constexpr uint32_t COL_RO = 256; // O^T (MMA4a is issued with MMA1)
+constexpr uint32_t TMEM_COLS = 512;
 
 
 // Segmented run of one long request (batch of 1). The state after a chunk is
@@ -801,6 +804,12 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       umma::mma_commit(&bar_mma);
+      // MMA4a: O^T = S0 Qhat^T (RO); completes before MMA2's commit fires
+      constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
+#pragma unroll
+      for (int k0 = 0; k0 < DH; k0 += 16)
+        umma::mma_f16(tm + COL_RO, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
+                      umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
     }
     if (!KDA && tid >= 32 && tid < 96) {
       // GDN: the in-chunk decay exp(b_t - b_i) factors as exp(b_t - b_s) exp(b_s - b_i),
@@ -1059,20 +1068,19 @@ __global__ void __launch_bounds__(NT, 1)
     umma::fence_before_sync();
     __syncthreads();
 
-    // ---- MMA3: U^T = U'^T + S0 (-W)^T (R1);  MMA4a: O^T = S0 Qhat^T (R2)
-    if (tid == 0) {
-      umma::fence_after_sync();
-      constexpr uint32_t id3 = umma::idesc_f16(128, 64, BF, false, true);
-      constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
+    // ---- MMA3: U^T = U'^T + S0 (-W)^T (R1); the additive form has no such term
+    if (!additive) {
+      if (tid == 0) {
+        umma::fence_after_sync();
+        constexpr uint32_t id3 = umma::idesc_f16(128, 64, BF, false, true);
 #pragma unroll
-      for (int k0 = 0; k0 < DH; k0 += 16) {
-        const uint64_t ad = umma::desc_kmajor(sb + OFF_SOP, 128, k0);
-        if (!additive) umma::mma_f16(tm + COL_R1, ad, umma::desc_mnmajor(sb + OFF_WW, 128, k0), id3, 1);
-        umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
+        for (int k0 = 0; k0 < DH; k0 += 16)
+          umma::mma_f16(tm + COL_R1, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
+                        umma::desc_mnmajor(sb + OFF_WW, 128, k0), id3, 1);
+        umma::mma_commit(&bar_mma);
       }
-      umma::mma_commit(&bar_mma);
+      if (!wait_mma()) break;
     }
-    if (!wait_mma()) break;
 
     // ---- U^T into shared memory (rows v)
     {
@@ -1087,7 +1095,7 @@ __global__ void __launch_bounds__(NT, 1)
     umma::fence_before_sync();
     __syncthreads();
 
-    // ---- MMA4b: O^T += U^T P^T (R2);  MMA5: S += U^T Ktil (S)
+    // ---- MMA4b: O^T += U^T P^T (RO);  MMA5: S += U^T Ktil (S)
     if (tid == 0) {
       umma::fence_after_sync();
       constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
@@ -1097,12 +1105,12 @@ __global__ void __launch_bounds__(NT, 1)
         const uint64_t ad = umma::desc_kmajor(sb + OFF_UT, 128, k0);
         const uint64_t bp = umma::desc_kmajor(sb + OFF_PP, 64, k0);
         const uint64_t bk = umma::desc_mnmajor(sb + OFF_KT, 64, k0);
-        umma::mma_f16(tm + COL_R2, ad, bp, id4, 1);
+        umma::mma_f16(tm + COL_RO, ad, bp, id4, 1);
         umma::mma_f16(tm + COL_S, ad, bk, id5, 1);
         if (SPLIT) {
           const uint64_t al = umma::desc_kmajor(sb + OFF_UTL, 128, k0);
-          umma::mma_f16(tm + COL_R2, ad, umma::desc_kmajor(sb + OFF_PPL, 64, k0), id4, 1);
-          umma::mma_f16(tm + COL_R2, al, bp, id4, 1);
+          umma::mma_f16(tm + COL_RO, ad, umma::desc_kmajor(sb + OFF_PPL, 64, k0), id4, 1);
+          umma::mma_f16(tm + COL_RO, al, bp, id4, 1);
           umma::mma_f16(tm + COL_S, al, bk, id5, 1);
         }
       }
@@ -1121,7 +1129,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int oes = a.out_dtype == LIN_BF16 ? 2 : 4;
       if (outputs_on) {
         float o16[16];
-        umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), o16);
+        umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_RO + slice * 16), o16);
         if (full) {
           uint8_t* ost = sm + OFF_OSTG;
           if (oes == 2) {
