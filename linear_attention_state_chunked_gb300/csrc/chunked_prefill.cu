@@ -1183,9 +1183,10 @@ __global__ void __launch_bounds__(NT, 1)
             *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
         }
         if (store_state) {
-          // state tile of 32 rows x 128 bytes, 128-byte swizzle (chunk m of row r at m ^ (r % 8))
+          // state tiles of 128 rows x 128 bytes (one per 128-byte column block,
+          // rows v in order), 128-byte swizzle (chunk m of row r at m ^ (r % 8))
           if (ST == LIN_BF16) {
-            const uint32_t tile = sb + OFF_STG + (quarter * 2 + (slice >> 1)) * 4096 + lane * 128;
+            const uint32_t tile = sb + OFF_STG + ((slice >> 1) * 4 + quarter) * 4096 + lane * 128;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               const int chunk = ((slice & 1) * 4 + m) ^ (lane & 7);
@@ -1196,7 +1197,7 @@ __global__ void __launch_bounds__(NT, 1)
                            static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 6])) | (static_cast<uint32_t>(f32_to_bf16_bits(v[8 * m + 7])) << 16));
             }
           } else {
-            const uint32_t tile = sb + OFF_STG + (quarter * 4 + slice) * 4096 + lane * 128;
+            const uint32_t tile = sb + OFF_STG + (slice * 4 + quarter) * 4096 + lane * 128;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
               const int chunk = m ^ (lane & 7);
@@ -1236,12 +1237,11 @@ __global__ void __launch_bounds__(NT, 1)
         if (full && outputs_on) tma_store_3d(&tmap_out, sb + OFF_OSTG, 0, h, static_cast<int>(row0));
         if (store_state) {
           constexpr int KB = ST == LIN_BF16 ? 64 : 32;  // key channels per tile
-          constexpr int NKB = DH / KB;
-          for (int tq = 0; tq < 4 * NKB; ++tq) {
-            const uint32_t src = sb + OFF_STG + tq * 4096;
-            const int v0 = (tq / NKB) * 32, k0 = (tq % NKB) * KB;
-            if (snap_dst >= 0) tma_store_4d(&tmap_state, src, k0, v0, h, snap_dst);
-            if (last_to_slot) tma_store_4d(&tmap_state, src, k0, v0, h, slot);
+#pragma unroll
+          for (int kb = 0; kb < DH / KB; ++kb) {
+            const uint32_t src = sb + OFF_STG + kb * 16384;
+            if (snap_dst >= 0) tma_store_4d(&tmap_state, src, kb * KB, 0, h, snap_dst);
+            if (last_to_slot) tma_store_4d(&tmap_state, src, kb * KB, 0, h, slot);
           }
         }
         bulk_commit();
@@ -1386,7 +1386,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  // state tiles: [slot][H][V][K] of this layer, box 32 rows x 128 bytes
+  // state tiles: [slot][H][V][K] of this layer, box 128 rows x 128 bytes
   CUtensorMap tmap_state;
   {
     const int es = ST == LIN_BF16 ? 2 : 4;
@@ -1395,7 +1395,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
                              static_cast<cuuint64_t>(pool.num_slots)};
     const cuuint64_t st[3] = {static_cast<cuuint64_t>(DH) * es, static_cast<cuuint64_t>(DH) * DH * es,
                               static_cast<cuuint64_t>(pool.temporal_slot_stride)};
-    const cuuint32_t bx[4] = {static_cast<cuuint32_t>(128 / es), 32, 1, 1};
+    const cuuint32_t bx[4] = {static_cast<cuuint32_t>(128 / es), DH, 1, 1};
     const cuuint32_t es4[4] = {1, 1, 1, 1};
     cr = enc(&tmap_state, ST == LIN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
              4, base, d, st, bx, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
