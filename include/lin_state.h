@@ -154,9 +154,9 @@ typedef struct {
  * segment then runs in parallel from its true initial state; with a cycled
  * track list only the snapshots that remain at the end in token order (the
  * request's last n_r) are written, so the slots end up as in one piece. The workspace
- * then holds 2 fp32 states per (segment, head); with less workspace than
- * the query reports, or in lin_state_prefill_noalloc, the request runs in
- * one piece. */
+ * then holds 2 fp32 states per (segment, head). Less workspace than the
+ * query reports is an error (LIN_EWORKSPACE); lin_state_prefill_noalloc runs
+ * the request in one piece. */
 typedef struct {
   int32_t layer;
   int32_t batch;

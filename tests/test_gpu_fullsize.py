@@ -191,3 +191,24 @@ def test_kda_verify4_replay_full_size_sampled():
         for k in range(2):
             assert rel_l2(gt[k], pool["temporal"][0, slot, k]) <= TOL_BF16
         assert np.array_equal(np64(wl.pools[0].conv[0, slot])[ch], pool["conv"][0, slot])
+
+
+def test_headline_e2e_pipeline_equals_one_call():
+    """bench.py's end-to-end leg runs the headline batch as groups of requests
+    on several streams, with host copies in and out. Its outputs read back to
+    the host equal the one-call prefill's, bit for bit (requests are
+    independent and every run starts cold), and so do the slots it leaves."""
+    wl = bench.make_workload("qwen35_gdn_prefill", L, DEV)
+    wl.step(0)
+    torch.cuda.synchronize()
+    ref_out = wl.out.clone()
+    ref_t = wl.pool.temporal.clone()
+    ref_c = wl.pool.conv.clone()
+    wl.out.zero_()
+    wl.setup_e2e()
+    assert len(wl.parts) > 1
+    wl.step_e2e(0)
+    torch.cuda.synchronize()
+    assert torch.equal(wl.h_out.to(DEV), ref_out)
+    assert torch.equal(wl.pool.temporal, ref_t)
+    assert torch.equal(wl.pool.conv, ref_c)
