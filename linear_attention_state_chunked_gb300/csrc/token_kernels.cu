@@ -218,8 +218,10 @@ constexpr uint32_t kDecWaitTries = 1u << 24;
 
 // Shared-memory layout of one decode stage (byte offsets; every piece
 // 16-aligned); the producer's bulk loads fill all of it.
+// Stage layout of one (request, head) item. Bytes [0, load) arrive by bulk
+// copies; bg holds (beta, scalar g) per draft, fetched by the producer warp.
 struct DecSmem {
-  int state, conv, w, x, g, load;
+  int state, conv, w, x, g, load, bg, size;
   __host__ __device__ DecSmem(int D, int es_state, int es_conv, int es_io, int nd, bool per_key) {
     state = 0;
     conv = state + D * D * es_state;
@@ -227,6 +229,8 @@ struct DecSmem {
     x = w + 3 * D * 4 * es_io;
     g = x + nd * 3 * D * es_io;
     load = g + (per_key ? nd * D * 4 : 0);
+    bg = load;
+    size = bg + nd * 2 * 4;
   }
 };
 
@@ -413,7 +417,8 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
                                mj.slot * pool.temporal_slot_stride + mj.h * head_bytes;
               const char* sc = static_cast<const char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                                mj.slot * pool.conv_slot_stride;
-              asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sf),
+              // the producer's own arrival comes after the (beta, g) stores below
+              asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(sf),
                            "r"(static_cast<uint32_t>(L.load))
                            : "memory");
               bulk_g2s(s0 + L.state, st, D * D * ES, sf);
@@ -433,11 +438,25 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
                   const int64_t tok = int64_t(mj.r) * ND + t;
                   bulk_g2s(s0 + L.g + t * D * 4, a.g + (tok * H + mj.h) * D, D * 4, sf);
                 }
-            } else {
-              mbar_arrive(full_bar(s));
             }
-            issued_n[s] = n;
           }
+        }
+        // (beta, scalar g) of the item's drafts into the stage, one draft per
+        // lane, while the bulk copies land; then the producer's arrival
+        // publishes them with the stage
+        const bool stage_ok = __shfl_sync(0xffffffffu, abort ? 0 : 1, 0) != 0;
+        if (stage_ok && mj.valid) {
+          float* bgs = reinterpret_cast<float*>(dsm + s * stage_bytes + L.bg);
+          for (int t = lane; t < ND; t += 32) {
+            const int64_t tok = int64_t(mj.r) * ND + t;
+            bgs[2 * t] = a.beta[tok * H + mj.h];
+            bgs[2 * t + 1] = per_key ? 0.f : a.g[tok * H + mj.h];
+          }
+        }
+        __syncwarp();
+        if (lane == 0 && stage_ok) {
+          mbar_arrive(full_bar(s));
+          issued_n[s] = n;
         }
         abort = __shfl_sync(0xffffffffu, abort, 0);
         if (abort) break;
@@ -510,8 +529,9 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
       char* tcv = nullptr;
       float pqq = 0.f, pkk = 0.f, pqk = 0.f;
       if (live) {
-        beta = a.beta[tok * H + m.h];
-        if (!per_key) gh = a.g[tok * H + m.h];
+        const float* bgs = reinterpret_cast<const float*>(buf + L.bg);
+        beta = bgs[2 * j];
+        if (!per_key) gh = bgs[2 * j + 1];
         if (REPLAY) {
           // in place: the slot after the last accepted token, the track slot
           // at a boundary crossed on the way
@@ -920,7 +940,7 @@ int device_sm_count(int dev) {
 int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a) {
   const DecSmem L(pool.head_k, dtype_size(pool.state_dtype), dtype_size(pool.conv_dtype),
                   dtype_size(a.io_dtype), a.n_draft, a.gate_mode == LIN_GATE_PER_KEY);
-  return (L.load + 127) & ~127;
+  return (L.size + 127) & ~127;
 }
 
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
