@@ -341,7 +341,11 @@ __device__ __forceinline__ void put16_split(uint32_t hi_buf, uint32_t lo_buf, in
   }
 }
 
-template <bool KDA, int ST>
+// SEG: the instantiation for the segmented launches, whose offset (after the
+// first segment) and transition runs write no outputs and skip the q (and, in
+// transition runs, the v) part of the conv and the output MMAs; the one-piece
+// launch uses SEG = false, where every run has outputs.
+template <bool KDA, int ST, bool SEG>
 __global__ void __launch_bounds__(NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x,
                            const __grid_constant__ CUtensorMap tmap_xt,
@@ -407,7 +411,8 @@ __global__ void __launch_bounds__(NT, 1)
   }
   const int P = P_r + static_cast<int>(bos - bos_r);  // tokens before bos in absolute positions
   const bool seg_last = (eos_c == eos);               // this CTA ends the request
-  const bool outputs_on = seg_mode == kSegOff || seg_mode == kSegFinal || (seg_mode == kSegOffset && seg == 0);
+  const bool outputs_on =
+      !SEG || seg_mode == kSegOff || seg_mode == kSegFinal || (seg_mode == kSegOffset && seg == 0);
   const bool state_to_ws = seg_mode == kSegOffset || seg_mode == kSegTransition;
   float* state_ws = seg_mode == kSegTransition ? p.seg_trans_out : p.seg_state_out;
   int t0 = 0, ntr = 0;
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(NT, 1)
   int init_kind = warm_r ? 1 : 0;
   if (seg > 0) init_kind = seg_mode == kSegOffset ? 0 : (seg_mode == kSegTransition ? 2 : 3);
   const bool warm = init_kind == 1;
-  const bool zero_v = seg_mode == kSegTransition;  // transition runs take no value input
+  const bool zero_v = SEG && seg_mode == kSegTransition;  // transition runs take no value input
   const int L = static_cast<int>(eos_c - bos);
   const int nch = (L + CH - 1) / CH;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
@@ -708,6 +713,19 @@ __global__ void __launch_bounds__(NT, 1)
       float yq[TPW][4], yk[TPW][4], yv[TPW][4], rq[TPW], rk[TPW];
 #pragma unroll
       for (int part = 0; part < 3; ++part) {
+        // runs without outputs need no q; transition runs take no values
+        if ((part == 0 && !outputs_on) || (part == 2 && zero_v)) {
+#pragma unroll
+          for (int i = 0; i < TPW; ++i) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (part == 0) yq[i][e] = 0.f;
+              else yv[i][e] = 0.f;
+            }
+            if (part == 0) rq[i] = 0.f;
+          }
+          continue;
+        }
         float4 w4[4];
 #pragma unroll
         for (int tap = 0; tap < 4; ++tap)
@@ -805,11 +823,13 @@ __global__ void __launch_bounds__(NT, 1)
       }
       umma::mma_commit(&bar_mma);
       // MMA4a: O^T = S0 Qhat^T (RO); completes before MMA2's commit fires
-      constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
+      if (outputs_on) {
+        constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
 #pragma unroll
-      for (int k0 = 0; k0 < DH; k0 += 16)
-        umma::mma_f16(tm + COL_RO, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
-                      umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
+        for (int k0 = 0; k0 < DH; k0 += 16)
+          umma::mma_f16(tm + COL_RO, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
+                        umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
+      }
     }
     if (!KDA && tid >= 32 && tid < 96) {
       // GDN: the in-chunk decay exp(b_t - b_i) factors as exp(b_t - b_s) exp(b_s - b_i),
@@ -1105,12 +1125,14 @@ __global__ void __launch_bounds__(NT, 1)
         const uint64_t ad = umma::desc_kmajor(sb + OFF_UT, 128, k0);
         const uint64_t bp = umma::desc_kmajor(sb + OFF_PP, 64, k0);
         const uint64_t bk = umma::desc_mnmajor(sb + OFF_KT, 64, k0);
-        umma::mma_f16(tm + COL_RO, ad, bp, id4, 1);
+        if (outputs_on) umma::mma_f16(tm + COL_RO, ad, bp, id4, 1);
         umma::mma_f16(tm + COL_S, ad, bk, id5, 1);
         if (SPLIT) {
           const uint64_t al = umma::desc_kmajor(sb + OFF_UTL, 128, k0);
-          umma::mma_f16(tm + COL_RO, ad, umma::desc_kmajor(sb + OFF_PPL, 64, k0), id4, 1);
-          umma::mma_f16(tm + COL_RO, al, bp, id4, 1);
+          if (outputs_on) {
+            umma::mma_f16(tm + COL_RO, ad, umma::desc_kmajor(sb + OFF_PPL, 64, k0), id4, 1);
+            umma::mma_f16(tm + COL_RO, al, bp, id4, 1);
+          }
           umma::mma_f16(tm + COL_S, al, bk, id5, 1);
         }
       }
@@ -1417,7 +1439,8 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  auto kern = chunked_prefill_kernel<KDA, ST>;
+  const bool segmented = sp.nseg >= 2 && seg_buf;
+  auto kern = segmented ? chunked_prefill_kernel<KDA, ST, true> : chunked_prefill_kernel<KDA, ST, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
@@ -1427,7 +1450,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
     if (e2 != cudaSuccess) return e2;
   }
   const unsigned H = static_cast<unsigned>(pool.num_heads);
-  if (sp.nseg >= 2 && seg_buf) {
+  if (segmented) {
     // one long request in segments: offset runs (segments 0 .. n-2) and
     // transition runs (1 .. n-2), the scan, then the final runs (all)
     float* bbuf = seg_buf;
