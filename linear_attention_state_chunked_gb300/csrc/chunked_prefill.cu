@@ -855,30 +855,64 @@ __global__ void __launch_bounds__(NT, 1)
         const float bet = SBETA[t];
         const float bt_ = SB[t];
         const float rfac = (KDA || s0 > t) ? 1.f : __expf(bt_ - SB[s0]);
+        // GDN: every lane of the warp reads the same 16 column factors, so the
+        // rare fallback to the direct exponential is a uniform branch
+        float cfv[16];
+        bool fast = true;
+        if (!KDA) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i = s0 + k;
-          float dec = 1.f;
-          if (!KDA) {
-            const float cf = CF[i];
-            dec = cf >= 0.f ? rfac * cf : __expf(bt_ - SB[i < t ? i : t]);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(CF + s0 + 4 * k4);
+            cfv[4 * k4] = c4.x; cfv[4 * k4 + 1] = c4.y; cfv[4 * k4 + 2] = c4.z; cfv[4 * k4 + 3] = c4.w;
           }
-          AX[t * AXS + i] = (i < t) ? bet * v[k] * dec : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) fast = fast && cfv[k] >= 0.f;
+        }
+        if (KDA || fast) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = s0 + k;
+            const float dec = KDA ? 1.f : rfac * cfv[k];
+            AX[t * AXS + i] = (i < t) ? bet * v[k] * dec : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = s0 + k;
+            const float dec = cfv[k] >= 0.f ? rfac * cfv[k] : __expf(bt_ - SB[i < t ? i : t]);
+            AX[t * AXS + i] = (i < t) ? bet * v[k] * dec : 0.f;
+          }
         }
       } else {
         const int t = vrow - 64;
         const float bt_ = SB[t];
         const float rfac = (KDA || s0 > t) ? 1.f : __expf(bt_ - SB[s0]);
         float pv[16];
+        float cfv[16];
+        bool fast = true;
+        if (!KDA) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i = s0 + k;
-          float dec = 1.f;
-          if (!KDA) {
-            const float cf = CF[i];
-            dec = cf >= 0.f ? rfac * cf : __expf(bt_ - SB[i <= t ? i : t]);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(CF + s0 + 4 * k4);
+            cfv[4 * k4] = c4.x; cfv[4 * k4 + 1] = c4.y; cfv[4 * k4 + 2] = c4.z; cfv[4 * k4 + 3] = c4.w;
           }
-          pv[k] = (i <= t) ? v[k] * dec : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) fast = fast && cfv[k] >= 0.f;
+        }
+        if (KDA || fast) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = s0 + k;
+            const float dec = KDA ? 1.f : rfac * cfv[k];
+            pv[k] = (i <= t) ? v[k] * dec : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = s0 + k;
+            const float dec = cfv[k] >= 0.f ? rfac * cfv[k] : __expf(bt_ - SB[i <= t ? i : t]);
+            pv[k] = (i <= t) ? v[k] * dec : 0.f;
+          }
         }
         if (SPLIT)
           put16_split(sb + OFF_PP, sb + OFF_PPL, 64, t, slice * 16, pv, 1.f);
