@@ -701,10 +701,10 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- conv, activation, q/k normalisation, operand rows
     {
-      // x value of window row m (chunk row tfirst - 3 + m), part, channel lane*4+e
+      // tile value of window row m (chunk row tfirst - 3 + m), part, channel
+      // lane*4+e; rows before the chunk (warp 0, m < 3) hold zeros here and
+      // their terms are added from the previous window below
       auto xv = [&](int m, int part, int e) -> float {
-        const int rel = tfirst - 3 + m;
-        if (rel < 0) return wprev[(rel + 3) * 384 + part * 128 + lane * 4 + e];
         const uint32_t w = (e < 2) ? xr[m][part].x : xr[m][part].y;
         return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
       };
@@ -730,17 +730,38 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int tap = 0; tap < 4; ++tap)
           w4[tap] = *reinterpret_cast<const float4*>(WC + tap * 384 + part * 128 + lane * 4);
+        float ypre[TPW][4];
 #pragma unroll
-        for (int i = 0; i < TPW; ++i) {
-          float ss = 0.f;
+        for (int i = 0; i < TPW; ++i)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float w0 = e == 0 ? w4[0].x : e == 1 ? w4[0].y : e == 2 ? w4[0].z : w4[0].w;
             const float w1 = e == 0 ? w4[1].x : e == 1 ? w4[1].y : e == 2 ? w4[1].z : w4[1].w;
             const float w2 = e == 0 ? w4[2].x : e == 1 ? w4[2].y : e == 2 ? w4[2].z : w4[2].w;
             const float w3 = e == 0 ? w4[3].x : e == 1 ? w4[3].y : e == 2 ? w4[3].z : w4[3].w;
-            float yy = w0 * xv(i, part, e) + w1 * xv(i + 1, part, e) + w2 * xv(i + 2, part, e) +
-                       w3 * xv(i + 3, part, e);
+            ypre[i][e] = w0 * xv(i, part, e) + w1 * xv(i + 1, part, e) + w2 * xv(i + 2, part, e) +
+                         w3 * xv(i + 3, part, e);
+          }
+        if (warp == 0) {
+          // tokens 0..2: the taps on the 3 rows before the chunk
+          const float* hp = wprev + part * 128 + lane * 4;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float w0 = e == 0 ? w4[0].x : e == 1 ? w4[0].y : e == 2 ? w4[0].z : w4[0].w;
+            const float w1 = e == 0 ? w4[1].x : e == 1 ? w4[1].y : e == 2 ? w4[1].z : w4[1].w;
+            const float w2 = e == 0 ? w4[2].x : e == 1 ? w4[2].y : e == 2 ? w4[2].z : w4[2].w;
+            const float h0 = hp[e], h1 = hp[384 + e], h2 = hp[768 + e];
+            ypre[0][e] += w0 * h0 + w1 * h1 + w2 * h2;
+            ypre[1][e] += w0 * h1 + w1 * h2;
+            ypre[2][e] += w0 * h2;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+          float ss = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float yy = ypre[i][e];
             yy = silu_on ? silu(yy) : yy;
             ss += yy * yy;
             if (part == 0) yq[i][e] = yy;
