@@ -1075,19 +1075,25 @@ __global__ void __launch_bounds__(NT, 1)
     }  // !additive
     {
       const int t = tid >> 3, c0 = (tid & 7) * 8;
+      // the thread's 8 columns lie in one 16-wide block: a diagonal block of
+      // X (XD) or an off-diagonal one (AX, zero above the diagonal)
+      float xrow[8];
+      if (additive) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) xrow[m] = (c0 + m == t) ? 1.f : 0.f;  // X = I
+      } else {
+        const float* src = ((c0 >> 4) == (t >> 4)) ? XD + (t >> 4) * XBS + (t & 15) * XDS + (c0 & 15)
+                                                   : AX + t * AXS + c0;
+        const float4 x0 = reinterpret_cast<const float4*>(src)[0], x1 = reinterpret_cast<const float4*>(src)[1];
+        xrow[0] = x0.x; xrow[1] = x0.y; xrow[2] = x0.z; xrow[3] = x0.w;
+        xrow[4] = x1.x; xrow[5] = x1.y; xrow[6] = x1.z; xrow[7] = x1.w;
+      }
+      const float4 b0 = *reinterpret_cast<const float4*>(SBETA + c0);
+      const float4 b1 = *reinterpret_cast<const float4*>(SBETA + c0 + 4);
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
       float tv[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int i = c0 + m;
-        float xvv;
-        if (additive)
-          xvv = (i == t) ? 1.f : 0.f;  // X = I
-        else if ((i >> 4) == (t >> 4))
-          xvv = XD[(t >> 4) * XBS + (t & 15) * XDS + (i & 15)];
-        else
-          xvv = AX[t * AXS + i];  // zero above the diagonal blocks
-        tv[m] = xvv * SBETA[i];
-      }
+      for (int m = 0; m < 8; ++m) tv[m] = xrow[m] * bv[m];
       const uint32_t off = umma::rp_offset(t, c0, 64);
       if (SPLIT) {
         uint32_t h0[2], l0[2], h1[2], l1[2];
