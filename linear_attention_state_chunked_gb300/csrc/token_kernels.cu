@@ -475,6 +475,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
   // factors meanwhile.
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2 = a.flags & LIN_QK_L2NORM;
+  const bool bf16_conv = a.io_dtype == LIN_BF16 && pool.conv_dtype == LIN_BF16;
   const float dmul = (a.flags & LIN_UPDATE_ADDITIVE) ? 0.f : 1.f;  // 0: additive form
   constexpr bool REPLAY = MODE == kDecReplay;
   const int t = threadIdx.x;
@@ -560,7 +561,40 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
                m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
         }  // kDecOutputsOnly: a verify that keeps no per-step states
-        if (t < D) {
+        if ((MODE == kDecOutputsOnly || MODE == kDecReplay) && t < D && bf16_conv) {
+          // bf16 inputs and conv state (the usual case): taps in one 8-byte
+          // load, no per-element dtype choice (in the modes where it measured
+          // faster; in the others the extra code costs registers)
+          const uint16_t* sx = reinterpret_cast<const uint16_t*>(buf + L.x) + j * 3 * D;
+          const uint16_t* swin = reinterpret_cast<const uint16_t*>(buf + L.conv);
+          const uint2* staps = reinterpret_cast<const uint2*>(buf + L.w);
+          float y3[3];
+#pragma unroll
+          for (int pt = 0; pt < 3; ++pt) {
+            const int cl = pt * D + t;
+            const uint2 wt = staps[cl];
+            const float w0 = __uint_as_float(wt.x << 16), w1 = __uint_as_float(wt.x & 0xffff0000u);
+            const float w2 = __uint_as_float(wt.y << 16), w3 = __uint_as_float(wt.y & 0xffff0000u);
+            const uint16_t b0 = swin[cl * 3], b1 = swin[cl * 3 + 1], b2 = swin[cl * 3 + 2], bx = sx[cl];
+            const float win0 = bf16_bits_to_f32(b0), win1 = bf16_bits_to_f32(b1), win2 = bf16_bits_to_f32(b2);
+            const float xin = bf16_bits_to_f32(bx);
+            const float y = w0 * win0 + w1 * win1 + w2 * win2 + w3 * xin;
+            const uint16_t nw[3] = {b1, b2, bx};  // the new window, already bf16
+            const int64_t ch = int64_t(pt) * H * D + int64_t(m.h) * D + t;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+              if (ND > 1) reinterpret_cast<uint16_t*>(buf + L.conv)[cl * 3 + q] = nw[q];  // next draft's window
+              if (MODE == kDecStates || MODE == kDecTree || (MODE == kDecReplay && dc))
+                reinterpret_cast<uint16_t*>(dc)[ch * 3 + q] = nw[q];
+              if (tcv) reinterpret_cast<uint16_t*>(tcv)[ch * 3 + q] = nw[q];
+            }
+            y3[pt] = silu_on ? silu(y) : y;
+            ys[cl] = y3[pt];
+          }
+          pqq = y3[0] * y3[0];
+          pkk = y3[1] * y3[1];
+          pqk = y3[0] * y3[1];
+        } else if (t < D) {
           const uint8_t* sx = buf + L.x + j * 3 * D * esi;
           float y3[3];
 #pragma unroll
