@@ -206,47 +206,59 @@ class PrefillWorkload(Workload):
         self._k_end()
 
     # e2e: the public call with host inputs (pinned) and the outputs read back.
-    # The batch runs as E2E_PARTS groups of requests, pipelined over three kinds
-    # of stream: one copies inputs in, one per group runs its prefill call as
-    # soon as its inputs have landed, one copies outputs out. Requests are
-    # independent, so every group's call computes exactly what the whole batch
-    # computes for its requests; the host link (about 0.2 TB/s each way, 0.3 TB/s
-    # both ways together) is then busy while the GPU computes.
-    E2E_PARTS = 8
+    # The batch is pipelined over streams: one copies inputs in, one per request
+    # runs that request's calls as soon as their inputs have landed, one copies
+    # outputs out, so the host link (about 0.2 TB/s each way, 0.3 TB/s both ways
+    # together) stays busy while the GPU computes. Each request runs as
+    # E2E_PIECES calls over consecutive 64-aligned token ranges, each warm from
+    # the state the one before left in the slot (the pages' chunked prefill),
+    # with its track list rotated so every boundary lands where the one-call run
+    # puts it. The inputs of every request's first piece are copied first, so
+    # the last computation to wait on the link is a short one. Requests are
+    # independent and a state round-trips the pool exactly (fp32 state, bf16
+    # windows that are copies of bf16 inputs), so the outputs and slots equal
+    # the one-call run's bit for bit.
+    E2E_PIECES = 4
 
     def setup_e2e(self):
         b, L, dev = self.b, self.L, self.dev
         cu = b.cu_seqlens.cpu().tolist()
         cut = self.cu_track.cpu().tolist()
-        B = self.B
-        P = min(self.E2E_PARTS, B)
-        bounds = [round(B * k / P) for k in range(P + 1)]
+        pre = b.prefix_len.cpu().tolist()
+        warm = b.has_initial_state.cpu().tolist()
+        tracks = self.track.cpu().tolist()
+        stride = self.track_stride
         self.h_in = [t.cpu().pin_memory() for t in (b.x, b.g, b.beta)]
         self.d_in = [b.x, b.g, b.beta]
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
-        self.parts = []
-        for k in range(P):
-            r0, r1 = bounds[k], bounds[k + 1]
-            t0, t1 = cu[r0], cu[r1]
-            kw = dict(self.kw)
-            kw.update(x=b.x[t0:t1], g=b.g[t0:t1], beta=b.beta[t0:t1], out=self.out[t0:t1],
-                      cu_seqlens=(b.cu_seqlens[r0:r1 + 1] - cu[r0]).contiguous(),
-                      prefix_len=b.prefix_len[r0:r1].contiguous(), slot=self.slot[r0:r1].contiguous(),
-                      has_initial_state=b.has_initial_state[r0:r1].contiguous(),
-                      track_slots=self.track[cut[r0]:cut[r1]].contiguous(),
-                      cu_track=(self.cu_track[r0:r1 + 1] - cut[r0]).contiguous())
-            # a group of one request would run in segments (three passes,
-            # made for a lone request that leaves SMs idle); here the groups
-            # fill the GPU together, so such a group goes through
-            # lin_state_prefill_noalloc, which runs it in one piece (a batch of
-            # one needs none of that call's shared scratch)
-            need = L.lin_state_prefill_workspace(self.pool, **kw)
-            self.parts.append(dict(
-                kw=kw, ws=torch.empty(max(need, 16), dtype=torch.uint8, device=dev),
-                one=(r1 - r0 == 1),
-                h_in=[h[t0:t1] for h in self.h_in], d_in=[d[t0:t1] for d in self.d_in],
-                h_out=self.h_out[t0:t1], d_out=self.out[t0:t1], stream=torch.cuda.Stream(),
-                ev_c=None, ev_d=None))
+        i32 = lambda v: torch.tensor(v, dtype=torch.int32, device=dev)
+        pieces = []  # (piece index, request, part)
+        for r in range(self.B):
+            Lr = cu[r + 1] - cu[r]
+            cuts = sorted({0, Lr} | {(Lr * k // self.E2E_PIECES) // 64 * 64 for k in range(1, self.E2E_PIECES)})
+            stream = torch.cuda.Stream()
+            tr = tracks[cut[r]:cut[r + 1]]
+            for k, (o0, o1) in enumerate(zip(cuts[:-1], cuts[1:])):
+                if o1 <= o0:
+                    continue
+                t0, t1 = cu[r] + o0, cu[r] + o1
+                # boundaries before this piece, counted within the whole call
+                j0 = ((pre[r] + o0) // stride - pre[r] // stride) if stride else 0
+                rot = [tr[(j0 + q) % len(tr)] for q in range(len(tr))] if tr else []
+                kw = dict(self.kw)
+                kw.update(x=b.x[t0:t1], g=b.g[t0:t1], beta=b.beta[t0:t1], out=self.out[t0:t1],
+                          cu_seqlens=i32([0, o1 - o0]), prefix_len=i32([pre[r] + o0]),
+                          slot=self.slot[r:r + 1].contiguous(),
+                          has_initial_state=torch.tensor([warm[r] if o0 == 0 else 1],
+                                                         dtype=torch.int64, device=dev),
+                          track_slots=i32(rot) if rot else None,
+                          cu_track=i32([0, len(rot)]) if rot else None)
+                pieces.append((k, r, dict(
+                    kw=kw, h_in=[h[t0:t1] for h in self.h_in], d_in=[d[t0:t1] for d in self.d_in],
+                    h_out=self.h_out[t0:t1], d_out=self.out[t0:t1], stream=stream,
+                    ev_c=None, ev_d=None)))
+        pieces.sort(key=lambda e: (e[0], e[1]))
+        self.parts = [pt for _, _, pt in pieces]
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
         return (sum(t.numel() * t.element_size() for t in self.h_in),
                 self.out.numel() * self.out.element_size())
@@ -256,7 +268,7 @@ class PrefillWorkload(Workload):
         start = cur.record_event()
         self.s_in.wait_event(start)
         for pt in self.parts:
-            # a group's input buffers are free once its previous call has run
+            # a piece's input buffers are free once its previous call has run
             if pt["ev_c"] is not None:
                 self.s_in.wait_event(pt["ev_c"])
             with torch.cuda.stream(self.s_in):
@@ -268,10 +280,10 @@ class PrefillWorkload(Workload):
             if pt["ev_d"] is not None:  # its outputs of the previous step are read back
                 s.wait_event(pt["ev_d"])
             with torch.cuda.stream(s):
-                if pt["one"]:
-                    self.L.lin_state_prefill_noalloc(self.pool, **pt["kw"])
-                else:
-                    self.L.lin_state_prefill(self.pool, workspace=pt["ws"], **pt["kw"])
+                # one request per call: noalloc runs it in one piece (a lone
+                # request would otherwise go in segments, made for a request
+                # that leaves SMs idle; here the requests fill the GPU together)
+                self.L.lin_state_prefill_noalloc(self.pool, **pt["kw"])
                 pt["ev_c"] = s.record_event()
             self.s_out.wait_event(pt["ev_c"])
             with torch.cuda.stream(self.s_out):

@@ -240,10 +240,12 @@ def test_kda_verify4_commit_full_size_sampled():
 
 
 def test_headline_e2e_pipeline_equals_one_call():
-    """bench.py's end-to-end leg runs the headline batch as groups of requests
-    on several streams, with host copies in and out. Its outputs read back to
-    the host equal the one-call prefill's, bit for bit (requests are
-    independent and every run starts cold), and so do the slots it leaves."""
+    """bench.py's end-to-end leg runs each request of the headline batch as
+    consecutive warm-started calls on its own stream, with host copies in and
+    out. Its outputs read back to the host equal the one-call prefill's, bit
+    for bit (requests are independent; the fp32 state and the bf16 windows
+    round-trip the pool exactly), and so do the slots and track slots it
+    leaves."""
     wl = bench.make_workload("qwen35_gdn_prefill", L, DEV)
     wl.step(0)
     torch.cuda.synchronize()
