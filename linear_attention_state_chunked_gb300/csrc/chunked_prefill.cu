@@ -778,6 +778,12 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       bool range_bad = false;
+      // KDA: exp(b_last - b) = exp(b_last - b_ref) exp(b_ref - b), the first
+      // factor per channel for the chunk; both stay inside e^+-80 (the range
+      // check below), so the product is the exponential up to one rounding
+      float ecl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ecl[e] = KDA ? __expf(blast[e] - bref[e]) : 1.f;
 #pragma unroll
       for (int i = 0; i < TPW; ++i) {
         const int t = tfirst + i;
@@ -795,9 +801,9 @@ __global__ void __launch_bounds__(NT, 1)
           const int ee = KDA ? e : 0;
           const float b = cs[i][ee];
           eH[e] = __expf(b);
-          eT[e] = __expf(blast[ee] - b);
           eL[e] = KDA ? __expf(b - bref[ee]) : 1.f;
           eR[e] = KDA ? __expf(bref[ee] - b) : 1.f;
+          eT[e] = KDA ? ecl[e] * eR[e] : __expf(blast[ee] - b);
           // the factored decay must stay inside fp32 range (see LIN_ST_DECAY_RANGE)
           if (KDA && ok && fabsf(b - bref[ee]) > 80.f) range_bad = true;
         }
