@@ -182,6 +182,17 @@ class PrefillWorkload(Workload):
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.kernel_kind = L.lin_state_prefill_kernel(self.pool, **self.kw)
         self.kernel = "prefill_chunked" if self.kernel_kind == L.LIN_KERNEL_CHUNKED else "prefill_recurrent"
+        # launches per call: the chunked kernel, plus the longest-first order of
+        # a varlen batch; a request in segments takes the offset / transition
+        # launch, the scan (more than two segments) and the final launch
+        if self.kernel_kind == L.LIN_KERNEL_CHUNKED:
+            ow = (B * 4 + 255) // 256 * 256 if 1 < B <= 4096 else 0
+            seg_bytes = need - ow
+            if seg_bytes > 0:
+                nseg = seg_bytes // (2 * dims.num_heads * dims.head_k * dims.head_k * 4)
+                self.launches_per_step = (1 if ow else 0) + 2 + (1 if nseg > 2 else 0)
+            else:
+                self.launches_per_step = 1 + (1 if ow else 0)
         # algorithmic bytes (inputs, outputs, snapshots, initial and final state)
         H, K, V, C = dims.num_heads, dims.head_k, dims.head_v, dims.conv_channels
         es_io, es_o, es_s = b.x.element_size(), self.out.element_size(), self.pool.temporal.element_size()
