@@ -181,3 +181,87 @@ def test_ssd_verify_replay_and_spec_commit():
     for s_ in range(S):
         assert max_rel_per_head(t[s_], op["temporal"][0, s_], 0) < TOL_BF16
     assert np.array_equal(np64(pb.conv), op["conv"])
+
+
+def test_ssd_recurrent_small_head_and_noalloc():
+    """The additive form on the token-by-token prefill at head dim 32 (fp32
+    pool, two ragged requests, one warm), and through lin_state_prefill_noalloc
+    on the chunked kernel (head dim 128, a batch of two)."""
+    dims = W.LayerDims(num_heads=3, head_k=32, head_v=32)
+    b = W.make_prefill_batch(dims, [150, 77], W.GATE_PER_HEAD, dtype=torch.float32, seed=8,
+                             gate="ssd", prefixes=[64, 0], warm=[1, 0], tag="ssdr")
+    pool = L.StatePool(1, 8, 3, 32, state_dtype=torch.float32, conv_dtype=torch.float32, device=DEV)
+    fill_pool(pool, 55, std=0.2)
+    op = oracle_pool(pool)
+    out, oo = _prefill_both(pool, op, b, [1, 2], [3, 4, 5, 6], [0, 2, 4], 64, "recurrent",
+                            torch.float32)
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), TOL_F32)
+    compare_slots(pool, op, list(range(1, 7)), TOL_F32)
+
+    dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
+    b = W.make_prefill_batch(dims, [333, 200], W.GATE_PER_HEAD, dtype=torch.bfloat16, seed=9,
+                             gate="ssd", tag="ssdn")
+    pool = L.StatePool(1, 8, 2, 128, state_dtype=torch.float32, conv_dtype=torch.bfloat16,
+                       device=DEV)
+    op = oracle_pool(pool)
+    T = b.total_tokens
+    out = torch.zeros((T, 2, 128), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lin_state_prefill_noalloc(pool, layer=0, x=b.x.to(DEV), conv_w=b.conv_w.to(DEV), g=b.g.to(DEV),
+                                beta=b.beta.to(DEV), out=out, cu_seqlens=b.cu_seqlens.to(DEV),
+                                prefix_len=b.prefix_len.to(DEV), slot=_i32([1, 2]),
+                                has_initial_state=b.has_initial_state.to(DEV),
+                                track_slots=_i32([3, 4, 5, 6]), cu_track=_i32([0, 2, 4]),
+                                track_stride=64, gate_mode=W.GATE_PER_HEAD, flags=FLAGS, status=st)
+    oo, ost = O.prefill(op, 0, np64(b.x), np64(b.conv_w), np64(b.g), np64(b.beta),
+                        b.cu_seqlens.tolist(), b.prefix_len.tolist(), [1, 2],
+                        b.has_initial_state.tolist(), [3, 4, 5, 6], [0, 2, 4], 64,
+                        W.GATE_PER_HEAD, FLAGS, 1.0, "f32")
+    assert L.lin_state_read_status(st) == ost == 0
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), TOL_F32)
+    compare_slots(pool, op, [1, 2, 3, 4, 5, 6], TOL_F32)
+
+
+def test_ssd_tree_verify_and_commit():
+    """Draft-tree verify and commit in the additive form: outputs, per-step
+    states and the committed node against the oracle (head dim 64, fp32)."""
+    H, D, ND = 2, 64, 8
+    trees = [[-1, -1, 0, 0, 1, 2, 2, 5], [-1, 0, 0, 2, 2, 2, 5, 1]]
+    B = len(trees)
+    dims = W.LayerDims(num_heads=H, head_k=D, head_v=D)
+    pool = L.StatePool(1, 12, H, D, state_dtype=torch.float32, conv_dtype=torch.float32, device=DEV)
+    fill_pool(pool, 56, std=0.1)
+    op = oracle_pool(pool)
+    conv_w = W.randn((dims.conv_channels, 4), 56, "ssdt.w", std=0.5).to(DEV)
+    x, g, beta = (t.to(DEV) for t in W.make_decode_inputs(dims, B, ND, L.LIN_GATE_PER_HEAD,
+                                                           torch.float32, 56, tag="ssdt",
+                                                           gate="ssd"))
+    slots, pos, track = [1, 2], [254, 100], [3, 4]
+    spec = L.SpecBuffer(pool, B, ND)
+    out = torch.zeros((B, ND, H, D), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    par = _i32(trees).view(B, ND)
+    L.lin_state_decode(pool, layer=0, x=x, conv_w=conv_w, g=g, beta=beta, out=out, slot=_i32(slots),
+                       pos=_i32(pos), spec=spec, gate_mode=L.LIN_GATE_PER_HEAD, flags=FLAGS,
+                       status=st, parent=par)
+    assert L.lin_state_read_status(st) == 0
+    ospec = O.make_spec_buffer(1, B, ND, H, D, D, dims.conv_channels)
+    oo, ost = O.decode(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots, pos, None, 0,
+                       O.GATE_PER_HEAD, FLAGS, 1.0, "f32", spec=ospec, parent=trees)
+    assert ost == 0
+    assert max_rel_per_head(np64(out), oo, 3) < TOL_F32
+    sp = np64(spec.temporal)
+    for r in range(B):
+        for j in range(ND):
+            assert max_rel_per_head(sp[0, r, j], ospec["temporal"][0, r, j], 0) < TOL_F32
+    acc_node = [7, 6]
+    L.lin_state_spec_commit(pool, spec=spec, slot=_i32(slots), pos=_i32(pos), n_draft=ND,
+                            track_slot=_i32(track), track_interval=256, status=st, parent=par,
+                            accept_node=_i32(acc_node))
+    assert L.lin_state_read_status(st) == 0
+    O.spec_commit(op, ospec, 0, 1, slots, pos, None, track, 256, ND, parent=trees,
+                  accept_node=acc_node)
+    t = np64(pool.temporal[0])
+    for s_ in slots + track:
+        assert max_rel_per_head(t[s_], op["temporal"][0, s_], 0) < TOL_F32
+    assert np.array_equal(np64(pool.conv)[0, slots + track], op["conv"][0, slots + track])
