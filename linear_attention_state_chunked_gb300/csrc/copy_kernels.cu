@@ -80,6 +80,9 @@ __global__ void __launch_bounds__(kCopyThreads) slot_copy_kernel(CopyParams p) {
   const char* src_t;
   const char* src_c;
   int dst_slot;
+  const char* src2_t = nullptr;  // commit: the track slot's source and slot
+  const char* src2_c = nullptr;
+  int dst2_slot = -1;
   const char* pool_t = static_cast<const char*>(p.pool.temporal);
   const char* pool_c = static_cast<const char*>(p.pool.conv);
 
@@ -124,73 +127,81 @@ __global__ void __launch_bounds__(kCopyThreads) slot_copy_kernel(CopyParams p) {
     src_t = pool_t + layer * p.pool.temporal_layer_stride + s * p.pool.temporal_slot_stride;
     src_c = pool_c + layer * p.pool.conv_layer_stride + s * p.pool.conv_slot_stride;
     dst_slot = op.linear_state_id;
-  } else {  // kModeCommit; blockIdx.y = 0 -> live slot, 1 -> track slot
+  } else {  // kModeCommit: the live slot, and the track slot when a boundary is crossed
     const lin_commit_args_t& c = p.commit;
-    int s = c.slot[item];
+    const int32_t* par = c.parent ? c.parent + int64_t(item) * c.n_draft : nullptr;
+    // the request's values, loaded together (no load waits on another)
+    const int s = c.slot[item];
+    const int a_in = par ? 0 : c.accept_len[item];
+    const int node_in = par ? c.accept_node[item] : -1;
+    const int ts = c.track_slot ? c.track_slot[item] : -1;
+    const int pos = c.pos ? c.pos[item] : 0;
     if (s < 0) return;
     if (s >= ns) {
-      if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_SLOT);
+      if (reporter) report(p.status, LIN_ST_BAD_SLOT);
       return;
     }
     // the accepted path: drafts 0 .. a-1 of a chain, or a tree node and its
     // ancestors (each parent strictly earlier, so the walk ends in <= n_draft steps)
     int a, last;
-    const int32_t* par = c.parent ? c.parent + int64_t(item) * c.n_draft : nullptr;
     if (par) {
-      last = c.accept_node[item];
+      last = node_in;
       if (last < -1 || last >= c.n_draft) {
-        if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_TREE);
+        if (reporter) report(p.status, LIN_ST_BAD_TREE);
         return;
       }
       a = 0;
       for (int nd = last; nd >= 0; ++a) {
         const int up = par[nd];
         if (up < -1 || up >= nd) {
-          if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_TREE);
+          if (reporter) report(p.status, LIN_ST_BAD_TREE);
           return;
         }
         nd = up;
       }
     } else {
-      a = c.accept_len[item];
+      a = a_in;
       if (a < 0 || a > c.n_draft) {
-        if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_ACCEPT);
+        if (reporter) report(p.status, LIN_ST_BAD_ACCEPT);
         return;
       }
       last = a - 1;
     }
     if (a == 0) return;
-    int ts = c.track_slot ? c.track_slot[item] : -1;
     if (ts >= ns) {
-      if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_BAD_SLOT);
+      if (reporter) report(p.status, LIN_ST_BAD_SLOT);
       return;
     }
     if (ts == s) {
-      if (reporter && blockIdx.y == 0) report(p.status, LIN_ST_TRACK_ALIAS);
+      if (reporter) report(p.status, LIN_ST_TRACK_ALIAS);
       return;
     }
-    int step;
-    if (blockIdx.y == 0) {
-      step = last;
-      dst_slot = s;
-    } else {
-      if (ts < 0 || c.track_interval <= 0) return;
-      const int pos = c.pos[item];
+    auto spec_t = [&](int step) {
+      return static_cast<const char*>(c.spec.temporal) + layer * c.spec.temporal_layer_stride +
+             item * c.spec.temporal_req_stride + step * c.spec.temporal_step_stride;
+    };
+    auto spec_c = [&](int step) {
+      return static_cast<const char*>(c.spec.conv) + layer * c.spec.conv_layer_stride +
+             item * c.spec.conv_req_stride + step * c.spec.conv_step_stride;
+    };
+    src_t = spec_t(last);
+    src_c = spec_c(last);
+    dst_slot = s;
+    if (ts >= 0 && c.track_interval > 0) {
       const int nb = ((pos + a) / c.track_interval) * c.track_interval;
-      if (nb <= pos) return;
-      // the path's node at depth nb - pos: nb - pos - 1 in a chain, or the
-      // accepted node's ancestor a - (nb - pos) levels up
-      step = nb - pos - 1;
-      if (par) {
-        step = last;
-        for (int up = a - (nb - pos); up > 0; --up) step = par[step];
+      if (nb > pos) {
+        // the path's node at depth nb - pos: nb - pos - 1 in a chain, or the
+        // accepted node's ancestor a - (nb - pos) levels up
+        int step = nb - pos - 1;
+        if (par) {
+          step = last;
+          for (int up = a - (nb - pos); up > 0; --up) step = par[step];
+        }
+        src2_t = spec_t(step);
+        src2_c = spec_c(step);
+        dst2_slot = ts;
       }
-      dst_slot = ts;
     }
-    src_t = static_cast<const char*>(c.spec.temporal) + layer * c.spec.temporal_layer_stride +
-            item * c.spec.temporal_req_stride + step * c.spec.temporal_step_stride;
-    src_c = static_cast<const char*>(c.spec.conv) + layer * c.spec.conv_layer_stride +
-            item * c.spec.conv_req_stride + step * c.spec.conv_step_stride;
   }
 
   char* dst_t = static_cast<char*>(p.pool.temporal) + layer * p.pool.temporal_layer_stride +
@@ -201,6 +212,16 @@ __global__ void __launch_bounds__(kCopyThreads) slot_copy_kernel(CopyParams p) {
     move_segment(src_t, dst_t, seg * kSegBytes, p.t_bytes);
   else
     move_segment(src_c, dst_c, (seg - p.segs_t) * kSegBytes, p.c_bytes);
+  if (dst2_slot >= 0) {
+    char* d2_t = static_cast<char*>(p.pool.temporal) + layer * p.pool.temporal_layer_stride +
+                 dst2_slot * p.pool.temporal_slot_stride;
+    char* d2_c = static_cast<char*>(p.pool.conv) + layer * p.pool.conv_layer_stride +
+                 dst2_slot * p.pool.conv_slot_stride;
+    if (seg < p.segs_t)
+      move_segment(src2_t, d2_t, seg * kSegBytes, p.t_bytes);
+    else
+      move_segment(src2_c, d2_c, (seg - p.segs_t) * kSegBytes, p.c_bytes);
+  }
 }
 
 CopyParams base_params(const lin_state_pool_t& pool, int mode, int32_t n, int32_t lb,
@@ -218,11 +239,11 @@ CopyParams base_params(const lin_state_pool_t& pool, int mode, int32_t n, int32_
   return p;
 }
 
-cudaError_t launch(const CopyParams& p, int ydim, cudaStream_t stream) {
+cudaError_t launch(const CopyParams& p, cudaStream_t stream) {
   if (p.n_items <= 0 || p.n_layers <= 0) return cudaSuccess;
   int64_t blocks = int64_t(p.n_items) * p.n_layers * (p.segs_t + p.segs_c);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  slot_copy_kernel<<<dim3(static_cast<unsigned>(blocks), ydim), kCopyThreads, 0, stream>>>(p);
+  slot_copy_kernel<<<static_cast<unsigned>(blocks), kCopyThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -237,7 +258,7 @@ cudaError_t launch_copy_slots(const lin_state_pool_t& pool, const int32_t* src,
   p.dst = dst;
   p.flags = flags;
   p.status = status;
-  return launch(p, 1, stream);
+  return launch(p, stream);
 }
 
 cudaError_t launch_restore(const lin_state_pool_t& pool, const lin_cache_op_t* ops,
@@ -247,7 +268,7 @@ cudaError_t launch_restore(const lin_state_pool_t& pool, const lin_cache_op_t* o
   p.ops = ops;
   p.has_initial_state = has_initial_state;
   p.status = status;
-  return launch(p, 1, stream);
+  return launch(p, stream);
 }
 
 cudaError_t launch_spec_commit(const lin_state_pool_t& pool, const lin_commit_args_t& a,
@@ -255,7 +276,7 @@ cudaError_t launch_spec_commit(const lin_state_pool_t& pool, const lin_commit_ar
   CopyParams p = base_params(pool, kModeCommit, a.batch, a.layer_begin, a.layer_end);
   p.commit = a;
   p.status = a.status;
-  return launch(p, a.track_slot ? 2 : 1, stream);
+  return launch(p, stream);
 }
 
 }  // namespace lin
