@@ -437,12 +437,13 @@ class CopyWorkload(Workload):
     bf16 + [4608][3] bf16 per layer, 29,039,616 B per slot) in a 256-slot pool,
     batches of 64 src -> dst pairs (distinct destinations, sources from the rest)."""
 
-    def __init__(self, L, dev, seed=0, n_batches=8):
+    def __init__(self, L, dev, seed=0, n_batches=8, layers=69):
         self.L, self.dev = L, dev
-        self.name = "slot_copy_kimi_k3_69l"
+        self.layers = layers
+        self.name = f"slot_copy_kimi_k3_{layers}l"
         self.unit = "GB/s"
         self.kernel = "slot_copy"
-        self.pool = L.StatePool(69, 256, 12, 128, state_dtype=torch.bfloat16,
+        self.pool = L.StatePool(layers, 256, 12, 128, state_dtype=torch.bfloat16,
                                 conv_dtype=torch.bfloat16, device=dev)
         g = torch.Generator(device=dev)
         g.manual_seed(seed + 5)
@@ -471,7 +472,7 @@ class CopyWorkload(Workload):
         self._k_end()
 
     def describe(self):
-        return {"pairs": 64, "layers": 69, "pool_slots": 256, "slot_bytes": self.slot_bytes}
+        return {"pairs": 64, "layers": self.layers, "pool_slots": 256, "slot_bytes": self.slot_bytes}
 
 
 def make_workload(name, L, dev):
@@ -501,6 +502,10 @@ def make_workload(name, L, dev):
         return DecodeWorkload(L, dev, 4, replay=True)
     if name == "slot_copy_kimi_k3_69l":
         return CopyWorkload(L, dev)
+    if name == "slot_copy_kimi_k3_8l":
+        # the same copies over 8 layers (a 0.86 GB pool): the case profiled
+        # with ncu, whose full capture would otherwise hold the 7.4 GB pool
+        return CopyWorkload(L, dev, layers=8)
     raise ValueError(name)
 
 
@@ -523,6 +528,8 @@ CONFIG_TEXT = {
                                "256 requests, per-step states in a spec buffer",
     "kda_spec_verify4_replay": "KDA speculative verify of 4 drafts (outputs only) + replay commit of "
                                "U{1..4} accepted tokens into the slot, 256 requests, no per-step buffer",
+    "slot_copy_kimi_k3_8l": "checkpoint fork/restore copy: Kimi-K3 slot over 8 layers (3,366,912 B), 64 "
+                            "random src->dst pairs per batch in a 256-slot pool (the profiled case)",
     "slot_copy_kimi_k3_69l": "checkpoint fork/restore copy: Kimi-K3 slot over 69 layers (29,039,616 B), "
                              "64 random src->dst pairs per batch in a 256-slot pool",
     "mamba2_ssd_prefill": "Mamba2-style SSD prefill (additive update, no delta correction): 32 heads, "
