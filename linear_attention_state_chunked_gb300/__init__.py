@@ -203,17 +203,22 @@ def dtype_code(dt: torch.dtype) -> int:
 class StatePool:
     """The slot-indexed state pool: temporal [L][S][H][V][K] and conv
     [L][S][C][3] torch tensors (layer-major, the layout of MambaPool in the
-    MambaRadixCache page, 1.3), or views with any 16-byte-multiple strides."""
+    MambaRadixCache page, 1.3), or views with any 16-byte-multiple strides.
+    head_dim is K (key channels, the state row length); head_v is V (value
+    channels, the state rows), K unless given."""
 
     def __init__(self, num_layers: int, num_slots: int, num_heads: int, head_dim: int,
                  state_dtype=torch.float32, conv_dtype=torch.bfloat16, device="cuda",
-                 temporal: Optional[torch.Tensor] = None, conv: Optional[torch.Tensor] = None):
+                 temporal: Optional[torch.Tensor] = None, conv: Optional[torch.Tensor] = None,
+                 head_v: Optional[int] = None):
         H, D = num_heads, head_dim
-        C = 3 * H * D
+        V = D if head_v is None else head_v
+        C = 2 * H * D + H * V
         self.num_layers, self.num_slots, self.num_heads, self.head_dim = num_layers, num_slots, H, D
+        self.head_k, self.head_v = D, V
         self.conv_channels = C
         if temporal is None:
-            temporal = torch.zeros((num_layers, num_slots, H, D, D), dtype=state_dtype, device=device)
+            temporal = torch.zeros((num_layers, num_slots, H, V, D), dtype=state_dtype, device=device)
         if conv is None:
             conv = torch.zeros((num_layers, num_slots, C, 3), dtype=conv_dtype, device=device)
         self.temporal, self.conv = temporal, conv
@@ -224,7 +229,7 @@ class StatePool:
         es_t, es_c = t.element_size(), c.element_size()
         d = PoolT()
         d.num_layers, d.num_slots, d.num_heads = self.num_layers, self.num_slots, self.num_heads
-        d.head_k = d.head_v = self.head_dim
+        d.head_k, d.head_v = self.head_k, self.head_v
         d.conv_channels, d.conv_width = self.conv_channels, 4
         d.state_dtype, d.conv_dtype = dtype_code(t.dtype), dtype_code(c.dtype)
         d.temporal = t.data_ptr()
@@ -240,9 +245,9 @@ class SpecBuffer:
 
     def __init__(self, pool: StatePool, max_batch: int, max_draft: int, num_layers=None):
         L = num_layers or pool.num_layers
-        H, D, C = pool.num_heads, pool.head_dim, pool.conv_channels
+        H, K, V, C = pool.num_heads, pool.head_k, pool.head_v, pool.conv_channels
         dev = pool.temporal.device
-        self.temporal = torch.zeros((L, max_batch, max_draft, H, D, D), dtype=pool.temporal.dtype, device=dev)
+        self.temporal = torch.zeros((L, max_batch, max_draft, H, V, K), dtype=pool.temporal.dtype, device=dev)
         self.conv = torch.zeros((L, max_batch, max_draft, C, 3), dtype=pool.conv.dtype, device=dev)
         self.num_layers, self.max_batch, self.max_draft = L, max_batch, max_draft
 

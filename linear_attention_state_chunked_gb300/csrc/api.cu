@@ -41,10 +41,12 @@ int check_pool(const lin_state_pool_t* p) {
   if (!valid_dtype(p->state_dtype) || !valid_dtype(p->conv_dtype))
     return fail(LIN_EINVAL, "pool: state_dtype / conv_dtype must be LIN_F32 or LIN_BF16");
   if (p->conv_width != 4) return fail(LIN_EUNSUPPORTED, "pool: conv_width must be 4");
-  if (p->head_k != p->head_v)
-    return fail(LIN_EUNSUPPORTED, "pool: head_k != head_v is not supported");
-  if (p->head_k != 16 && p->head_k != 32 && p->head_k != 64 && p->head_k != 128)
-    return fail(LIN_EUNSUPPORTED, "pool: head_k must be 16, 32, 64 or 128 (got %d)", p->head_k);
+  const bool square = p->head_k == p->head_v &&
+                      (p->head_k == 16 || p->head_k == 32 || p->head_k == 64 || p->head_k == 128);
+  if (!square && !(p->head_k == 128 && p->head_v == 64))
+    return fail(LIN_EUNSUPPORTED,
+                "pool: (head_k, head_v) must be (16,16), (32,32), (64,64), (128,128) or (128,64) (got (%d,%d))",
+                p->head_k, p->head_v);
   const int64_t C = 2LL * p->num_heads * p->head_k + int64_t(p->num_heads) * p->head_v;
   if (p->conv_channels != C)
     return fail(LIN_EINVAL, "pool: conv_channels must be 2*H*K + H*V = %lld (got %d)",

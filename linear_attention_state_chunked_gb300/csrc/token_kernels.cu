@@ -27,22 +27,26 @@ namespace {
 
 constexpr float kL2Eps = 1e-6f;
 
-template <int D>
+// D: key channels per head (state row length), V: value channels (state rows).
+template <int D, int V = D>
 struct TokCfg {
   static constexpr int LPR = D / 8;  // lanes per state row
-  static constexpr int NT = (D * LPR < 256) ? D * LPR : 256;
-  static constexpr int RPT = D * LPR / NT;  // rows per thread
+  static constexpr int NT = (V * LPR < 256) ? V * LPR : 256;
+  static constexpr int RPT = V * LPR / NT;  // rows per thread
   static constexpr int RSTEP = NT / LPR;    // row stride between a thread's rows
-  static constexpr int CH = 3 * D;          // conv channels of one head
+  static constexpr int CH = 2 * D + V;      // conv channels of one head: q | k | v
+  static constexpr int YN = CH;             // the two norm factors follow them in ys
   static constexpr int CPT = (CH + NT - 1) / NT;
   static_assert(NT % 32 == 0, "whole warps");
+  static_assert(RPT * RSTEP == V, "rows");
 };
 
-// Global conv channel of local channel cl (q | k | v of head h).
-__device__ __forceinline__ int head_channel(int cl, int h, int H, int D) {
+// Global conv channel of local channel cl (q | k | v of head h; q and k have D
+// channels per head, v has V).
+__device__ __forceinline__ int head_channel(int cl, int h, int H, int D, int V) {
   if (cl < D) return h * D + cl;
   if (cl < 2 * D) return H * D + h * D + (cl - D);
-  return 2 * H * D + h * D + (cl - 2 * D);
+  return 2 * H * D + h * V + (cl - 2 * D);
 }
 
 template <int LPR>
@@ -53,19 +57,19 @@ __device__ __forceinline__ float row_sum(float v) {
 }
 
 // Per-token shared scratch: post-conv q | k | v and the two norm factors.
-template <int D>
+template <int D, int V>
 struct TokSmem {
-  float y[2][3 * D + 2];
+  float y[2][2 * D + V + 2];
 };
 
 // Conv + activation for one token: each thread does its own channels and
 // keeps the window win[c][0..2] (oldest first) in registers.
-template <int D>
-__device__ __forceinline__ void conv_token(float (&win)[TokCfg<D>::CPT][3],
-                                           const float (&w)[TokCfg<D>::CPT][4],
-                                           const void* x, int64_t xrow, const int (&chan)[TokCfg<D>::CPT],
+template <int D, int V>
+__device__ __forceinline__ void conv_token(float (&win)[TokCfg<D, V>::CPT][3],
+                                           const float (&w)[TokCfg<D, V>::CPT][4],
+                                           const void* x, int64_t xrow, const int (&chan)[TokCfg<D, V>::CPT],
                                            int io_dtype, bool do_silu, float* ys) {
-  using C = TokCfg<D>;
+  using C = TokCfg<D, V>;
 #pragma unroll
   for (int i = 0; i < C::CPT; ++i) {
     const int cl = threadIdx.x + i * C::NT;
@@ -82,17 +86,18 @@ __device__ __forceinline__ void conv_token(float (&win)[TokCfg<D>::CPT][3],
 }
 
 // Sum of squares of q and k (first 2D entries of ys) -> 1/sqrt(ss + eps).
-template <int D>
+template <int D, int V>
 __device__ __forceinline__ void qk_norms(float* ys, bool l2) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int YN = TokCfg<D, V>::YN;
   if (!l2) {
     if (threadIdx.x == 0) {
-      ys[3 * D] = 1.f;
-      ys[3 * D + 1] = 1.f;
+      ys[YN] = 1.f;
+      ys[YN + 1] = 1.f;
     }
     return;
   }
-  constexpr int NW = TokCfg<D>::NT / 32;
+  constexpr int NW = TokCfg<D, V>::NT / 32;
   if (NW >= 2) {
     if (warp < 2) {
       const float* v = ys + warp * D;
@@ -100,7 +105,7 @@ __device__ __forceinline__ void qk_norms(float* ys, bool l2) {
       for (int i = lane; i < D; i += 32) ss += v[i] * v[i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) ys[3 * D + warp] = rsqrtf(ss + kL2Eps);
+      if (lane == 0) ys[YN + warp] = rsqrtf(ss + kL2Eps);
     }
   } else {
     for (int part = 0; part < 2; ++part) {
@@ -109,20 +114,20 @@ __device__ __forceinline__ void qk_norms(float* ys, bool l2) {
       for (int i = lane; i < D; i += 32) ss += v[i] * v[i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) ys[3 * D + part] = rsqrtf(ss + kL2Eps);
+      if (lane == 0) ys[YN + part] = rsqrtf(ss + kL2Eps);
     }
   }
 }
 
 // Update this thread's rows for one token; writes o for the rows it leads.
-template <int D>
-__device__ __forceinline__ void rows_update(float (&s)[TokCfg<D>::RPT][8], const float* ys,
+template <int D, int V>
+__device__ __forceinline__ void rows_update(float (&s)[TokCfg<D, V>::RPT][8], const float* ys,
                                             const float (&a8)[8], float beta, float dmul,
                                             float q_scale, void* out, int64_t orow, int out_dtype) {
-  using C = TokCfg<D>;
+  using C = TokCfg<D, V>;
   const int lr = threadIdx.x % C::LPR;
   const int row0 = threadIdx.x / C::LPR;
-  const float rq = ys[3 * D] * q_scale, rk = ys[3 * D + 1];
+  const float rq = ys[C::YN] * q_scale, rk = ys[C::YN + 1];
   float q8[8], k8[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -165,9 +170,9 @@ __device__ __forceinline__ void load_alpha(float (&a8)[8], const float* g, int64
   }
 }
 
-template <int D, int ST>
-__device__ __forceinline__ void store_rows(char* base, const float (&s)[TokCfg<D>::RPT][8]) {
-  using C = TokCfg<D>;
+template <int D, int V, int ST>
+__device__ __forceinline__ void store_rows(char* base, const float (&s)[TokCfg<D, V>::RPT][8]) {
+  using C = TokCfg<D, V>;
   const int lr = threadIdx.x % C::LPR, row0 = threadIdx.x / C::LPR;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
 #pragma unroll
@@ -175,9 +180,9 @@ __device__ __forceinline__ void store_rows(char* base, const float (&s)[TokCfg<D
     Vec8<ST>::store(base + (int64_t(row0 + i * C::RSTEP) * D + lr * 8) * ES, s[i]);
 }
 
-template <int D, int ST>
-__device__ __forceinline__ void load_rows(const char* base, float (&s)[TokCfg<D>::RPT][8]) {
-  using C = TokCfg<D>;
+template <int D, int V, int ST>
+__device__ __forceinline__ void load_rows(const char* base, float (&s)[TokCfg<D, V>::RPT][8]) {
+  using C = TokCfg<D, V>;
   const int lr = threadIdx.x % C::LPR, row0 = threadIdx.x / C::LPR;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
 #pragma unroll
@@ -185,14 +190,14 @@ __device__ __forceinline__ void load_rows(const char* base, float (&s)[TokCfg<D>
     Vec8<ST>::load(base + (int64_t(row0 + i * C::RSTEP) * D + lr * 8) * ES, s[i]);
 }
 
-// NS: threads that share the channels (0: the whole block).
-template <int CPT, int D, int NS = 0>
+// CH: conv channels of the head; NS: threads that share them (0: the whole block).
+template <int CPT, int CH, int NS = 0>
 __device__ __forceinline__ void store_window(void* conv_base, int conv_dtype, const int (&chan)[CPT],
                                              const float (&win)[CPT][3]) {
 #pragma unroll
   for (int i = 0; i < CPT; ++i) {
     const int cl = threadIdx.x + i * (NS ? NS : static_cast<int>(blockDim.x));
-    if (cl < 3 * D) {
+    if (cl < CH) {
 #pragma unroll
       for (int j = 0; j < 3; ++j) store_elem(conv_base, int64_t(chan[i]) * 3 + j, conv_dtype, win[i][j]);
     }
@@ -222,12 +227,14 @@ constexpr uint32_t kDecWaitTries = 1u << 24;
 // copies; bg holds (beta, scalar g) per draft, fetched by the producer warp.
 struct DecSmem {
   int state, conv, w, x, g, load, bg, size;
-  __host__ __device__ DecSmem(int D, int es_state, int es_conv, int es_io, int nd, bool per_key) {
+  // D key channels, V value channels per head (q | k | v: 2D + V conv channels)
+  __host__ __device__ DecSmem(int D, int V, int es_state, int es_conv, int es_io, int nd, bool per_key) {
+    const int CH = 2 * D + V;
     state = 0;
-    conv = state + D * D * es_state;
-    w = conv + 3 * D * 3 * es_conv;
-    x = w + 3 * D * 4 * es_io;
-    g = x + nd * 3 * D * es_io;
+    conv = state + V * D * es_state;
+    w = conv + CH * 3 * es_conv;
+    x = w + CH * 4 * es_io;
+    g = x + nd * CH * es_io;
     load = g + (per_key ? nd * D * 4 : 0);
     bg = load;
     size = bg + nd * 2 * 4;
@@ -257,17 +264,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // are summed across the row's lanes together by a transposing butterfly (each
 // exchange halves the values a lane still carries), then each row's u_r is
 // taken from the lane that ends up holding (S A k)_r.
-template <int D>
+// D: key channels (row length), V: value channels (rows) per head.
+template <int D, int V = D>
 struct DecPCfg {
   static constexpr int LPR = D / 8;  // lanes per row, 8 key channels each
   static constexpr int NC = (D * LPR) < 256 ? ((D * LPR) < 32 ? 32 : D * LPR) : 256;
   static constexpr int NCW = NC / 32;   // consumer warps
   static constexpr int NT = NC + 32;    // + one producer warp
   static constexpr int RSTEP = NC / LPR;
-  static constexpr int RPT = D / RSTEP;        // rows per consumer thread
+  static constexpr int RPT = V / RSTEP;        // rows per consumer thread
   static constexpr int RB = RPT < 4 ? RPT : 4;  // rows reduced together
   static constexpr int NV = 2 * RB;             // values reduced per lane group
-  static_assert(RPT * RSTEP == D && RPT % RB == 0, "rows");
+  static constexpr int CH = 2 * D + V;          // conv channels of one head
+  static_assert(V <= D && RPT * RSTEP == V && RPT % RB == 0, "rows");
   static_assert(NV <= LPR, "one reduced value per lane");
   static_assert(2 * D <= NC, "conv and gate threads");
 };
@@ -316,13 +325,13 @@ __device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
 enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2, kDecTree = 3 };
 constexpr int kDecMaxTree = 32;  // drafts per request in a tree verify
 
-template <int D, int ST, int MODE>
-__global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
+template <int D, int V, int ST, int MODE>
+__global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
     decode_kernel(DecodeParams p, int n_items, int stage_bytes, int stages) {
-  using C = DecPCfg<D>;
+  using C = DecPCfg<D, V>;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ __align__(16) float ysm[2][3 * D];        // post-conv q | k | v, by token parity
+  __shared__ __align__(16) float ysm[2][C::CH];        // post-conv q | k | v, by token parity
   __shared__ __align__(16) float agsm[2][D];           // per-key decay factors
   __shared__ float normsm[2][D < 32 ? 1 : D / 32][3];  // q.q, k.k, q.k partials per conv warp
   __shared__ uint64_t full[kDecMaxStages], empty[kDecMaxStages];
@@ -335,8 +344,12 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
   const bool per_key = a.gate_mode == LIN_GATE_PER_KEY;
   const int esc = pool.conv_dtype == LIN_BF16 ? 2 : 4;
   const int esi = a.io_dtype == LIN_BF16 ? 2 : 4;
-  const DecSmem L(D, ES, esc, esi, ND, per_key);
-  const int64_t head_bytes = int64_t(D) * D * ES;
+  const DecSmem L(D, V, ES, esc, esi, ND, per_key);
+  const int64_t head_bytes = int64_t(V) * D * ES;
+  // global conv channel of local channel t of part pt (q, k: D per head; v: V)
+  auto gchan = [&](int pt, int hh, int tt) -> int64_t {
+    return pt < 2 ? int64_t(pt) * H * D + int64_t(hh) * D + tt : 2LL * H * D + int64_t(hh) * V + tt;
+  };
   const int C_all = pool.conv_channels;
   const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(dsm));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -421,16 +434,17 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
               asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(sf),
                            "r"(static_cast<uint32_t>(L.load))
                            : "memory");
-              bulk_g2s(s0 + L.state, st, D * D * ES, sf);
+              bulk_g2s(s0 + L.state, st, V * D * ES, sf);
               for (int part = 0; part < 3; ++part) {
-                const int64_t ch0 = int64_t(part) * H * D + int64_t(mj.h) * D;
-                bulk_g2s(s0 + L.conv + part * D * 3 * esc, sc + ch0 * 3 * esc, D * 3 * esc, sf);
+                const int64_t ch0 = gchan(part, mj.h, 0);
+                const int nch = part < 2 ? D : V;
+                bulk_g2s(s0 + L.conv + part * D * 3 * esc, sc + ch0 * 3 * esc, nch * 3 * esc, sf);
                 bulk_g2s(s0 + L.w + part * D * 4 * esi, static_cast<const char*>(a.conv_w) + ch0 * 4 * esi,
-                         D * 4 * esi, sf);
+                         nch * 4 * esi, sf);
                 for (int t = 0; t < ND; ++t) {
                   const int64_t tok = int64_t(mj.r) * ND + t;
-                  bulk_g2s(s0 + L.x + (t * 3 + part) * D * esi,
-                           static_cast<const char*>(a.x) + (tok * C_all + ch0) * esi, D * esi, sf);
+                  bulk_g2s(s0 + L.x + (t * C::CH + part * D) * esi,
+                           static_cast<const char*>(a.x) + (tok * C_all + ch0) * esi, nch * esi, sf);
                 }
               }
               if (per_key)
@@ -565,12 +579,13 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           // bf16 inputs and conv state (the usual case): taps in one 8-byte
           // load, no per-element dtype choice (in the modes where it measured
           // faster; in the others the extra code costs registers)
-          const uint16_t* sx = reinterpret_cast<const uint16_t*>(buf + L.x) + j * 3 * D;
+          const uint16_t* sx = reinterpret_cast<const uint16_t*>(buf + L.x) + j * C::CH;
           const uint16_t* swin = reinterpret_cast<const uint16_t*>(buf + L.conv);
           const uint2* staps = reinterpret_cast<const uint2*>(buf + L.w);
           float y3[3];
 #pragma unroll
           for (int pt = 0; pt < 3; ++pt) {
+            if (V < D && pt == 2 && t >= V) break;  // v has V channels
             const int cl = pt * D + t;
             const uint2 wt = staps[cl];
             const float w0 = __uint_as_float(wt.x << 16), w1 = __uint_as_float(wt.x & 0xffff0000u);
@@ -580,7 +595,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
             const float xin = bf16_bits_to_f32(bx);
             const float y = w0 * win0 + w1 * win1 + w2 * win2 + w3 * xin;
             const uint16_t nw[3] = {b1, b2, bx};  // the new window, already bf16
-            const int64_t ch = int64_t(pt) * H * D + int64_t(m.h) * D + t;
+            const int64_t ch = gchan(pt, m.h, t);
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
               if (ND > 1) reinterpret_cast<uint16_t*>(buf + L.conv)[cl * 3 + q] = nw[q];  // next draft's window
@@ -595,23 +610,23 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           pkk = y3[1] * y3[1];
           pqk = y3[0] * y3[1];
         } else if (t < D) {
-          const uint8_t* sx = buf + L.x + j * 3 * D * esi;
+          const uint8_t* sx = buf + L.x + j * C::CH * esi;
           float y3[3];
 #pragma unroll
           for (int pt = 0; pt < 3; ++pt) {
+            if (V < D && pt == 2 && t >= V) break;  // v has V channels
             const int cl = pt * D + t;
             float win[3], w[4];
 #pragma unroll
             for (int q = 0; q < 3; ++q)
-              win[q] = (MODE == kDecTree && src_c)
-                           ? load_elem(src_c, (int64_t(pt) * H * D + int64_t(m.h) * D + t) * 3 + q, pool.conv_dtype)
-                           : load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
+              win[q] = (MODE == kDecTree && src_c) ? load_elem(src_c, gchan(pt, m.h, t) * 3 + q, pool.conv_dtype)
+                                                   : load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
 #pragma unroll
             for (int q = 0; q < 4; ++q) w[q] = load_elem(buf + L.w, cl * 4 + q, a.io_dtype);
             const float xin = load_elem(sx, cl, a.io_dtype);
             const float y = w[0] * win[0] + w[1] * win[1] + w[2] * win[2] + w[3] * xin;
             const float nw[3] = {win[1], win[2], round_to_dtype(xin, pool.conv_dtype)};
-            const int64_t ch = int64_t(pt) * H * D + int64_t(m.h) * D + t;
+            const int64_t ch = gchan(pt, m.h, t);
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
               if (ND > 1) store_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype, nw[q]);  // next draft's window
@@ -741,7 +756,7 @@ __global__ void __launch_bounds__(DecPCfg<D>::NT, 2)
           for (int i = 0; i < C::RB; ++i)
             if (i == (my_v >> 1)) ui = u[i];
           const int row = row0 + (rb + (my_v >> 1)) * C::RSTEP;
-          store_elem(a.out, (tok * H + m.h) * D + row, a.out_dtype, fmaf(ui, kq, red[0]));
+          store_elem(a.out, (tok * H + m.h) * V + row, a.out_dtype, fmaf(ui, kq, red[0]));
         }
 #pragma unroll
         for (int i = 0; i < C::RB; ++i) {
@@ -775,10 +790,10 @@ struct PrefillParams {
   lin_prefill_args_t a;
 };
 
-template <int D, int ST>
-__global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(PrefillParams p) {
-  using C = TokCfg<D>;
-  __shared__ TokSmem<D> sm;
+template <int D, int V, int ST>
+__global__ void __launch_bounds__(TokCfg<D, V>::NT) prefill_recurrent_kernel(PrefillParams p) {
+  using C = TokCfg<D, V>;
+  __shared__ TokSmem<D, V> sm;
   const lin_state_pool_t& pool = p.pool;
   const lin_prefill_args_t& a = p.a;
   const int r = blockIdx.x, h = blockIdx.y;
@@ -818,7 +833,7 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
     }
   }
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
-  const int64_t head_bytes = int64_t(D) * D * ES;
+  const int64_t head_bytes = int64_t(V) * D * ES;
   char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
                  slot * pool.temporal_slot_stride + h * head_bytes;
   char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
@@ -827,7 +842,7 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
 
   float s[C::RPT][8];
   if (warm) {
-    load_rows<D, ST>(slot_t, s);
+    load_rows<D, V, ST>(slot_t, s);
   } else {
 #pragma unroll
     for (int i = 0; i < C::RPT; ++i)
@@ -840,7 +855,7 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
 #pragma unroll
   for (int i = 0; i < C::CPT; ++i) {
     const int cl = threadIdx.x + i * C::NT;
-    chan[i] = cl < C::CH ? head_channel(cl, h, H, D) : 0;
+    chan[i] = cl < C::CH ? head_channel(cl, h, H, D, V) : 0;
 #pragma unroll
     for (int j = 0; j < 3; ++j)
       win[i][j] = (warm && cl < C::CH) ? load_elem(slot_c, int64_t(chan[i]) * 3 + j, pool.conv_dtype) : 0.f;
@@ -854,14 +869,14 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
   int snap = 0;
   for (int64_t t = bos; t < eos; ++t) {
     float* ys = sm.y[(t - bos) & 1];
-    conv_token<D>(win, w, a.x, t * C_all, chan, a.io_dtype, a.flags & LIN_CONV_SILU, ys);
+    conv_token<D, V>(win, w, a.x, t * C_all, chan, a.io_dtype, a.flags & LIN_CONV_SILU, ys);
     __syncthreads();
-    qk_norms<D>(ys, a.flags & LIN_QK_L2NORM);
+    qk_norms<D, V>(ys, a.flags & LIN_QK_L2NORM);
     __syncthreads();
     float a8[8];
     const int64_t gbase = a.gate_mode == LIN_GATE_PER_KEY ? (t * H + h) * D : t * H + h;
     load_alpha<D>(a8, a.g, gbase, a.gate_mode);
-    rows_update<D>(s, ys, a8, a.beta[t * H + h], dmul, a.q_scale, a.out, (t * H + h) * D, a.out_dtype);
+    rows_update<D, V>(s, ys, a8, a.beta[t * H + h], dmul, a.q_scale, a.out, (t * H + h) * V, a.out_dtype);
     const int64_t n = P + (t - bos) + 1;
     if (nt > 0 && n % a.track_stride == 0) {
       const int dst = a.track_slots[t0 + (snap % nt)];
@@ -871,13 +886,13 @@ __global__ void __launch_bounds__(TokCfg<D>::NT) prefill_recurrent_kernel(Prefil
                    dst * pool.temporal_slot_stride + h * head_bytes;
         char* tc = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                    dst * pool.conv_slot_stride;
-        store_rows<D, ST>(tt, s);
-        store_window<TokCfg<D>::CPT, D>(tc, pool.conv_dtype, chan, win);
+        store_rows<D, V, ST>(tt, s);
+        store_window<C::CPT, C::CH>(tc, pool.conv_dtype, chan, win);
       }
     }
   }
-  store_rows<D, ST>(slot_t, s);
-  store_window<TokCfg<D>::CPT, D>(slot_c, pool.conv_dtype, chan, win);
+  store_rows<D, V, ST>(slot_t, s);
+  store_window<C::CPT, C::CH>(slot_c, pool.conv_dtype, chan, win);
 }
 
 // Per device: the dynamic shared memory the kernel instance was last opened
@@ -888,7 +903,7 @@ struct DecodeLaunchCache {
   std::atomic<int64_t> occupancy[kMaxDevices];  // (smem << 32) | CTAs per SM
 };
 
-template <int D, int ST>
+template <int D, int V, int ST>
 cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           const int32_t* accept, cudaStream_t stream) {
   const int mode = accept ? kDecReplay
@@ -905,10 +920,10 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (stages > kDecMaxStages) stages = kDecMaxStages;
   if (stages < 2) stages = 2;
   const int smem = stages * stage;
-  auto kern = mode == kDecReplay ? decode_kernel<D, ST, kDecReplay>
-             : mode == kDecTree   ? decode_kernel<D, ST, kDecTree>
-             : mode == kDecOutputsOnly ? decode_kernel<D, ST, kDecOutputsOnly>
-                                       : decode_kernel<D, ST, kDecStates>;
+  auto kern = mode == kDecReplay ? decode_kernel<D, V, ST, kDecReplay>
+             : mode == kDecTree   ? decode_kernel<D, V, ST, kDecTree>
+             : mode == kDecOutputsOnly ? decode_kernel<D, V, ST, kDecOutputsOnly>
+                                       : decode_kernel<D, V, ST, kDecStates>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -925,7 +940,7 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if ((occ >> 32) == smem && (occ & 0xffffffff) > 0) {
     per_sm = static_cast<int>(occ & 0xffffffff);
   } else {
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DecPCfg<D>::NT, smem)) != cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DecPCfg<D, V>::NT, smem)) != cudaSuccess)
       return e;
     if (per_sm < 1) per_sm = 1;
     cache.occupancy[dev].store((int64_t(smem) << 32) | per_sm);
@@ -935,30 +950,35 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (sms <= 0) return cudaErrorInvalidDevice;
   int grid = sms * per_sm;
   if (grid > items) grid = items;
-  kern<<<grid, DecPCfg<D>::NT, smem, stream>>>(p, items, stage, stages);
+  kern<<<grid, DecPCfg<D, V>::NT, smem, stream>>>(p, items, stage, stages);
   return cudaGetLastError();
 }
 
-template <int D, int ST>
+template <int D, int V, int ST>
 cudaError_t prefill_launch(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
                            cudaStream_t stream) {
   PrefillParams p{pool, a};
-  prefill_recurrent_kernel<D, ST><<<dim3(a.batch, pool.num_heads), TokCfg<D>::NT, 0, stream>>>(p);
+  prefill_recurrent_kernel<D, V, ST><<<dim3(a.batch, pool.num_heads), TokCfg<D, V>::NT, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-#define LIN_DISPATCH_D_ST(FN, D, ST, ...)                                   \
-  do {                                                                      \
-    const bool bf = (ST) == LIN_BF16;                                       \
-    switch (D) {                                                            \
-      case 16: return bf ? FN<16, LIN_BF16>(__VA_ARGS__) : FN<16, LIN_F32>(__VA_ARGS__);    \
-      case 32: return bf ? FN<32, LIN_BF16>(__VA_ARGS__) : FN<32, LIN_F32>(__VA_ARGS__);    \
-      case 64: return bf ? FN<64, LIN_BF16>(__VA_ARGS__) : FN<64, LIN_F32>(__VA_ARGS__);    \
-      case 128: return bf ? FN<128, LIN_BF16>(__VA_ARGS__) : FN<128, LIN_F32>(__VA_ARGS__); \
-      default: return cudaErrorInvalidValue;                                \
-    }                                                                       \
+// (head_k, head_v): square heads of 16..128, or 128 key channels with 64 value
+// channels (the SSD-style head: state size 128, head dim 64).
+#define LIN_DISPATCH_D_ST(FN, D, V, ST, ...)                                          \
+  do {                                                                                \
+    const bool bf = (ST) == LIN_BF16;                                                 \
+    if ((D) == 128 && (V) == 64)                                                      \
+      return bf ? FN<128, 64, LIN_BF16>(__VA_ARGS__) : FN<128, 64, LIN_F32>(__VA_ARGS__); \
+    if ((D) != (V)) return cudaErrorInvalidValue;                                     \
+    switch (D) {                                                                      \
+      case 16: return bf ? FN<16, 16, LIN_BF16>(__VA_ARGS__) : FN<16, 16, LIN_F32>(__VA_ARGS__);      \
+      case 32: return bf ? FN<32, 32, LIN_BF16>(__VA_ARGS__) : FN<32, 32, LIN_F32>(__VA_ARGS__);      \
+      case 64: return bf ? FN<64, 64, LIN_BF16>(__VA_ARGS__) : FN<64, 64, LIN_F32>(__VA_ARGS__);      \
+      case 128: return bf ? FN<128, 128, LIN_BF16>(__VA_ARGS__) : FN<128, 128, LIN_F32>(__VA_ARGS__); \
+      default: return cudaErrorInvalidValue;                                          \
+    }                                                                                 \
   } while (0)
 
 int device_sm_count(int dev) {
@@ -972,7 +992,7 @@ int device_sm_count(int dev) {
 }
 
 int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a) {
-  const DecSmem L(pool.head_k, dtype_size(pool.state_dtype), dtype_size(pool.conv_dtype),
+  const DecSmem L(pool.head_k, pool.head_v, dtype_size(pool.state_dtype), dtype_size(pool.conv_dtype),
                   dtype_size(a.io_dtype), a.n_draft, a.gate_mode == LIN_GATE_PER_KEY);
   return (L.size + 127) & ~127;
 }
@@ -980,13 +1000,13 @@ int decode_stage_bytes(const lin_state_pool_t& pool, const lin_decode_args_t& a)
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           const int32_t* accept, cudaStream_t stream) {
   if (a.batch <= 0) return cudaSuccess;
-  LIN_DISPATCH_D_ST(decode_launch, pool.head_k, pool.state_dtype, pool, a, accept, stream);
+  LIN_DISPATCH_D_ST(decode_launch, pool.head_k, pool.head_v, pool.state_dtype, pool, a, accept, stream);
 }
 
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,
                                      const lin_prefill_args_t& a, cudaStream_t stream) {
   if (a.batch <= 0) return cudaSuccess;
-  LIN_DISPATCH_D_ST(prefill_launch, pool.head_k, pool.state_dtype, pool, a, stream);
+  LIN_DISPATCH_D_ST(prefill_launch, pool.head_k, pool.head_v, pool.state_dtype, pool, a, stream);
 }
 
 }  // namespace lin

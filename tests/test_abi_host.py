@@ -8,6 +8,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import linear_attention_state_chunked_gb300 as L
 
@@ -81,6 +82,24 @@ def test_pool_validation(field, value, code):
         p.head_v = value
     assert L.lib.lin_state_slot_bytes(ctypes.byref(p)) == code
     assert L.lib.lin_state_last_error().decode()
+
+
+@pytest.mark.parametrize("hk,hv,ok", [(128, 64, True), (128, 32, False), (64, 32, False),
+                                      (64, 128, False)])
+def test_pool_value_head_dim(hk, hv, ok):
+    """Heads with V != K: (128, 64) is accepted (slot bytes count the [H][V][K]
+    state and the 2HK + HV conv channels); other pairs are LIN_EUNSUPPORTED."""
+    H, S, NL = 3, 5, 2
+    pool = L.StatePool(NL, S, H, hk, state_dtype=torch.bfloat16, conv_dtype=torch.bfloat16,
+                       device="cpu", head_v=hv)
+    assert tuple(pool.temporal.shape) == (NL, S, H, hv, hk)
+    assert pool.conv_channels == 2 * H * hk + H * hv
+    n = L.lib.lin_state_slot_bytes(ctypes.byref(pool.desc()))
+    if ok:
+        assert n == NL * (H * hv * hk * 2 + (2 * H * hk + H * hv) * 3 * 2)
+    else:
+        assert n == L.LIN_EUNSUPPORTED
+        assert "head_v" in L.lib.lin_state_last_error().decode()
 
 
 def _prefill_args(**kw):
