@@ -317,23 +317,38 @@ __device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
   return res != 0;
 }
 
-// MODE: kDecStates (decode in place, or verify into the spec buffer),
-// kDecOutputsOnly (verify without per-step states), kDecReplay (the commit
-// form: accepted tokens per request, in place, no outputs).
-// kDecTree: verify into the spec buffer where draft j starts from the state
-// after draft parent[r][j] (-1: the slot's).
-enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2, kDecTree = 3 };
+// MODE: kDecStates (one token in place), kDecVerify (a chain of drafts into
+// the spec buffer), kDecOutputsOnly (a chain verify without per-step states),
+// kDecReplay (the commit form: accepted tokens per request, in place, no
+// outputs), kDecTree (verify into the spec buffer where draft j starts from
+// the state after draft parent[r][j], -1: the slot's).
+// The three chain modes run the drafts in groups (see the consumer loop).
+enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2, kDecTree = 3, kDecVerify = 4 };
 constexpr int kDecMaxTree = 32;  // drafts per request in a tree verify
+constexpr int kDecGroup = 4;     // drafts per group in the chain modes
+// Dynamic shared memory of one decode CTA: at most the opt-in limit (227 KB)
+// less 1 KB for the static part; at most kDecPairSmem where two CTAs share an
+// SM (228 KB per SM, 1 KB of it reserved per CTA).
+constexpr int kDecMaxDynSmem = 227 * 1024 - 1024;
+constexpr int kDecPairSmem = 112 * 1024;
+// Floats of one group buffer: post-conv q | k | v, per-key decay factors and
+// the norm partials of each conv warp, for `group` drafts.
+__host__ __device__ constexpr int dec_group_floats(int D, int V, int group) {
+  return (group * (2 * D + V + D + (D < 32 ? 1 : D / 32) * 3) + 3) & ~3;
+}
 
 template <int D, int V, int ST, int MODE>
 __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
-    decode_kernel(DecodeParams p, int n_items, int stage_bytes, int stages) {
+    decode_kernel(DecodeParams p, int n_items, int stage_bytes, int stages, int group) {
   using C = DecPCfg<D, V>;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
+  constexpr bool BATCH = MODE == kDecVerify || MODE == kDecOutputsOnly || MODE == kDecReplay;
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ __align__(16) float ysm[2][C::CH];        // post-conv q | k | v, by token parity
-  __shared__ __align__(16) float agsm[2][D];           // per-key decay factors
-  __shared__ float normsm[2][D < 32 ? 1 : D / 32][3];  // q.q, k.k, q.k partials per conv warp
+  // per-token scratch of the one-token and tree modes (the chain modes keep
+  // theirs in the group buffers after the stages)
+  __shared__ __align__(16) float ysm[BATCH ? 1 : 2][BATCH ? 4 : C::CH];  // post-conv q | k | v, by token parity
+  __shared__ __align__(16) float agsm[BATCH ? 1 : 2][BATCH ? 4 : D];     // per-key decay factors
+  __shared__ float normsm[BATCH ? 1 : 2][D < 32 ? 1 : D / 32][3];        // q.q, k.k, q.k partials per conv warp
   __shared__ uint64_t full[kDecMaxStages], empty[kDecMaxStages];
   __shared__ DecMeta meta[kDecMaxStages];
   __shared__ int8_t par_sm[MODE == kDecTree ? kDecMaxStages : 1][MODE == kDecTree ? kDecMaxTree : 1];
@@ -489,7 +504,6 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
   // factors meanwhile.
   const bool silu_on = a.flags & LIN_CONV_SILU;
   const bool l2 = a.flags & LIN_QK_L2NORM;
-  const bool bf16_conv = a.io_dtype == LIN_BF16 && pool.conv_dtype == LIN_BF16;
   const float dmul = (a.flags & LIN_UPDATE_ADDITIVE) ? 0.f : 1.f;  // 0: additive form
   constexpr bool REPLAY = MODE == kDecReplay;
   const int t = threadIdx.x;
@@ -500,6 +514,9 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
   constexpr int NPW = D < 32 ? 1 : D / 32;  // warps holding conv channels
   const int my_v = lr / VSTEP;            // value this lane ends up holding
   int tc = 0;                             // tokens done (parity of the scratch)
+  int gc = 0;                             // draft groups done (parity of the group buffer)
+  const int gfloats = dec_group_floats(D, V, group);
+  float* const gbuf = reinterpret_cast<float*>(dsm + stages * stage_bytes);
   int n = 0;
   bool abort = false;
   for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x, ++n) {
@@ -515,6 +532,231 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
                    int64_t(m.slot) * pool.temporal_slot_stride + m.h * head_bytes;
     char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                    int64_t(m.slot) * pool.conv_slot_stride;
+    if constexpr (BATCH) {
+      // A chain of drafts, in groups of `group`: the conv, gate factors and
+      // norm partials of every draft of the group first (none of them depends
+      // on the state), one barrier, then the group's row updates back to
+      // back. Group buffers alternate, so a warp starts the next group's conv
+      // while others still read the previous group. Every item runs the same
+      // number of groups (with no work when it is empty), so all consumers
+      // meet the same barriers whatever they saw. The arithmetic is the
+      // one-token path's, draft by draft.
+      for (int j0 = 0; j0 < ND; j0 += group, ++gc) {
+        const int gn = ND - j0 < group ? ND - j0 : group;
+        int nl = m.valid ? gn : 0;  // drafts of this group that run
+        if (REPLAY && nl > m.acc - j0) nl = m.acc - j0 > 0 ? m.acc - j0 : 0;
+        float* gys = gbuf + (gc & 1) * gfloats;  // [group][CH] post-conv q | k | v
+        float* gag = gys + group * C::CH;        // [group][D] per-key decay factors
+        float* gnr = gag + group * D;            // [group][NPW][3] q.q, k.k, q.k partials
+        if (t < D && nl > 0) {
+          float win[3][3], w[3][4];
+#pragma unroll
+          for (int pt = 0; pt < 3; ++pt) {
+            if (V < D && pt == 2 && t >= V) break;  // v has V channels
+            const int cl = pt * D + t;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) win[pt][q] = load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[pt][q] = load_elem(buf + L.w, cl * 4 + q, a.io_dtype);
+          }
+          for (int jj = 0; jj < nl; ++jj) {
+            const int j = j0 + jj;
+            const uint8_t* sx = buf + L.x + j * C::CH * esi;
+            // where the window after draft j goes (besides the next draft)
+            char* dc = nullptr;
+            char* tcv = nullptr;
+            if (MODE == kDecVerify) {
+              dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
+                   m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
+            } else if (REPLAY) {
+              if (j == m.acc - 1) dc = slot_c;
+              if (m.ts >= 0 && a.track_interval > 0 && (m.pos + j + 1) % a.track_interval == 0)
+                tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                      int64_t(m.ts) * pool.conv_slot_stride;
+            }
+#pragma unroll
+            for (int pt = 0; pt < 3; ++pt) {
+              if (V < D && pt == 2 && t >= V) break;
+              const int cl = pt * D + t;
+              const float xin = load_elem(sx, cl, a.io_dtype);
+              const float y = w[pt][0] * win[pt][0] + w[pt][1] * win[pt][1] + w[pt][2] * win[pt][2] +
+                              w[pt][3] * xin;
+              win[pt][0] = win[pt][1];
+              win[pt][1] = win[pt][2];
+              win[pt][2] = round_to_dtype(xin, pool.conv_dtype);
+              if (dc || tcv) {
+                const int64_t ch = gchan(pt, m.h, t);
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                  if (dc) store_elem(dc, ch * 3 + q, pool.conv_dtype, win[pt][q]);
+                  if (tcv) store_elem(tcv, ch * 3 + q, pool.conv_dtype, win[pt][q]);
+                }
+              }
+              gys[jj * C::CH + cl] = silu_on ? silu(y) : y;
+            }
+          }
+          if (j0 + gn < ND) {  // the next group starts from this window
+#pragma unroll
+            for (int pt = 0; pt < 3; ++pt) {
+              if (V < D && pt == 2 && t >= V) break;
+#pragma unroll
+              for (int q = 0; q < 3; ++q)
+                store_elem(buf + L.conv, (pt * D + t) * 3 + q, pool.conv_dtype, win[pt][q]);
+            }
+          }
+        } else if (per_key && t >= D && t < 2 * D) {
+          const float* sg = reinterpret_cast<const float*>(buf + L.g);
+          for (int jj = 0; jj < nl; ++jj) gag[jj * D + (t - D)] = expf(sg[(j0 + jj) * D + (t - D)]);
+        }
+        if (warp < NPW) {
+          // this warp's partial q.q, k.k, q.k of each draft (its own conv outputs)
+          for (int jj = 0; jj < nl; ++jj) {
+            const float yq = t < D ? gys[jj * C::CH + t] : 0.f;
+            const float yk = t < D ? gys[jj * C::CH + D + t] : 0.f;
+            float pqq = yq * yq, pkk = yk * yk, pqk = yq * yk;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              pqq += __shfl_xor_sync(0xffffffffu, pqq, o);
+              pkk += __shfl_xor_sync(0xffffffffu, pkk, o);
+              pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+            }
+            if (lane == 0) {
+              float* nr = gnr + (jj * NPW + warp) * 3;
+              nr[0] = pqq;
+              nr[1] = pkk;
+              nr[2] = pqk;
+            }
+          }
+        }
+        // the group's conv outputs published; also agrees on whether any
+        // consumer's wait gave up
+        if (consumers_sync_or(C::NC, !got)) {
+          abort = true;
+          break;
+        }
+        const float* bgs = reinterpret_cast<const float*>(buf + L.bg);
+        uint8_t* sst = buf + L.state;
+        for (int jj = 0; jj < nl; ++jj) {
+          const int j = j0 + jj;
+          const int64_t tok = int64_t(m.r) * ND + j;
+          const float* ys = gys + jj * C::CH;
+          const float beta = bgs[2 * j];
+          char* dt = nullptr;
+          char* tt = nullptr;
+          if (MODE == kDecVerify) {
+            dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
+                 m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
+          } else if (REPLAY) {
+            if (j == m.acc - 1) dt = slot_t;
+            if (m.ts >= 0 && a.track_interval > 0 && (m.pos + j + 1) % a.track_interval == 0)
+              tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                   int64_t(m.ts) * pool.temporal_slot_stride + m.h * head_bytes;
+          }
+          float sqq = 0.f, skk = 0.f, sqk = 0.f;
+#pragma unroll
+          for (int pw = 0; pw < NPW; ++pw) {
+            const float* nr = gnr + (jj * NPW + pw) * 3;
+            sqq += nr[0];
+            skk += nr[1];
+            sqk += nr[2];
+          }
+          const float rq = (l2 ? rsqrtf(sqq + kL2Eps) : 1.f) * a.q_scale;
+          const float rk = l2 ? rsqrtf(skk + kL2Eps) : 1.f;
+          const float kq = sqk * rq * rk;
+          uint64_t a2[4], q2[4], k2[4];
+          {
+            const float4* yq4 = reinterpret_cast<const float4*>(ys + lr * 8);
+            const float4* yk4 = reinterpret_cast<const float4*>(ys + D + lr * 8);
+            const uint64_t rq2 = f2pack(rq, rq), rk2 = f2pack(rk, rk);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const float4 fq = yq4[h2], fk = yk4[h2];
+              q2[2 * h2] = fmul2(f2pack(fq.x, fq.y), rq2);
+              q2[2 * h2 + 1] = fmul2(f2pack(fq.z, fq.w), rq2);
+              k2[2 * h2] = fmul2(f2pack(fk.x, fk.y), rk2);
+              k2[2 * h2 + 1] = fmul2(f2pack(fk.z, fk.w), rk2);
+            }
+            if (per_key) {
+              const float4* ag4 = reinterpret_cast<const float4*>(gag + jj * D + lr * 8);
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const float4 fa = ag4[h2];
+                a2[2 * h2] = f2pack(fa.x, fa.y);
+                a2[2 * h2 + 1] = f2pack(fa.z, fa.w);
+              }
+            } else {
+              const float av = expf(bgs[2 * j + 1]);
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) a2[e2] = f2pack(av, av);
+            }
+          }
+#pragma unroll
+          for (int rb = 0; rb < C::RPT; rb += C::RB) {
+            uint64_t sv[C::RB][4];
+            float red[C::NV];
+#pragma unroll
+            for (int i = 0; i < C::RB; ++i) {
+              const int64_t roff = (int64_t(row0 + (rb + i) * C::RSTEP) * D + lr * 8) * ES;
+              Pair8<ST>::load(sst + roff, sv[i]);
+              uint64_t dk2 = 0ull, dq2 = 0ull;
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                sv[i][e2] = fmul2(sv[i][e2], a2[e2]);
+                dk2 = ffma2(sv[i][e2], k2[e2], dk2);
+                dq2 = ffma2(sv[i][e2], q2[e2], dq2);
+              }
+              red[2 * i] = f2sum(dk2);
+              red[2 * i + 1] = f2sum(dq2);
+            }
+            // transposing butterfly, as in the one-token path
+#pragma unroll
+            for (int d = C::LPR / 2, nv = C::NV; d > 0; d >>= 1) {
+              if (nv > 1) {
+                const bool up = lr & d;
+                nv >>= 1;
+#pragma unroll
+                for (int v = 0; v < C::NV / 2; ++v) {
+                  if (v < nv) {
+                    const float keep = up ? red[v + nv] : red[v];
+                    const float send = up ? red[v] : red[v + nv];
+                    red[v] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+                  }
+                }
+              } else {
+                red[0] += __shfl_xor_sync(0xffffffffu, red[0], d);
+              }
+            }
+            float u[C::RB];
+#pragma unroll
+            for (int i = 0; i < C::RB; ++i) {
+              const float dk = __shfl_sync(0xffffffffu, red[0], gbase + (2 * i) * VSTEP);
+              u[i] = beta * fmaf(-dmul, dk, ys[2 * D + row0 + (rb + i) * C::RSTEP]);
+            }
+            if (!REPLAY && (my_v & 1) && (lr % VSTEP) == 0) {
+              float ui = 0.f;
+#pragma unroll
+              for (int i = 0; i < C::RB; ++i)
+                if (i == (my_v >> 1)) ui = u[i];
+              const int row = row0 + (rb + (my_v >> 1)) * C::RSTEP;
+              store_elem(a.out, (tok * H + m.h) * V + row, a.out_dtype, fmaf(ui, kq, red[0]));
+            }
+#pragma unroll
+            for (int i = 0; i < C::RB; ++i) {
+              const int64_t off = (int64_t(row0 + (rb + i) * C::RSTEP) * D + lr * 8) * ES;
+              const uint64_t u2 = f2pack(u[i], u[i]);
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) sv[i][e2] = ffma2(u2, k2[e2], sv[i][e2]);
+              if (dt) Pair8<ST>::store(dt + off, sv[i]);
+              if (tt) Pair8<ST>::store(tt + off, sv[i]);
+              if (ND > 1) {
+                Pair8<ST>::round(sv[i]);  // the next draft starts from the stored state
+                Pair8<ST>::store(sst + off, sv[i]);
+              }
+            }
+          }
+        }
+      }
+    } else {
     // every item runs ND token steps (with no work when it is empty), so all
     // consumers meet the same number of barriers whatever they saw
     for (int j = 0; j < ND; ++j, ++tc) {
@@ -575,41 +817,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
                m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
         }  // kDecOutputsOnly: a verify that keeps no per-step states
-        if ((MODE == kDecOutputsOnly || MODE == kDecReplay) && t < D && bf16_conv) {
-          // bf16 inputs and conv state (the usual case): taps in one 8-byte
-          // load, no per-element dtype choice (in the modes where it measured
-          // faster; in the others the extra code costs registers)
-          const uint16_t* sx = reinterpret_cast<const uint16_t*>(buf + L.x) + j * C::CH;
-          const uint16_t* swin = reinterpret_cast<const uint16_t*>(buf + L.conv);
-          const uint2* staps = reinterpret_cast<const uint2*>(buf + L.w);
-          float y3[3];
-#pragma unroll
-          for (int pt = 0; pt < 3; ++pt) {
-            if (V < D && pt == 2 && t >= V) break;  // v has V channels
-            const int cl = pt * D + t;
-            const uint2 wt = staps[cl];
-            const float w0 = __uint_as_float(wt.x << 16), w1 = __uint_as_float(wt.x & 0xffff0000u);
-            const float w2 = __uint_as_float(wt.y << 16), w3 = __uint_as_float(wt.y & 0xffff0000u);
-            const uint16_t b0 = swin[cl * 3], b1 = swin[cl * 3 + 1], b2 = swin[cl * 3 + 2], bx = sx[cl];
-            const float win0 = bf16_bits_to_f32(b0), win1 = bf16_bits_to_f32(b1), win2 = bf16_bits_to_f32(b2);
-            const float xin = bf16_bits_to_f32(bx);
-            const float y = w0 * win0 + w1 * win1 + w2 * win2 + w3 * xin;
-            const uint16_t nw[3] = {b1, b2, bx};  // the new window, already bf16
-            const int64_t ch = gchan(pt, m.h, t);
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-              if (ND > 1) reinterpret_cast<uint16_t*>(buf + L.conv)[cl * 3 + q] = nw[q];  // next draft's window
-              if (MODE == kDecStates || MODE == kDecTree || (MODE == kDecReplay && dc))
-                reinterpret_cast<uint16_t*>(dc)[ch * 3 + q] = nw[q];
-              if (tcv) reinterpret_cast<uint16_t*>(tcv)[ch * 3 + q] = nw[q];
-            }
-            y3[pt] = silu_on ? silu(y) : y;
-            ys[cl] = y3[pt];
-          }
-          pqq = y3[0] * y3[0];
-          pkk = y3[1] * y3[1];
-          pqk = y3[0] * y3[1];
-        } else if (t < D) {
+        if (t < D) {
           const uint8_t* sx = buf + L.x + j * C::CH * esi;
           float y3[3];
 #pragma unroll
@@ -773,6 +981,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
         }
       }
     }
+    }  // one-token and tree modes
     if (abort) break;
     // this warp's reads (and, in verify, writes) of the stage are done
     __syncwarp();
@@ -909,8 +1118,9 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   const int mode = accept ? kDecReplay
                    : (a.n_draft > 1 && a.parent && a.spec.temporal) ? kDecTree
                    : (a.n_draft > 1 && !a.spec.temporal) ? kDecOutputsOnly
-                                                         : kDecStates;
-  static DecodeLaunchCache caches[4];  // one per DecMode
+                   : a.n_draft > 1                        ? kDecVerify
+                                                          : kDecStates;
+  static DecodeLaunchCache caches[5];  // one per DecMode
   DecodeLaunchCache& cache = caches[mode];
   DecodeParams p{pool, a, accept};
   const int stage = decode_stage_bytes(pool, a);
@@ -919,11 +1129,24 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   int stages = (100 * 1024) / stage;
   if (stages > kDecMaxStages) stages = kDecMaxStages;
   if (stages < 2) stages = 2;
-  const int smem = stages * stage;
-  auto kern = mode == kDecReplay ? decode_kernel<D, V, ST, kDecReplay>
-             : mode == kDecTree   ? decode_kernel<D, V, ST, kDecTree>
-             : mode == kDecOutputsOnly ? decode_kernel<D, V, ST, kDecOutputsOnly>
-                                       : decode_kernel<D, V, ST, kDecStates>;
+  int smem = stages * stage;
+  int group = 1;
+  if (mode == kDecVerify || mode == kDecOutputsOnly || mode == kDecReplay) {
+    // the chain modes' two group buffers follow the stages: the largest group
+    // (up to kDecGroup drafts) that keeps two CTAs per SM where the stages
+    // alone would, else that fits one CTA
+    const int budget = 2 * stage <= 100 * 1024 ? kDecPairSmem : kDecMaxDynSmem;
+    auto gbytes = [](int g) { return 2 * dec_group_floats(D, V, g) * 4; };
+    group = a.n_draft < kDecGroup ? a.n_draft : kDecGroup;
+    while (group > 1 && smem + gbytes(group) > budget) --group;
+    smem += gbytes(group);
+    if (smem > kDecMaxDynSmem) return cudaErrorInvalidValue;
+  }
+  auto kern = mode == kDecReplay        ? decode_kernel<D, V, ST, kDecReplay>
+              : mode == kDecTree        ? decode_kernel<D, V, ST, kDecTree>
+              : mode == kDecOutputsOnly ? decode_kernel<D, V, ST, kDecOutputsOnly>
+              : mode == kDecVerify      ? decode_kernel<D, V, ST, kDecVerify>
+                                        : decode_kernel<D, V, ST, kDecStates>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -950,7 +1173,7 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (sms <= 0) return cudaErrorInvalidDevice;
   int grid = sms * per_sm;
   if (grid > items) grid = items;
-  kern<<<grid, DecPCfg<D, V>::NT, smem, stream>>>(p, items, stage, stages);
+  kern<<<grid, DecPCfg<D, V>::NT, smem, stream>>>(p, items, stage, stages, group);
   return cudaGetLastError();
 }
 
