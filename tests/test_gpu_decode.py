@@ -354,3 +354,80 @@ def test_decode_status_bits():
                        gate_mode=L.LIN_GATE_PER_HEAD, flags=FLAGS, status=st)
     assert L.lin_state_read_status(st) == L.LIN_ST_BAD_SLOT | L.LIN_ST_TRACK_ALIAS
     assert torch.equal(pool.temporal, before)
+
+
+@pytest.mark.parametrize("D,sdt,io,ND,gate", [
+    (128, torch.float32, torch.bfloat16, 7, L.LIN_GATE_PER_HEAD),   # groups of 4 + 3
+    (64, torch.bfloat16, torch.bfloat16, 9, L.LIN_GATE_PER_KEY),    # 4 + 4 + 1
+    (128, torch.float32, torch.float32, 17, L.LIN_GATE_PER_KEY),    # the staging limit: smaller groups
+])
+def test_long_chains_in_groups(D, sdt, io, ND, gate):
+    """Chains longer than one group of drafts: verify with and without a
+    per-step buffer (same outputs bit for bit), buffer commit and replay commit
+    (same pools bit for bit), both equal to running the accepted tokens as
+    single-token decodes, bit for bit, and to the oracle. Accept lengths span
+    the groups; positions cross the 256 boundary inside later groups."""
+    H, B, S = 2, 5, 20
+    dims = W.LayerDims(num_heads=H, head_k=D, head_v=D)
+    cdt = torch.float32 if io == torch.float32 else torch.bfloat16
+    pa = L.StatePool(1, S, H, D, state_dtype=sdt, conv_dtype=cdt, device=DEV)
+    fill_pool(pa, 71, std=0.1)
+    pb = L.StatePool(1, S, H, D, state_dtype=sdt, conv_dtype=cdt, device=DEV,
+                     temporal=pa.temporal.clone(), conv=pa.conv.clone())
+    pc = L.StatePool(1, S, H, D, state_dtype=sdt, conv_dtype=cdt, device=DEV,
+                     temporal=pa.temporal.clone(), conv=pa.conv.clone())
+    op = oracle_pool(pa)
+    conv_w = W.randn((dims.conv_channels, 4), 71, "lc.w", std=0.5).to(io).to(DEV)
+    slots, track = [2, 5, 9, 13, 17], [3, 6, -1, 14, 18]
+    pos = [250, 256 - ND + 2, 100, 511 - ND // 2, 7]
+    acc = [ND, ND - 2, 5, 1, 0]
+    x, g, beta = (t.to(DEV) for t in W.make_decode_inputs(dims, B, ND, gate, io, 71, tag="lc"))
+    spec = L.SpecBuffer(pa, B, ND)
+    oa = torch.zeros((B, ND, H, D), device=DEV)
+    ob = torch.zeros((B, ND, H, D), device=DEV)
+    common = dict(layer=0, x=x, conv_w=conv_w, g=g, beta=beta, slot=_i32(slots), pos=_i32(pos),
+                  gate_mode=gate, flags=FLAGS)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.lin_state_decode(pa, out=oa, spec=spec, status=st, **common)
+    L.lin_state_decode(pb, out=ob, status=st, **common)
+    assert L.lin_state_read_status(st) == 0
+    assert torch.equal(oa, ob)
+    L.lin_state_spec_commit(pa, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
+                            n_draft=ND, track_slot=_i32(track), track_interval=256, status=st)
+    L.lin_state_replay_commit(pb, layer=0, x=x, conv_w=conv_w, g=g, beta=beta, slot=_i32(slots),
+                              pos=_i32(pos), accept_len=_i32(acc), track_slot=_i32(track),
+                              track_interval=256, gate_mode=gate, flags=FLAGS, status=st)
+    assert L.lin_state_read_status(st) == 0
+    assert torch.equal(pa.temporal, pb.temporal)
+    assert torch.equal(pa.conv, pb.conv)
+    # the linear chain: the accepted tokens as single-token decodes
+    for j in range(ND):
+        sl = [s if acc[r] > j else -1 for r, s in enumerate(slots)]
+        oc = torch.zeros((B, 1, H, D), device=DEV)
+        L.lin_state_decode(pc, layer=0, x=x[:, j:j + 1].contiguous(), conv_w=conv_w,
+                           g=g[:, j:j + 1].contiguous(), beta=beta[:, j:j + 1].contiguous(),
+                           out=oc, slot=_i32(sl), pos=_i32([p + j for p in pos]),
+                           track_slot=_i32(track), track_interval=256, gate_mode=gate,
+                           flags=FLAGS, status=st)
+        live = [r for r in range(B) if acc[r] > j]
+        assert torch.equal(oc[live, 0], oa[live, j])
+    assert L.lin_state_read_status(st) == 0
+    assert torch.equal(pa.temporal, pc.temporal)
+    assert torch.equal(pa.conv, pc.conv)
+    # the oracle's verify and commit
+    ospec = O.make_spec_buffer(1, B, ND, H, D, D, dims.conv_channels)
+    oo, ost = O.decode(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots, pos, None, 0,
+                       gate, FLAGS, 1.0, "f32", spec=ospec)
+    assert ost == 0
+    tol = TOL_F32 if sdt == torch.float32 else TOL_BF16
+    assert max_rel_per_head(np64(oa), oo, 2) < tol
+    sp = np64(spec.temporal)
+    for r in range(B):
+        for j in range(ND):
+            assert max_rel_per_head(sp[0, r, j], ospec["temporal"][0, r, j], 0) < tol
+    assert np.array_equal(np64(spec.conv), ospec["conv"])
+    O.spec_commit(op, ospec, 0, 1, slots, pos, acc, track, 256, ND)
+    t = np64(pa.temporal[0])
+    for s_ in range(S):
+        assert max_rel_per_head(t[s_], op["temporal"][0, s_], 0) < tol
+    assert np.array_equal(np64(pa.conv), op["conv"])
