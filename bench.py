@@ -219,17 +219,20 @@ class PrefillWorkload(Workload):
     # e2e: the public call with host inputs (pinned) and the outputs read back.
     # The batch is pipelined over streams: one copies inputs in, one per request
     # runs that request's calls as soon as their inputs have landed, one copies
-    # outputs out, so the host link (about 0.2 TB/s each way, 0.3 TB/s both ways
-    # together) stays busy while the GPU computes. Each request runs as
-    # E2E_PIECES calls over consecutive 64-aligned token ranges, each warm from
-    # the state the one before left in the slot (the pages' chunked prefill),
-    # with its track list rotated so every boundary lands where the one-call run
-    # puts it. The inputs of every request's first piece are copied first, so
-    # the last computation to wait on the link is a short one. Requests are
-    # independent and a state round-trips the pool exactly (fp32 state, bf16
-    # windows that are copies of bf16 inputs), so the outputs and slots equal
-    # the one-call run's bit for bit.
-    E2E_PIECES = 4
+    # outputs out, so the host link (about 0.2 TB/s each way, 0.34 TB/s both
+    # ways together with large copies) stays busy while the GPU computes. Each
+    # request runs as calls over consecutive 64-aligned token ranges cut at
+    # E2E_CUTS of its length, each warm from the state the one before left in
+    # the slot (the pages' chunked prefill), with its track list rotated so
+    # every boundary lands where the one-call run puts it. The small first
+    # pieces start the computation and the output copies early, the small last
+    # pieces keep the tail after the last input copy short; pieces go in order
+    # of their index, then request. The gates and betas of the whole step
+    # (8 MB) go in one copy ahead of the first piece: two small copies per piece
+    # cost the link more than their bytes. Requests are independent and a state
+    # round-trips the pool exactly (fp32 state, bf16 windows that are copies of
+    # bf16 inputs), so the outputs and slots equal the one-call run's bit for bit.
+    E2E_CUTS = (0.125, 0.5, 0.875)
 
     def setup_e2e(self):
         b, L, dev = self.b, self.L, self.dev
@@ -246,7 +249,7 @@ class PrefillWorkload(Workload):
         pieces = []  # (piece index, request, part)
         for r in range(self.B):
             Lr = cu[r + 1] - cu[r]
-            cuts = sorted({0, Lr} | {(Lr * k // self.E2E_PIECES) // 64 * 64 for k in range(1, self.E2E_PIECES)})
+            cuts = sorted({0, Lr} | {int(Lr * f) // 64 * 64 for f in self.E2E_CUTS})
             stream = torch.cuda.Stream()
             tr = tracks[cut[r]:cut[r + 1]]
             for k, (o0, o1) in enumerate(zip(cuts[:-1], cuts[1:])):
@@ -265,7 +268,7 @@ class PrefillWorkload(Workload):
                           track_slots=i32(rot) if rot else None,
                           cu_track=i32([0, len(rot)]) if rot else None)
                 pieces.append((k, r, dict(
-                    kw=kw, h_in=[h[t0:t1] for h in self.h_in], d_in=[d[t0:t1] for d in self.d_in],
+                    kw=kw, h_in=self.h_in[0][t0:t1], d_in=self.d_in[0][t0:t1],
                     h_out=self.h_out[t0:t1], d_out=self.out[t0:t1], stream=stream,
                     ev_c=None, ev_d=None)))
         pieces.sort(key=lambda e: (e[0], e[1]))
@@ -278,13 +281,15 @@ class PrefillWorkload(Workload):
         cur = torch.cuda.current_stream()
         start = cur.record_event()
         self.s_in.wait_event(start)
+        with torch.cuda.stream(self.s_in):  # the step's gates and betas
+            for h, d in zip(self.h_in[1:], self.d_in[1:]):
+                d.copy_(h, non_blocking=True)
         for pt in self.parts:
             # a piece's input buffers are free once its previous call has run
             if pt["ev_c"] is not None:
                 self.s_in.wait_event(pt["ev_c"])
             with torch.cuda.stream(self.s_in):
-                for h, d in zip(pt["h_in"], pt["d_in"]):
-                    d.copy_(h, non_blocking=True)
+                pt["d_in"].copy_(pt["h_in"], non_blocking=True)
                 ev_in = self.s_in.record_event()
             s = pt["stream"]
             s.wait_event(ev_in)
