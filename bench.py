@@ -321,11 +321,17 @@ class DecodeWorkload(Workload):
     step, interval 256 with per-request track slots; the pool is rotated over 4
     replicas so the per-step working set does not stay in L2."""
 
-    def __init__(self, L, dev, n_draft=1, replicas=4, seed=0, replay=False):
+    # the draft tree of the tree-verify workload: the MambaRadixCache page's
+    # shape (9.6), two roots and depth 4, for every request
+    TREE = [-1, -1, 0, 0, 1, 2, 2, 5]
+
+    def __init__(self, L, dev, n_draft=1, replicas=4, seed=0, replay=False, tree=False):
         self.L, self.dev = L, dev
         self.n_draft = n_draft
         self.replay = replay
+        self.tree = tree
         self.name = ("kda_decode" if n_draft == 1 else
+                     f"kda_tree_verify{n_draft}_commit" if tree else
                      f"kda_spec_verify{n_draft}_replay" if replay else f"kda_spec_verify{n_draft}_commit")
         self.unit = "req-steps/s" if n_draft == 1 else "verify-rounds/s"
         self.kernel = "decode"
@@ -359,6 +365,15 @@ class DecodeWorkload(Workload):
                 self.specs = [L.SpecBuffer(p, B, n_draft) for p in self.pools]
             self.acc = (W.randint(1, n_draft, (B,), seed, "kd.acc")).to(torch.int32).to(dev)
             self.launches_per_step = 2
+        if tree:
+            assert n_draft == len(self.TREE) and not replay
+            self.parent = torch.tensor([self.TREE] * B, dtype=torch.int32, device=dev)
+            node = W.randint(0, n_draft - 1, (B,), seed, "kd.node")
+            self.accept_node = node.to(torch.int32).to(dev)
+            depth = [0] * n_draft  # tokens on the path from a root to each node
+            for j, pj in enumerate(self.TREE):
+                depth[j] = 1 + (depth[pj] if pj >= 0 else 0)
+            acc_tokens_tree = float(sum(depth[int(k)] for k in node))
         st = W.state_bytes(dims, 2, 2)
         x_b = dims.conv_channels * 2 + 12 * 128 * 4 + 12 * 4 + 12 * 128 * 2
         if n_draft == 1:
@@ -379,6 +394,10 @@ class DecodeWorkload(Workload):
             self.units = 1
             self.acc_tokens = B * acc_mean
         else:
+            # chain or tree: the slot state read once, every draft's state
+            # written, inputs and outputs; a tree node reads its parent's state
+            # back from the per-step buffer (written just before, in L2), which
+            # is not counted
             D = n_draft
             acc_mean = (n_draft + 1) / 2.0
             verify = B * (st + D * st + D * x_b)
@@ -386,7 +405,7 @@ class DecodeWorkload(Workload):
             self.bytes = verify + commit
             self.verify_bytes = verify
             self.units = 1
-            self.acc_tokens = B * acc_mean
+            self.acc_tokens = acc_tokens_tree if tree else B * acc_mean
         self.steps_done = 0
 
     def units_per_step(self):
@@ -422,6 +441,16 @@ class DecodeWorkload(Workload):
                                       track_slot=self.track, track_interval=256,
                                       gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
             return
+        elif self.tree:
+            self._k_begin()
+            L.lin_state_decode(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta, out=self.out,
+                               slot=self.slot, pos=pos, spec=self.specs[r], parent=self.parent,
+                               gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
+            self._k_end()
+            L.lin_state_spec_commit(p, spec=self.specs[r], slot=self.slot, pos=pos,
+                                    n_draft=self.n_draft, track_slot=self.track, track_interval=256,
+                                    parent=self.parent, accept_node=self.accept_node,
+                                    status=self.status)
         else:
             self._k_begin()
             L.lin_state_decode(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta, out=self.out,
@@ -433,8 +462,11 @@ class DecodeWorkload(Workload):
                                     track_slot=self.track, track_interval=256, status=self.status)
 
     def describe(self):
-        return {"batch": self.B, "n_draft": self.n_draft, "pool_slots": 2000,
-                "replicas": len(self.pools)}
+        d = {"batch": self.B, "n_draft": self.n_draft, "pool_slots": 2000,
+             "replicas": len(self.pools)}
+        if self.tree:
+            d["parent"] = self.TREE
+        return d
 
 
 class CopyWorkload(Workload):
@@ -505,6 +537,8 @@ def make_workload(name, L, dev):
         return DecodeWorkload(L, dev, 4)
     if name == "kda_spec_verify4_replay":
         return DecodeWorkload(L, dev, 4, replay=True)
+    if name == "kda_tree_verify8_commit":
+        return DecodeWorkload(L, dev, 8, tree=True)
     if name == "slot_copy_kimi_k3_69l":
         return CopyWorkload(L, dev)
     if name == "slot_copy_kimi_k3_8l":
@@ -516,7 +550,7 @@ def make_workload(name, L, dev):
 
 HEADLINE = "qwen35_gdn_prefill"
 DEFAULT_EXTRA = ["kimi_k3_kda_varlen_prefill", "kda_decode", "kda_spec_verify4_commit",
-                 "kda_spec_verify4_replay",
+                 "kda_spec_verify4_replay", "kda_tree_verify8_commit",
                  "slot_copy_kimi_k3_69l", "kda_long_prefill_131k", "mamba2_ssd_prefill"]
 
 CONFIG_TEXT = {
@@ -531,6 +565,9 @@ CONFIG_TEXT = {
                   "1 token per step, track interval 256, 4 pool replicas",
     "kda_spec_verify4_commit": "KDA speculative verify of 4 drafts + commit of U{1..4} accepted, "
                                "256 requests, per-step states in a spec buffer",
+    "kda_tree_verify8_commit": "KDA draft-tree verify of 8 drafts (two roots, depth 4: parents "
+                               "-1,-1,0,0,1,2,2,5) into a spec buffer + commit of a random accepted "
+                               "node, 256 requests",
     "kda_spec_verify4_replay": "KDA speculative verify of 4 drafts (outputs only) + replay commit of "
                                "U{1..4} accepted tokens into the slot, 256 requests, no per-step buffer",
     "slot_copy_kimi_k3_8l": "checkpoint fork/restore copy: Kimi-K3 slot over 8 layers (3,366,912 B), 64 "

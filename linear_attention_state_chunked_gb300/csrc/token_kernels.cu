@@ -322,10 +322,10 @@ __device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
 // kDecReplay (the commit form: accepted tokens per request, in place, no
 // outputs), kDecTree (verify into the spec buffer where draft j starts from
 // the state after draft parent[r][j], -1: the slot's).
-// The three chain modes run the drafts in groups (see the consumer loop).
+// All but the one-token mode run the drafts in groups (see the consumer loop).
 enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2, kDecTree = 3, kDecVerify = 4 };
 constexpr int kDecMaxTree = 32;  // drafts per request in a tree verify
-constexpr int kDecGroup = 4;     // drafts per group in the chain modes
+constexpr int kDecGroup = 4;     // drafts per group in the draft modes
 // Dynamic shared memory of one decode CTA: at most the opt-in limit (227 KB)
 // less 1 KB for the static part; at most kDecPairSmem where two CTAs share an
 // SM (228 KB per SM, 1 KB of it reserved per CTA).
@@ -342,10 +342,10 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
     decode_kernel(DecodeParams p, int n_items, int stage_bytes, int stages, int group) {
   using C = DecPCfg<D, V>;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
-  constexpr bool BATCH = MODE == kDecVerify || MODE == kDecOutputsOnly || MODE == kDecReplay;
+  constexpr bool BATCH = MODE != kDecStates;  // the draft modes: chains and trees
   extern __shared__ __align__(128) uint8_t dsm[];
-  // per-token scratch of the one-token and tree modes (the chain modes keep
-  // theirs in the group buffers after the stages)
+  // per-token scratch of the one-token mode (the draft modes keep theirs in
+  // the group buffers after the stages)
   __shared__ __align__(16) float ysm[BATCH ? 1 : 2][BATCH ? 4 : C::CH];  // post-conv q | k | v, by token parity
   __shared__ __align__(16) float agsm[BATCH ? 1 : 2][BATCH ? 4 : D];     // per-key decay factors
   __shared__ float normsm[BATCH ? 1 : 2][D < 32 ? 1 : D / 32][3];        // q.q, k.k, q.k partials per conv warp
@@ -533,10 +533,11 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
     char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
                    int64_t(m.slot) * pool.conv_slot_stride;
     if constexpr (BATCH) {
-      // A chain of drafts, in groups of `group`: the conv, gate factors and
-      // norm partials of every draft of the group first (none of them depends
-      // on the state), one barrier, then the group's row updates back to
-      // back. Group buffers alternate, so a warp starts the next group's conv
+      // Drafts in groups of `group`: the conv, gate factors and norm partials
+      // of every draft of the group first (none of them depends on the state:
+      // a chain carries each window to the next draft, a tree node builds its
+      // window from its ancestors' inputs), one barrier, then the group's row
+      // updates back to back. Group buffers alternate, so a warp starts the next group's conv
       // while others still read the previous group. Every item runs the same
       // number of groups (with no work when it is empty), so all consumers
       // meet the same barriers whatever they saw. The arithmetic is the
@@ -562,10 +563,17 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           for (int jj = 0; jj < nl; ++jj) {
             const int j = j0 + jj;
             const uint8_t* sx = buf + L.x + j * C::CH * esi;
+            // tree: ancestors of node j (parent first; -1 past a root)
+            int a1 = -1, a2 = -1, a3 = -1;
+            if (MODE == kDecTree) {
+              a1 = par_sm[s][j];
+              a2 = a1 >= 0 ? par_sm[s][a1] : -1;
+              a3 = a2 >= 0 ? par_sm[s][a2] : -1;
+            }
             // where the window after draft j goes (besides the next draft)
             char* dc = nullptr;
             char* tcv = nullptr;
-            if (MODE == kDecVerify) {
+            if (MODE == kDecVerify || MODE == kDecTree) {
               dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
                    m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
             } else if (REPLAY) {
@@ -578,6 +586,19 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
             for (int pt = 0; pt < 3; ++pt) {
               if (V < D && pt == 2 && t >= V) break;
               const int cl = pt * D + t;
+              if (MODE == kDecTree) {
+                // the window before node j: the inputs of its last three
+                // ancestors, topped up from the slot's window (oldest first)
+                auto xr = [&](int n) {
+                  return round_to_dtype(load_elem(buf + L.x + n * C::CH * esi, cl, a.io_dtype), pool.conv_dtype);
+                };
+                const float s0 = load_elem(buf + L.conv, cl * 3, pool.conv_dtype);
+                const float s1 = load_elem(buf + L.conv, cl * 3 + 1, pool.conv_dtype);
+                const float s2 = load_elem(buf + L.conv, cl * 3 + 2, pool.conv_dtype);
+                win[pt][2] = a1 >= 0 ? xr(a1) : s2;
+                win[pt][1] = a2 >= 0 ? xr(a2) : (a1 >= 0 ? s2 : s1);
+                win[pt][0] = a3 >= 0 ? xr(a3) : (a2 >= 0 ? s2 : (a1 >= 0 ? s1 : s0));
+              }
               const float xin = load_elem(sx, cl, a.io_dtype);
               const float y = w[pt][0] * win[pt][0] + w[pt][1] * win[pt][1] + w[pt][2] * win[pt][2] +
                               w[pt][3] * xin;
@@ -595,7 +616,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
               gys[jj * C::CH + cl] = silu_on ? silu(y) : y;
             }
           }
-          if (j0 + gn < ND) {  // the next group starts from this window
+          if (MODE != kDecTree && j0 + gn < ND) {  // the next group starts from this window
 #pragma unroll
             for (int pt = 0; pt < 3; ++pt) {
               if (V < D && pt == 2 && t >= V) break;
@@ -643,7 +664,19 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           const float beta = bgs[2 * j];
           char* dt = nullptr;
           char* tt = nullptr;
-          if (MODE == kDecVerify) {
+          // a tree node whose parent is not the previous node starts from the
+          // parent's state in the spec buffer (the slot's for a root); each
+          // thread reads back only the rows it wrote itself
+          const char* src_t = nullptr;
+          if (MODE == kDecTree && j > 0) {
+            const int pj = par_sm[s][j];
+            if (pj != j - 1)
+              src_t = pj < 0 ? slot_t
+                             : static_cast<const char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
+                                   m.r * a.spec.temporal_req_stride + pj * a.spec.temporal_step_stride +
+                                   m.h * head_bytes;
+          }
+          if (MODE == kDecVerify || MODE == kDecTree) {
             dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
                  m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
           } else if (REPLAY) {
@@ -697,7 +730,10 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
 #pragma unroll
             for (int i = 0; i < C::RB; ++i) {
               const int64_t roff = (int64_t(row0 + (rb + i) * C::RSTEP) * D + lr * 8) * ES;
-              Pair8<ST>::load(sst + roff, sv[i]);
+              if (MODE == kDecTree && src_t)
+                Pair8<ST>::load(src_t + roff, sv[i]);
+              else
+                Pair8<ST>::load(sst + roff, sv[i]);
               uint64_t dk2 = 0ull, dq2 = 0ull;
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
@@ -757,28 +793,13 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
         }
       }
     } else {
-    // every item runs ND token steps (with no work when it is empty), so all
-    // consumers meet the same number of barriers whatever they saw
-    for (int j = 0; j < ND; ++j, ++tc) {
+    // one token in place (n_draft == 1): every item runs the token step (with
+    // no work when it is empty), so all consumers meet the same barriers
+    // whatever they saw
+    for (int j = 0; j < 1; ++j, ++tc) {
       float* ys = ysm[tc & 1];
-      const int64_t tok = int64_t(m.r) * ND + j;
-      const bool live = REPLAY ? (m.valid && j < m.acc) : static_cast<bool>(m.valid);
-      // a tree draft whose parent is not the previous draft starts from the
-      // parent's stored state and window (the slot's for a root); each thread
-      // reads back only the rows and channels it wrote itself
-      const char* src_t = nullptr;
-      const char* src_c = nullptr;
-      if (MODE == kDecTree && live && j > 0) {
-        const int pj = par_sm[s][j];
-        if (pj != j - 1) {
-          src_t = pj < 0 ? slot_t
-                         : static_cast<const char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
-                               m.r * a.spec.temporal_req_stride + pj * a.spec.temporal_step_stride + m.h * head_bytes;
-          src_c = pj < 0 ? slot_c
-                         : static_cast<const char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
-                               m.r * a.spec.conv_req_stride + pj * a.spec.conv_step_stride;
-        }
-      }
+      const int64_t tok = m.r;
+      const bool live = m.valid;
       float beta = 0.f, gh = 0.f;
       char* dt = nullptr;
       char* dc = nullptr;
@@ -789,34 +810,15 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
         const float* bgs = reinterpret_cast<const float*>(buf + L.bg);
         beta = bgs[2 * j];
         if (!per_key) gh = bgs[2 * j + 1];
-        if (REPLAY) {
-          // in place: the slot after the last accepted token, the track slot
-          // at a boundary crossed on the way
-          if (j == m.acc - 1) {
-            dt = slot_t;
-            dc = slot_c;
-          }
-          if (m.ts >= 0 && a.track_interval > 0 && (m.pos + j + 1) % a.track_interval == 0) {
-            tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
-                 int64_t(m.ts) * pool.temporal_slot_stride + m.h * head_bytes;
-            tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
-                  int64_t(m.ts) * pool.conv_slot_stride;
-          }
-        } else if (ND == 1) {
-          dt = slot_t;
-          dc = slot_c;
-          if (m.ts >= 0 && a.track_interval > 0 && (m.pos + 1) % a.track_interval == 0) {
-            tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
-                 int64_t(m.ts) * pool.temporal_slot_stride + m.h * head_bytes;
-            tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
-                  int64_t(m.ts) * pool.conv_slot_stride;
-          }
-        } else if (MODE == kDecStates || MODE == kDecTree) {
-          dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
-               m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
-          dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
-               m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
-        }  // kDecOutputsOnly: a verify that keeps no per-step states
+        // in place, and into the track slot when the token ends an interval
+        dt = slot_t;
+        dc = slot_c;
+        if (m.ts >= 0 && a.track_interval > 0 && (m.pos + 1) % a.track_interval == 0) {
+          tt = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+               int64_t(m.ts) * pool.temporal_slot_stride + m.h * head_bytes;
+          tcv = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                int64_t(m.ts) * pool.conv_slot_stride;
+        }
         if (t < D) {
           const uint8_t* sx = buf + L.x + j * C::CH * esi;
           float y3[3];
@@ -826,9 +828,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
             const int cl = pt * D + t;
             float win[3], w[4];
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-              win[q] = (MODE == kDecTree && src_c) ? load_elem(src_c, gchan(pt, m.h, t) * 3 + q, pool.conv_dtype)
-                                                   : load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
+            for (int q = 0; q < 3; ++q) win[q] = load_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype);
 #pragma unroll
             for (int q = 0; q < 4; ++q) w[q] = load_elem(buf + L.w, cl * 4 + q, a.io_dtype);
             const float xin = load_elem(sx, cl, a.io_dtype);
@@ -837,9 +837,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
             const int64_t ch = gchan(pt, m.h, t);
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
-              if (ND > 1) store_elem(buf + L.conv, cl * 3 + q, pool.conv_dtype, nw[q]);  // next draft's window
-              if (MODE == kDecStates || MODE == kDecTree || (MODE == kDecReplay && dc))
-                store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
+              store_elem(dc, ch * 3 + q, pool.conv_dtype, nw[q]);
               if (tcv) store_elem(tcv, ch * 3 + q, pool.conv_dtype, nw[q]);
             }
             y3[pt] = silu_on ? silu(y) : y;
@@ -919,10 +917,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
         for (int i = 0; i < C::RB; ++i) {
           const int row = row0 + (rb + i) * C::RSTEP;
           const int64_t roff = (int64_t(row) * D + lr * 8) * ES;
-          if (MODE == kDecTree && src_t)
-            Pair8<ST>::load(src_t + roff, sv[i]);
-          else
-            Pair8<ST>::load(sst + roff, sv[i]);
+          Pair8<ST>::load(sst + roff, sv[i]);
           uint64_t dk2 = 0ull, dq2 = 0ull;
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
@@ -958,7 +953,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           const float dk = __shfl_sync(0xffffffffu, red[0], gbase + (2 * i) * VSTEP);
           u[i] = beta * fmaf(-dmul, dk, ys[2 * D + row0 + (rb + i) * C::RSTEP]);
         }
-        if (!REPLAY && (my_v & 1) && (lr % VSTEP) == 0) {
+        if ((my_v & 1) && (lr % VSTEP) == 0) {
           float ui = 0.f;
 #pragma unroll
           for (int i = 0; i < C::RB; ++i)
@@ -972,16 +967,12 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           const uint64_t u2 = f2pack(u[i], u[i]);
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) sv[i][e2] = ffma2(u2, k2[e2], sv[i][e2]);
-          if (MODE == kDecStates || MODE == kDecTree || (MODE == kDecReplay && dt)) Pair8<ST>::store(dt + off, sv[i]);
+          Pair8<ST>::store(dt + off, sv[i]);
           if (tt) Pair8<ST>::store(tt + off, sv[i]);
-          if (ND > 1) {
-            Pair8<ST>::round(sv[i]);  // the next draft starts from the stored state
-            Pair8<ST>::store(sst + off, sv[i]);
-          }
         }
       }
     }
-    }  // one-token and tree modes
+    }  // one-token mode
     if (abort) break;
     // this warp's reads (and, in verify, writes) of the stage are done
     __syncwarp();
@@ -1131,8 +1122,8 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   if (stages < 2) stages = 2;
   int smem = stages * stage;
   int group = 1;
-  if (mode == kDecVerify || mode == kDecOutputsOnly || mode == kDecReplay) {
-    // the chain modes' two group buffers follow the stages: the largest group
+  if (mode != kDecStates) {
+    // the draft modes' two group buffers follow the stages: the largest group
     // (up to kDecGroup drafts) that keeps two CTAs per SM where the stages
     // alone would, else that fits one CTA
     const int budget = 2 * stage <= 100 * 1024 ? kDecPairSmem : kDecMaxDynSmem;

@@ -239,6 +239,57 @@ def test_kda_verify4_commit_full_size_sampled():
             assert np.array_equal(np64(wl.pools[0].conv[0, s_])[ch], pool["conv"][0, s_])
 
 
+def test_kda_tree_verify8_commit_full_size_sampled():
+    """The draft-tree verify + commit workload (2000-slot pools, 256 requests,
+    8 drafts in the MambaRadixCache page's tree shape, a random accepted node
+    per request): one step as bench.py runs it, then two requests x two heads
+    of replica 0 against the oracle: outputs, every node's state and window in
+    the spec buffer, and the committed slot and track slot."""
+    wl = bench.make_workload("kda_tree_verify8_commit", L, DEV)
+    rep0_t = wl.pools[0].temporal.clone().cpu()
+    rep0_c = wl.pools[0].conv.clone().cpu()
+    wl.step(0)
+    torch.cuda.synchronize()
+    assert L.lin_state_read_status(wl.status) == 0
+    heads = [4, 11]
+    ch = head_channels(12, 128, heads)
+    x, g, beta = wl.inputs[0]
+    node = wl.accept_node.cpu().tolist()
+    spec = wl.specs[0]
+    ND = len(wl.TREE)
+    for req in [7, 131]:
+        slot = int(wl.slot[req])
+        ts = int(wl.track[req])
+        pos = int(wl.pos0[req])
+        pool = {"temporal": np.zeros((1, 2000, 2, 128, 128)), "conv": np.zeros((1, 2000, len(ch), 3)),
+                "state_dtype": "bf16", "conv_dtype": "bf16"}
+        pool["temporal"][0, slot] = np64(rep0_t[0, slot][heads])
+        pool["conv"][0, slot] = np64(rep0_c[0, slot][ch])
+        pool["temporal"][0, ts] = np64(rep0_t[0, ts][heads])
+        pool["conv"][0, ts] = np64(rep0_c[0, ts][ch])
+        ospec = O.make_spec_buffer(1, 1, ND, 2, 128, 128, len(ch))
+        o, st = O.decode(pool, 0, np64(x[req:req + 1])[:, :, ch], np64(wl.conv_w)[ch],
+                         np64(g[req:req + 1])[:, :, heads], np64(beta[req:req + 1])[:, :, heads],
+                         [slot], [pos], None, 0, O.GATE_PER_KEY, FLAGS, 1.0, "bf16", spec=ospec,
+                         parent=[wl.TREE])
+        assert st == 0
+        got = np64(wl.out[req][:, heads])
+        for k in range(2):
+            assert rel_l2(got[:, k], o[0, :, k]) <= TOL_BF16
+        for j in range(ND):
+            gs = np64(spec.temporal[0, req, j][heads])
+            for k in range(2):
+                assert rel_l2(gs[k], ospec["temporal"][0, 0, j, k]) <= TOL_BF16
+            assert np.array_equal(np64(spec.conv[0, req, j])[ch], ospec["conv"][0, 0, j])
+        O.spec_commit(pool, ospec, 0, 1, [slot], [pos], None, [ts], 256, ND, parent=[wl.TREE],
+                      accept_node=[node[req]])
+        for s_ in (slot, ts):
+            gt = np64(wl.pools[0].temporal[0, s_][heads])
+            for k in range(2):
+                assert rel_l2(gt[k], pool["temporal"][0, s_, k]) <= TOL_BF16
+            assert np.array_equal(np64(wl.pools[0].conv[0, s_])[ch], pool["conv"][0, s_])
+
+
 def test_headline_e2e_pipeline_equals_one_call():
     """bench.py's end-to-end leg runs each request of the headline batch as
     consecutive warm-started calls on its own stream, with host copies in and
