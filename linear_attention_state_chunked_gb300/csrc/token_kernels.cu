@@ -352,6 +352,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
   __shared__ uint64_t full[kDecMaxStages], empty[kDecMaxStages];
   __shared__ DecMeta meta[kDecMaxStages];
   __shared__ int8_t par_sm[MODE == kDecTree ? kDecMaxStages : 1][MODE == kDecTree ? kDecMaxTree : 1];
+  __shared__ int8_t ord_sm[MODE == kDecTree ? kDecMaxStages : 1][MODE == kDecTree ? kDecMaxTree : 1];
   const lin_state_pool_t& pool = p.pool;
   const lin_decode_args_t& a = p.a;
   const int H = pool.num_heads;
@@ -438,6 +439,31 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
             meta[s] = mj;
             if (MODE == kDecTree && mj.valid)
               for (int t = 0; t < ND; ++t) par_sm[s][t] = static_cast<int8_t>(a.parent[int64_t(mj.r) * ND + t]);
+            if (MODE == kDecTree && mj.valid) {
+              // the order the nodes run in: depth-first preorder, each node
+              // followed by its lowest-index unvisited child, so that as many
+              // nodes as possible start from the state of the node run just
+              // before them (parents always run before their children)
+              uint32_t seen = 0u;
+              int cnt = 0, cur = -1;
+              for (int it = 0; it < 4 * kDecMaxTree * kDecMaxTree && cnt < ND; ++it) {
+                int c = -1;
+                for (int k = 0; k < ND; ++k)
+                  if (!((seen >> k) & 1u) && par_sm[s][k] == cur) {
+                    c = k;
+                    break;
+                  }
+                if (c >= 0) {
+                  ord_sm[s][cnt++] = static_cast<int8_t>(c);
+                  seen |= 1u << c;
+                  cur = c;
+                } else {
+                  cur = cur >= 0 ? par_sm[s][cur] : -1;  // back to the parent
+                }
+              }
+              if (cnt < ND)  // not reached for a valid tree; index order is also valid
+                for (int t = 0; t < ND; ++t) ord_sm[s][t] = static_cast<int8_t>(t);
+            }
             if (mj.valid) {
               const uint32_t sf = full_bar(s);
               const uint32_t s0 = s_base + s * stage_bytes;
@@ -562,11 +588,12 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           }
           for (int jj = 0; jj < nl; ++jj) {
             const int j = j0 + jj;
-            const uint8_t* sx = buf + L.x + j * C::CH * esi;
-            // tree: ancestors of node j (parent first; -1 past a root)
+            const int nd = MODE == kDecTree ? ord_sm[s][j] : j;  // the draft run at position j
+            const uint8_t* sx = buf + L.x + nd * C::CH * esi;
+            // tree: ancestors of node nd (parent first; -1 past a root)
             int a1 = -1, a2 = -1, a3 = -1;
             if (MODE == kDecTree) {
-              a1 = par_sm[s][j];
+              a1 = par_sm[s][nd];
               a2 = a1 >= 0 ? par_sm[s][a1] : -1;
               a3 = a2 >= 0 ? par_sm[s][a2] : -1;
             }
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
             char* tcv = nullptr;
             if (MODE == kDecVerify || MODE == kDecTree) {
               dc = static_cast<char*>(a.spec.conv) + a.layer * a.spec.conv_layer_stride +
-                   m.r * a.spec.conv_req_stride + j * a.spec.conv_step_stride;
+                   m.r * a.spec.conv_req_stride + nd * a.spec.conv_step_stride;
             } else if (REPLAY) {
               if (j == m.acc - 1) dc = slot_c;
               if (m.ts >= 0 && a.track_interval > 0 && (m.pos + j + 1) % a.track_interval == 0)
@@ -627,7 +654,10 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           }
         } else if (per_key && t >= D && t < 2 * D) {
           const float* sg = reinterpret_cast<const float*>(buf + L.g);
-          for (int jj = 0; jj < nl; ++jj) gag[jj * D + (t - D)] = expf(sg[(j0 + jj) * D + (t - D)]);
+          for (int jj = 0; jj < nl; ++jj) {
+            const int nd = MODE == kDecTree ? ord_sm[s][j0 + jj] : j0 + jj;
+            gag[jj * D + (t - D)] = expf(sg[nd * D + (t - D)]);
+          }
         }
         if (warp < NPW) {
           // this warp's partial q.q, k.k, q.k of each draft (its own conv outputs)
@@ -659,18 +689,19 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
         uint8_t* sst = buf + L.state;
         for (int jj = 0; jj < nl; ++jj) {
           const int j = j0 + jj;
-          const int64_t tok = int64_t(m.r) * ND + j;
+          const int nd = MODE == kDecTree ? ord_sm[s][j] : j;  // the draft run at position j
+          const int64_t tok = int64_t(m.r) * ND + nd;
           const float* ys = gys + jj * C::CH;
-          const float beta = bgs[2 * j];
+          const float beta = bgs[2 * nd];
           char* dt = nullptr;
           char* tt = nullptr;
-          // a tree node whose parent is not the previous node starts from the
-          // parent's state in the spec buffer (the slot's for a root); each
-          // thread reads back only the rows it wrote itself
+          // a tree node whose parent is not the node run before it starts from
+          // the parent's state in the spec buffer (the slot's for a root);
+          // each thread reads back only the rows it wrote itself
           const char* src_t = nullptr;
           if (MODE == kDecTree && j > 0) {
-            const int pj = par_sm[s][j];
-            if (pj != j - 1)
+            const int pj = par_sm[s][nd];
+            if (pj != ord_sm[s][j - 1])
               src_t = pj < 0 ? slot_t
                              : static_cast<const char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
                                    m.r * a.spec.temporal_req_stride + pj * a.spec.temporal_step_stride +
@@ -678,7 +709,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
           }
           if (MODE == kDecVerify || MODE == kDecTree) {
             dt = static_cast<char*>(a.spec.temporal) + a.layer * a.spec.temporal_layer_stride +
-                 m.r * a.spec.temporal_req_stride + j * a.spec.temporal_step_stride + m.h * head_bytes;
+                 m.r * a.spec.temporal_req_stride + nd * a.spec.temporal_step_stride + m.h * head_bytes;
           } else if (REPLAY) {
             if (j == m.acc - 1) dt = slot_t;
             if (m.ts >= 0 && a.track_interval > 0 && (m.pos + j + 1) % a.track_interval == 0)
@@ -718,7 +749,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
                 a2[2 * h2 + 1] = f2pack(fa.z, fa.w);
               }
             } else {
-              const float av = expf(bgs[2 * j + 1]);
+              const float av = expf(bgs[2 * nd + 1]);
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) a2[e2] = f2pack(av, av);
             }
