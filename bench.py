@@ -246,33 +246,20 @@ class PrefillWorkload(Workload):
         self.d_in = [b.x, b.g, b.beta]
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
         i32 = lambda v: torch.tensor(v, dtype=torch.int32, device=dev)
-        pieces = []  # (piece index, request, part)
-        for r in range(self.B):
-            Lr = cu[r + 1] - cu[r]
-            cuts = sorted({0, Lr} | {int(Lr * f) // 64 * 64 for f in self.E2E_CUTS})
-            stream = torch.cuda.Stream()
-            tr = tracks[cut[r]:cut[r + 1]]
-            for k, (o0, o1) in enumerate(zip(cuts[:-1], cuts[1:])):
-                if o1 <= o0:
-                    continue
-                t0, t1 = cu[r] + o0, cu[r] + o1
-                # boundaries before this piece, counted within the whole call
-                j0 = ((pre[r] + o0) // stride - pre[r] // stride) if stride else 0
-                rot = [tr[(j0 + q) % len(tr)] for q in range(len(tr))] if tr else []
-                kw = dict(self.kw)
-                kw.update(x=b.x[t0:t1], g=b.g[t0:t1], beta=b.beta[t0:t1], out=self.out[t0:t1],
-                          cu_seqlens=i32([0, o1 - o0]), prefix_len=i32([pre[r] + o0]),
-                          slot=self.slot[r:r + 1].contiguous(),
-                          has_initial_state=torch.tensor([warm[r] if o0 == 0 else 1],
-                                                         dtype=torch.int64, device=dev),
-                          track_slots=i32(rot) if rot else None,
-                          cu_track=i32([0, len(rot)]) if rot else None)
-                pieces.append((k, r, dict(
-                    kw=kw, h_in=self.h_in[0][t0:t1], d_in=self.d_in[0][t0:t1],
-                    h_out=self.h_out[t0:t1], d_out=self.out[t0:t1], stream=stream,
-                    ev_c=None, ev_d=None)))
-        pieces.sort(key=lambda e: (e[0], e[1]))
-        self.parts = [pt for _, _, pt in pieces]
+        streams = [torch.cuda.Stream() for _ in range(self.B)]
+        self.parts = []
+        for pc in plan_e2e_pieces(cu, pre, warm, tracks, cut, stride, self.E2E_CUTS):
+            r, t0, t1, rot = pc["request"], pc["t0"], pc["t1"], pc["tracks"]
+            kw = dict(self.kw)
+            kw.update(x=b.x[t0:t1], g=b.g[t0:t1], beta=b.beta[t0:t1], out=self.out[t0:t1],
+                      cu_seqlens=i32([0, t1 - t0]), prefix_len=i32([pc["prefix"]]),
+                      slot=self.slot[r:r + 1].contiguous(),
+                      has_initial_state=torch.tensor([pc["warm"]], dtype=torch.int64, device=dev),
+                      track_slots=i32(rot) if rot else None,
+                      cu_track=i32([0, len(rot)]) if rot else None)
+            self.parts.append(dict(kw=kw, h_in=self.h_in[0][t0:t1], d_in=self.d_in[0][t0:t1],
+                                   h_out=self.h_out[t0:t1], d_out=self.out[t0:t1],
+                                   stream=streams[r], ev_c=None, ev_d=None))
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
         return (sum(t.numel() * t.element_size() for t in self.h_in),
                 self.out.numel() * self.out.element_size())
@@ -313,6 +300,36 @@ class PrefillWorkload(Workload):
     def describe(self):
         return {"batch": self.B, "tokens": self.tokens, "snapshots": self.n_snap,
                 "kernel": self.kernel}
+
+
+def plan_e2e_pieces(cu_seqlens, prefix_len, has_initial_state, track_slots, cu_track,
+                    track_stride, cut_fractions):
+    """The calls of the end-to-end leg. Request r's tokens [cu[r], cu[r+1]) are
+    cut at the 64-aligned fractions `cut_fractions` of its length into
+    consecutive calls; a call starts from the request's own initial state if
+    it is the first, else warm from the state the call before left in the
+    slot (its prefix then covers the tokens before it). Each call's track list
+    is request r's list rotated by the boundaries that lie before the call, so
+    boundary j of the request lands in list[j mod n] as in the one-call run.
+    Returns dicts (index, request, t0, t1, prefix, warm, tracks), ordered by
+    index within the request, then request."""
+    pieces = []
+    for r in range(len(cu_seqlens) - 1):
+        n = cu_seqlens[r + 1] - cu_seqlens[r]
+        cuts = sorted({0, n} | {int(n * f) // 64 * 64 for f in cut_fractions})
+        tr = list(track_slots[cu_track[r]:cu_track[r + 1]]) if cu_track is not None else []
+        p0 = prefix_len[r]
+        for k, (o0, o1) in enumerate(zip(cuts[:-1], cuts[1:])):
+            if o1 <= o0:
+                continue
+            # boundaries before this call, counted within the whole request
+            j0 = ((p0 + o0) // track_stride - p0 // track_stride) if track_stride else 0
+            rot = [tr[(j0 + q) % len(tr)] for q in range(len(tr))] if tr else []
+            pieces.append({"index": k, "request": r, "t0": cu_seqlens[r] + o0,
+                           "t1": cu_seqlens[r] + o1, "prefix": p0 + o0,
+                           "warm": has_initial_state[r] if o0 == 0 else 1, "tracks": rot})
+    pieces.sort(key=lambda e: (e["index"], e["request"]))
+    return pieces
 
 
 class DecodeWorkload(Workload):
