@@ -6,8 +6,6 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from oracle import lin_state_oracle as O
-
 DT_NAME = {torch.float32: "f32", torch.bfloat16: "bf16"}
 
 # Parity bars: rel-L2 per (request, head) tensor.

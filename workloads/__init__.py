@@ -19,8 +19,7 @@ from __future__ import annotations
 
 import dataclasses
 import hashlib
-import math
-from typing import Dict, List, Optional
+from typing import List, Optional
 
 import torch
 
