@@ -693,17 +693,44 @@ def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=Fals
 ROOT = os.path.dirname(os.path.abspath(__file__))
 
 
+def _code_only(src):
+    """C / C++ / CUDA source without its comments and with each line's
+    whitespace collapsed (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    lines = (" ".join(line.split()) for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def library_source_hash():
-    """Digest of the CUDA library sources (csrc and the C header): a traffic
-    figure is reported only while the kernels it was measured on are unchanged."""
+    """Digest of the CUDA library sources (csrc and the C header), comments and
+    whitespace left out: a traffic figure is reported only while the code of
+    the kernels it was measured on is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_state_chunked_gb300", "csrc")
     files = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh", ".h"))]
     files.append(os.path.join(ROOT, "include", "lin_state.h"))
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

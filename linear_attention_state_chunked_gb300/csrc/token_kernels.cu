@@ -255,8 +255,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // up to `stages` items ahead. The NC consumer threads (8 warps at head 128)
 // wait for a stage warp by warp, so a warp that is done with one item starts
 // the conv of the next while others still update rows; the only CTA-wide
-// barrier is the one per token that publishes the conv outputs. Each warp
-// hands the stage back as soon as its own reads of it are done.
+// barrier is the one that publishes the conv outputs (per token in one-token
+// decode, per group of drafts in the draft modes). Each warp hands the stage
+// back as soon as its own reads of it are done.
 //
 // Row arithmetic: with A = Diag(alpha), the output needs no second pass over
 // the updated row, since  o_r = sum_c S'[r,c] q_c = (S A q)_r + u_r (k . q):
