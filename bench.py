@@ -137,6 +137,21 @@ class Workload:
             self.kern_events[-1][1] = e
 
 
+def prefill_algo_bytes(dims, lengths, prefixes, warm, gate_mode, es_io, es_out, es_state,
+                       track_stride):
+    """Algorithmic bytes of one prefill launch and its snapshot count: per
+    token x, g, beta in and the output out; one state block (state and conv
+    window) per snapshot, per final write-back and per warm start; the conv
+    taps once. The conv window is stored in the input dtype."""
+    H, K, V, C = dims.num_heads, dims.head_k, dims.head_v, dims.conv_channels
+    per_tok = C * es_io + (H * K if gate_mode == W.GATE_PER_KEY else H) * 4 + H * 4 + H * V * es_out
+    state_b = H * V * K * es_state + C * 3 * es_io
+    n_snap = sum(((p + l) // track_stride - p // track_stride) for p, l in zip(prefixes, lengths))
+    n_init = sum(1 for w in warm if w)
+    T = sum(lengths)
+    return T * per_tok + (n_snap + len(lengths) + n_init) * state_b + C * 4 * es_io, n_snap
+
+
 class PrefillWorkload(Workload):
     def __init__(self, L, dev, name, dims, lengths, prefixes, warm, gate_mode, io_dtype,
                  out_dtype, state_dtype, track_stride, tracks_per_req, gate, seed=0, flags=None):
@@ -192,17 +207,10 @@ class PrefillWorkload(Workload):
                 self.launches_per_step = (1 if ow else 0) + 2 + (1 if nseg > 2 else 0)
             else:
                 self.launches_per_step = 1 + (1 if ow else 0)
-        # algorithmic bytes (inputs, outputs, snapshots, initial and final state)
-        H, K, V, C = dims.num_heads, dims.head_k, dims.head_v, dims.conv_channels
-        es_io, es_o, es_s = b.x.element_size(), self.out.element_size(), self.pool.temporal.element_size()
-        T = b.total_tokens
-        per_tok = C * es_io + (H * K if gate_mode == W.GATE_PER_KEY else H) * 4 + H * 4 + H * V * es_o
-        state_b = H * V * K * es_s + C * 3 * es_io
-        n_snap = sum(((p + l) // track_stride - p // track_stride) for p, l in zip(prefixes, lengths))
-        n_init = sum(1 for w in warm if w)
-        self.tokens = T
-        self.bytes = T * per_tok + (n_snap + B + n_init) * state_b + C * 4 * es_io
-        self.n_snap = n_snap
+        self.tokens = b.total_tokens
+        self.bytes, self.n_snap = prefill_algo_bytes(
+            dims, lengths, prefixes, warm, gate_mode, b.x.element_size(), self.out.element_size(),
+            self.pool.temporal.element_size(), track_stride)
 
     def units_per_step(self):
         return self.tokens
@@ -331,6 +339,32 @@ def plan_e2e_pieces(cu_seqlens, prefix_len, has_initial_state, track_slots, cu_t
     return pieces
 
 
+def decode_algo_bytes(dims, batch, n_draft, replay=False, track_interval=256):
+    """Algorithmic bytes of a decode step and of its dominant launch, bf16
+    state, conv window and inputs, per-key gates: (step bytes, launch bytes).
+    One token: state and window read and written, the token's x, g, beta and
+    output, and the track copy amortised over the interval. Verify of D drafts
+    (chain or tree): the slot's state and window read once, every draft's
+    state and window written, the drafts' inputs and outputs; the commit reads
+    and writes one state. A tree node's read-back of its parent's state is not
+    counted. Replay form: the verify reads the state and writes outputs only;
+    the commit reads and writes the state and reads the inputs of the accepted
+    tokens, (D + 1) / 2 on average."""
+    H, K, V = dims.num_heads, dims.head_k, dims.head_v
+    st = W.state_bytes(dims, 2, 2)
+    o_b = H * V * 2
+    x_b = dims.conv_channels * 2 + H * K * 4 + H * 4 + o_b
+    B, D = batch, n_draft
+    if D == 1:
+        b = B * (2 * st + x_b + st / float(track_interval))
+        return b, b
+    if replay:
+        verify = B * (st + D * x_b)
+        return verify + B * (2 * st + (D + 1) / 2.0 * (x_b - o_b)), verify
+    verify = B * (st + D * st + D * x_b)
+    return verify + B * (2 * st), verify
+
+
 class DecodeWorkload(Workload):
     """KDA decode: pool of 2000 slots x 1 layer (12 x 128 x 128 bf16 temporal,
     [4608][3] bf16 conv), 256 requests on distinct random slots, one token per
@@ -390,38 +424,12 @@ class DecodeWorkload(Workload):
             for j, pj in enumerate(self.TREE):
                 depth[j] = 1 + (depth[pj] if pj >= 0 else 0)
             acc_tokens_tree = float(sum(depth[int(k)] for k in node))
-        st = W.state_bytes(dims, 2, 2)
-        x_b = dims.conv_channels * 2 + 12 * 128 * 4 + 12 * 4 + 12 * 128 * 2
+        self.bytes, self.verify_bytes = decode_algo_bytes(dims, B, n_draft, replay)
         if n_draft == 1:
-            # read + write state and conv per request-step, inputs, output, and
-            # the amortised track copy (one per 256 steps)
-            self.bytes = B * (2 * st + x_b + st / 256.0)
             self.units = B
-        elif replay:
-            # verify reads the state and writes outputs only; the commit reads
-            # and writes the state and reads the accepted tokens' inputs
-            D = n_draft
-            acc_mean = (n_draft + 1) / 2.0
-            o_b = 12 * 128 * 2
-            verify = B * (st + D * x_b)
-            commit = B * (2 * st + acc_mean * (x_b - o_b))
-            self.bytes = verify + commit
-            self.verify_bytes = verify
-            self.units = 1
-            self.acc_tokens = B * acc_mean
         else:
-            # chain or tree: the slot state read once, every draft's state
-            # written, inputs and outputs; a tree node reads its parent's state
-            # back from the per-step buffer (written just before, in L2), which
-            # is not counted
-            D = n_draft
-            acc_mean = (n_draft + 1) / 2.0
-            verify = B * (st + D * st + D * x_b)
-            commit = B * (2 * st)
-            self.bytes = verify + commit
-            self.verify_bytes = verify
             self.units = 1
-            self.acc_tokens = acc_tokens_tree if tree else B * acc_mean
+            self.acc_tokens = acc_tokens_tree if tree else B * (n_draft + 1) / 2.0
         self.steps_done = 0
 
     def units_per_step(self):
@@ -432,7 +440,7 @@ class DecodeWorkload(Workload):
 
     def kernel_bytes_per_launch(self):
         # the dominant kernel is the decode / verify launch
-        return self.bytes if self.n_draft == 1 else self.verify_bytes
+        return self.verify_bytes
 
     def step(self, i):
         L = self.L
