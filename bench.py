@@ -199,14 +199,20 @@ class PrefillWorkload(Workload):
         # launches per call: the chunked kernel, plus the longest-first order of
         # a varlen batch; a request in segments takes the offset / transition
         # launch, the scan (more than two segments) and the final launch
+        # per-key gates add the token-by-token rerun launch behind the chunked
+        # one (its CTAs return at once unless their pair left the chunk's
+        # factored decay range) and the rerun flags in the workspace
         if self.kernel_kind == L.LIN_KERNEL_CHUNKED:
+            kda = gate_mode == W.GATE_PER_KEY
             ow = (B * 4 + 255) // 256 * 256 if 1 < B <= 4096 else 0
-            seg_bytes = need - ow
+            rw = ((B * dims.num_heads + 31) // 32 * 4 + 255) // 256 * 256 if kda else 0
+            seg_bytes = need - ow - rw
             if seg_bytes > 0:
                 nseg = seg_bytes // (2 * dims.num_heads * dims.head_k * dims.head_k * 4)
                 self.launches_per_step = (1 if ow else 0) + 2 + (1 if nseg > 2 else 0)
             else:
                 self.launches_per_step = 1 + (1 if ow else 0)
+            self.launches_per_step += 1 if kda else 0
         self.tokens = b.total_tokens
         self.bytes, self.n_snap = prefill_algo_bytes(
             dims, lengths, prefixes, warm, gate_mode, b.x.element_size(), self.out.element_size(),
@@ -744,20 +750,17 @@ def library_source_hash():
 
 def measured_traffic(workload):
     """dram__bytes_read.sum + dram__bytes_write.sum per launch of the workload's
-    dominant kernel, from the table in profiles/dram_traffic.md, or None when
-    there is no row or the row was measured on other library sources."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    dominant kernel, from the capture table profiles/dram_traffic.json, or None
+    when there is no row or the row was measured on other library sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     cur = library_source_hash()
     with open(path) as fh:
-        for line in fh:
-            cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if len(cells) >= 6 and cells[0] == workload and cells[5] == cur:
-                try:
-                    return int(cells[4])
-                except ValueError:
-                    return None
+        rows = json.load(fh).get("rows", [])
+    for row in rows:
+        if row.get("workload") == workload and row.get("library_source") == cur:
+            return int(row["traffic_per_launch"])
     return None
 
 

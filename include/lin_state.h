@@ -72,12 +72,6 @@ extern "C" {
 #define LIN_ST_BAD_ACCEPT 64   /* commit accept_len outside [0, n_draft]      */
 #define LIN_ST_BAD_TREE 256    /* a draft's parent outside [-1, j), or an
                                   accepted node outside [-1, n_draft)         */
-#define LIN_ST_DECAY_RANGE 128 /* KDA chunked prefill: some key channel decays
-                                  by more than e^80 across half a chunk (mean
-                                  log-decay below -2.5 per token), outside the
-                                  range of the chunk's factored decay; that
-                                  request's results are not valid: rerun it
-                                  with LIN_PREFILL_RECURRENT                   */
 
 /* ---- enums ------------------------------------------------------------- */
 typedef enum { LIN_F32 = 0, LIN_BF16 = 1 } lin_dtype_t;
@@ -147,6 +141,17 @@ typedef struct {
  * distinct live slots; a track slot equal to the live slot is rejected
  * (LIN_ST_TRACK_ALIAS). Workspace: lin_state_prefill_workspace() bytes of
  * device memory (may be 0 -> workspace may be NULL).
+ * Per-key (KDA) gates on the chunked kernel: the chunk factors each key
+ * channel's decay around the chunk's middle row, which holds while no channel
+ * decays by more than e^80 across half a chunk (a mean log-decay above about
+ * -2.5 per token). A (request, head) beyond that stops before it stores its
+ * state and is rerun token by token by a launch the call queues behind the
+ * chunked one (it runs only such pairs and needs no host synchronisation),
+ * so every valid g gives a valid result.
+ * Precision: the chunked kernel carries the state in fp32; its tensor-core
+ * operands are fp16 with high / low splits where the pool is fp32 (and for
+ * per-head gates), so an fp32 pool gets fp32-class results; a bf16 pool with
+ * per-key gates takes bf16 operands.
  * Long single requests: with the chunked kernel, a batch of one request
  * whose heads alone cannot fill the GPU (heads x 4 <= SMs, >= 4096 tokens
  * by total_tokens; any request of >= 8 chunks with LIN_PREFILL_SEGMENTED)
@@ -159,7 +164,8 @@ typedef struct {
  * request's last n_r) are written, so the slots end up as in one piece. The workspace
  * then holds 2 fp32 states per (segment, head). Less workspace than the
  * query reports is an error (LIN_EWORKSPACE); lin_state_prefill_noalloc runs
- * the request in one piece. */
+ * the request in one piece. The workspace also holds the longest-first order
+ * of a varlen batch and, for per-key gates, one rerun bit per (request, head). */
 typedef struct {
   int32_t layer;
   int32_t batch;
@@ -202,14 +208,24 @@ LIN_API int lin_state_prefill(const lin_state_pool_t* pool, const lin_prefill_ar
  * memory during a step: serving engines that give all device memory to their
  * own pools at start-up (so an extra allocation fails or fragments it) and
  * loops that must not pay the device-wide synchronisation of cudaMalloc /
- * cudaFree. Same arguments and results as lin_state_prefill. Its scratch (the
- * longest-first order of the batch) is a fixed array in the library's device
- * memory, held by every GPU that loads the library until the process exits:
- *   - batches above 4096 requests are rejected with LIN_EINVAL;
- *   - the first call on a device looks up that array's device address (with
- *     the device current), so make the first call before any stream capture;
- *   - all calls share the array, so calls that overlap on the GPU (different
- *     streams, no ordering between them) race on it. */
+ * cudaFree. Same arguments as lin_state_prefill; the results are the same
+ * within rounding (a batch equal bit for bit), except that a batch of one long
+ * request runs in one piece, not in segments: the same values within the
+ * fp32 / bf16 tolerances, but on only `heads` CTAs, so much slower than
+ * lin_state_prefill for such a request. Its scratch (the longest-first order
+ * of a batch, the per-key rerun bits) is fixed arrays in the library's device
+ * memory (48 KB), held by every GPU that loads the library until the process
+ * exits:
+ *   - on the chunked kernel, batches of more than one request above 4096
+ *     requests, and per-key gates with more than 262,144 (request, head)
+ *     pairs, are rejected with LIN_EINVAL; the token-by-token kernel has
+ *     lin_state_prefill's limits;
+ *   - the first call on a device looks up the arrays' device addresses with
+ *     the device current (and again in a new context of that device, e.g.
+ *     after cudaDeviceReset), so make the first call before any stream capture;
+ *   - all calls share the arrays, so calls that overlap on the GPU (different
+ *     streams, no ordering between them) race on them; each call clears what
+ *     must start at zero. */
 LIN_API int lin_state_prefill_noalloc(const lin_state_pool_t* pool,
                                       const lin_prefill_args_t* args, void* stream);
 

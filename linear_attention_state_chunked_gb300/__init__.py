@@ -28,7 +28,6 @@ LIN_PREFILL_SEGMENTED = 16
 LIN_UPDATE_ADDITIVE = 32
 LIN_ST_BAD_SLOT, LIN_ST_BAD_PREFIX, LIN_ST_TRACK_ALIAS, LIN_ST_BAD_SEQLEN = 1, 2, 4, 8
 LIN_ST_COPY_ALIAS, LIN_ST_TIMEOUT, LIN_ST_BAD_ACCEPT = 16, 32, 64
-LIN_ST_DECAY_RANGE = 128
 LIN_ST_BAD_TREE = 256
 
 LIN_KERNEL_RECURRENT, LIN_KERNEL_CHUNKED = 0, 1

@@ -101,7 +101,7 @@ int check_spec(const lin_state_pool_t* p, const lin_spec_buf_t& s, int batch, in
 
 extern "C" {
 
-int lin_state_version(void) { return (1 << 16) | 0; }
+int lin_state_version(void) { return (1 << 16) | 1; }
 
 int lin_state_selftest_mma(const float* A, const float* B, float* D, int32_t n, int32_t k,
                            int32_t flags, int32_t* status, void* stream) {
@@ -211,10 +211,21 @@ int lin_state_prefill_noalloc(const lin_state_pool_t* pool, const lin_prefill_ar
                               void* stream) {
   int rc = check_prefill(pool, a);
   if (rc) return rc;
-  if (a->batch > lin::noalloc_max_batch())
+  if (a->batch == 0) return ok();
+  // the fixed scratch bounds only the chunked kernel: its batch order (more
+  // than one request) and its per-key rerun flags; the token-by-token kernel
+  // takes what lin_state_prefill takes
+  const bool chunked = !(a->flags & LIN_PREFILL_RECURRENT) && lin::chunked_prefill_supported(*pool, *a);
+  if (chunked && a->batch > 1 && a->batch > lin::noalloc_max_batch())
     return fail(LIN_EINVAL, "prefill_noalloc: batch %d above the fixed scratch of %d requests",
                 a->batch, lin::noalloc_max_batch());
-  if (a->batch == 0) return ok();
+  if (chunked && a->gate_mode == LIN_GATE_PER_KEY &&
+      int64_t(a->batch) * pool->num_heads > lin::noalloc_max_pairs())
+    return fail(LIN_EINVAL,
+                "prefill_noalloc: %lld (request, head) pairs above the fixed scratch of %lld",
+                static_cast<long long>(int64_t(a->batch) * pool->num_heads),
+                static_cast<long long>(lin::noalloc_max_pairs()));
+  if (!chunked && a->batch > 65535) return fail(LIN_EINVAL, "prefill: batch above 65535");
   cudaError_t e = lin::launch_prefill_noalloc(*pool, *a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lin_state_prefill_noalloc launch");
   return ok();

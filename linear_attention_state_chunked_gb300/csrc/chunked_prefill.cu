@@ -33,8 +33,18 @@
 // GDN: the scalar decay exp(b_t - b_i) is applied in fp32 to A' and P'.)
 // The state is carried in fp32 in tensor memory across chunks and written
 // (rounded to the pool dtype) at every snapshot boundary and at the end.
-// Operands are fp16 for GDN (10-bit mantissa; every decay-scaled factor stays
-// in [0, 1]) and bf16 for KDA (the per-channel decay ratios exceed fp16 range).
+// Operand precision follows the pool's state dtype:
+//   - fp32 pools (and every GDN pool): fp16 operands (10-bit mantissa; every
+//     decay-scaled factor stays within [0, 1]) with high / low splits on the
+//     products that set the error. KDA's MMA1 factors exp(+-(b - b_ref)) leave
+//     fp16 range, so that one product takes bf16 operands, split likewise
+//     (hi = bf16(x), lo = bf16(x - hi): 16 significant bits, fp32 range).
+//   - KDA with a bf16 pool: bf16 operands, single products (the pool itself
+//     holds 8 significant bits).
+// A KDA (request, head) whose decay leaves the factored range (some key
+// channel decaying by more than e^80 across half a chunk) stops before it
+// writes its state back and is flagged; a token-by-token launch queued behind
+// this one then reruns exactly the flagged pairs from the untouched slot.
 //
 // One CTA (16 warps) runs one (request, head) sequentially over its chunks.
 
@@ -42,6 +52,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -85,7 +96,8 @@ constexpr uint32_t OFF_VV = 131072;             // V, rows i (MN-major A)
 constexpr uint32_t OFF_UT = OFF_VV;             //   after MMA2: U^T (high), rows v (K-major A)
 constexpr uint32_t OFF_QH = 147456;             // gamma . Q, rows t (K-major B)
 constexpr uint32_t OFF_KT = 163840;             // (gamma_last/gamma) . K, rows i (MN-major B)
-constexpr uint32_t OFF_WC = 180224;             // conv taps, fp32 [4][384] (tap-major)
+constexpr uint32_t OFF_KRL = 180224;            // K_r low part (KDA with fp32 state), 64 x 128
+constexpr uint32_t OFF_WC = OFF_KRL + 16384;    // conv taps, fp32 [4][384] (tap-major)
 constexpr uint32_t OFF_HALO = OFF_WC + 6144;    // initial conv window, fp32 [3][384]
 constexpr uint32_t OFF_WTOT = OFF_HALO + 4608;  // per-warp gate sums, fp32 [16][128]
 constexpr uint32_t OFF_SBETA = OFF_WTOT + 8192; // beta_t, fp32 [64]
@@ -135,6 +147,8 @@ struct ChunkParams {
   float* seg_state_out;        // offset runs: fp32 state after the segment, [seg][H][V][K]
   float* seg_trans_out;        // transition runs: likewise
   const float* seg_state_in;   // mode 3: fp32 state before segment k >= 1 at index k - 1
+  uint32_t* redo;              // KDA: bit r * H + h set when (request r, head h) left the
+                               // factored decay range (cleared before the launch)
 };
 
 // Longest-first order of a varlen batch: the sequential chunk chain of the
@@ -282,6 +296,19 @@ __device__ __forceinline__ void split4(float a, float b, float c, float d, uint3
   lo[1] = *reinterpret_cast<const uint32_t*>(&l1);
 }
 
+// hi / lo bf16 split of four values: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split4_bf(float a, float b, float c, float d, uint32_t (&hi)[2],
+                                          uint32_t (&lo)[2]) {
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(a, b), h1 = __floats2bfloat162_rn(c, d);
+  const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+  const __nv_bfloat162 l0 = __floats2bfloat162_rn(a - f0.x, b - f0.y);
+  const __nv_bfloat162 l1 = __floats2bfloat162_rn(c - f1.x, d - f1.y);
+  hi[0] = *reinterpret_cast<const uint32_t*>(&h0);
+  hi[1] = *reinterpret_cast<const uint32_t*>(&h1);
+  lo[0] = *reinterpret_cast<const uint32_t*>(&l0);
+  lo[1] = *reinterpret_cast<const uint32_t*>(&l1);
+}
+
 // Gate inputs of one chunk for this thread: KDA log-decay for TPW tokens x 4
 // key channels, or the per-head scalar; beta for the TPW tokens.
 template <bool KDA>
@@ -351,15 +378,18 @@ __global__ void __launch_bounds__(NT, 1)
                            const __grid_constant__ CUtensorMap tmap_xt,
                            const __grid_constant__ CUtensorMap tmap_state,
                            const __grid_constant__ CUtensorMap tmap_out, const ChunkParams p) {
-  // GDN: fp16 operands with high / low splits on the products that set the
-  // error (see the header); KDA: bf16 operands, single products.
-  constexpr bool BF = KDA;
-  constexpr bool SPLIT = !KDA;
+  // fp32 pools and GDN: fp16 operands with high / low splits on the products
+  // that set the error, KDA's MMA1 in bf16 (split); KDA with a bf16 pool:
+  // bf16 operands, single products (see the header).
+  constexpr bool SPLIT = !KDA || ST == LIN_F32;
+  constexpr bool BF = KDA && !SPLIT;  // operand type of every product but MMA1
+  constexpr bool BF1 = KDA;           // operand type of MMA1 ([K_l; Q_l] K_r^T)
   extern __shared__ uint8_t dsm[];
   __shared__ uint64_t bar_mma;
   __shared__ uint64_t bar_x;  // x tile of the next chunk landed
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ int range_sh;  // KDA: a key channel's decay left the factored range
 
   const lin_state_pool_t& pool = p.pool;
   const lin_prefill_args_t& a = p.a;
@@ -432,6 +462,12 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
   // initial state: 0 zeros, 1 the slot, 2 identity, 3 the segment workspace
+  if (KDA && seg_mode == kSegFinal && p.redo) {
+    // an offset or transition run of this (request, head) left the factored
+    // decay range: the token-by-token rerun redoes it from the slot
+    const int idx = r * H + h;
+    if ((p.redo[idx >> 5] >> (idx & 31)) & 1u) return;
+  }
   const bool warm_r = a.has_initial_state[r] != 0;
   int init_kind = warm_r ? 1 : 0;
   if (seg > 0) init_kind = seg_mode == kSegOffset ? 0 : (seg_mode == kSegTransition ? 2 : 3);
@@ -488,6 +524,7 @@ __global__ void __launch_bounds__(NT, 1)
     umma::mbar_init(&bar_x, 1);
     umma::mbar_fence_init();
     abort_sh = 0;
+    range_sh = 0;
   }
   if (warp == 0) umma::tmem_alloc(&tmem_base_sh, TMEM_COLS);
   umma::fence_before_sync();
@@ -804,11 +841,23 @@ __global__ void __launch_bounds__(NT, 1)
           eL[e] = KDA ? __expf(b - bref[ee]) : 1.f;
           eR[e] = KDA ? __expf(bref[ee] - b) : 1.f;
           eT[e] = KDA ? ecl[e] * eR[e] : __expf(blast[ee] - b);
-          // the factored decay must stay inside fp32 range (see LIN_ST_DECAY_RANGE)
+          // the factored decay must stay inside fp32 range (else the pair is rerun)
           if (KDA && ok && fabsf(b - bref[ee]) > 80.f) range_bad = true;
         }
         const int c = lane * 4;
-        if (SPLIT) {
+        if (SPLIT && KDA) {
+          // MMA1 operands in bf16 (hi / lo): K_l, Q_l and K_r
+          uint32_t hi[2], lo[2];
+          split4_bf(kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3], hi, lo);
+          st_shared_v2(sb + OFF_KQ + umma::rp_offset(t, c, 128), hi[0], hi[1]);
+          st_shared_v2(sb + OFF_KQL + umma::rp_offset(t, c, 128), lo[0], lo[1]);
+          split4_bf(qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3], hi, lo);
+          st_shared_v2(sb + OFF_KQ + umma::rp_offset(CH + t, c, 128), hi[0], hi[1]);
+          st_shared_v2(sb + OFF_KQL + umma::rp_offset(CH + t, c, 128), lo[0], lo[1]);
+          split4_bf(kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3], hi, lo);
+          st_shared_v2(sb + OFF_KR + umma::rp_offset(t, c, 64), hi[0], hi[1]);
+          st_shared_v2(sb + OFF_KRL + umma::rp_offset(t, c, 64), lo[0], lo[1]);
+        } else if (SPLIT) {
           uint32_t hi[2], lo[2];
           split4(kn[0], kn[1], kn[2], kn[3], hi, lo);
           st_shared_v2(sb + OFF_KQ + umma::rp_offset(t, c, 128), hi[0], hi[1]);
@@ -817,29 +866,46 @@ __global__ void __launch_bounds__(NT, 1)
           st_shared_v2(sb + OFF_KQ + umma::rp_offset(CH + t, c, 128), hi[0], hi[1]);
           st_shared_v2(sb + OFF_KQL + umma::rp_offset(CH + t, c, 128), lo[0], lo[1]);
         } else {
-          put4<BF>(sb + OFF_KQ, 128, t, c, kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3]);
-          put4<BF>(sb + OFF_KQ, 128, CH + t, c, qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3]);
-          put4<BF>(sb + OFF_KR, 64, t, c, kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3]);
+          put4<BF1>(sb + OFF_KQ, 128, t, c, kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3]);
+          put4<BF1>(sb + OFF_KQ, 128, CH + t, c, qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3]);
+          put4<BF1>(sb + OFF_KR, 64, t, c, kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3]);
         }
         put4<BF>(sb + OFF_KH, 64, t, c, kn[0] * eH[0], kn[1] * eH[1], kn[2] * eH[2], kn[3] * eH[3]);
         put4<BF>(sb + OFF_VV, 64, t, c, vv[0], vv[1], vv[2], vv[3]);
         put4<BF>(sb + OFF_QH, 64, t, c, qn[0] * eH[0], qn[1] * eH[1], qn[2] * eH[2], qn[3] * eH[3]);
         put4<BF>(sb + OFF_KT, 64, t, c, kn[0] * eT[0], kn[1] * eT[1], kn[2] * eT[2], kn[3] * eT[3]);
       }
-      if (KDA && __any_sync(0xffffffffu, range_bad) && lane == 0) report(a.status, LIN_ST_DECAY_RANGE);
+      if (KDA && __any_sync(0xffffffffu, range_bad) && lane == 0) range_sh = 1;
     }
     umma::fence_smem_to_async();
     __syncthreads();
+    if (KDA && range_sh) {
+      // The factored decay of this chunk leaves fp32 range: stop before any
+      // of its results (or the final state) is stored, and flag the pair for
+      // the token-by-token rerun queued behind this launch. Every MMA and x
+      // tile issued so far has completed; the teardown drains the stores.
+      if (tid == 0 && p.redo) {
+        const int idx = r * H + h;
+        atomicOr(p.redo + (idx >> 5), 1u << (idx & 31));
+      }
+      break;
+    }
 
     // ---- MMA1: [A'; P'] = [K_l; Q_l] K_r^T; prefetch the next chunk's x rows
     if (tid == 0) {
       if (j + 1 < nch) prefetch_x_tile(&tmap_x, row0 + CH, h, H);
       umma::fence_after_sync();
-      constexpr uint32_t id1 = umma::idesc_f16(128, 64, BF, false, false);
+      constexpr uint32_t id1 = umma::idesc_f16(128, 64, BF1, false, false);
 #pragma unroll
       for (int k0 = 0; k0 < DH; k0 += 16) {
         const uint64_t ah = umma::desc_kmajor(sb + OFF_KQ, 128, k0);
-        if (SPLIT) {
+        if (SPLIT && KDA) {
+          const uint64_t al = umma::desc_kmajor(sb + OFF_KQL, 128, k0);
+          const uint64_t bh = umma::desc_kmajor(sb + OFF_KR, 64, k0);
+          umma::mma_f16(tm + COL_R1, ah, bh, id1, k0 > 0);
+          umma::mma_f16(tm + COL_R1, ah, umma::desc_kmajor(sb + OFF_KRL, 64, k0), id1, 1);
+          umma::mma_f16(tm + COL_R1, al, bh, id1, 1);
+        } else if (SPLIT) {
           const uint64_t al = umma::desc_kmajor(sb + OFF_KQL, 128, k0);
           umma::mma_f16(tm + COL_R1, ah, ah, id1, k0 > 0);  // B: rows 0..63 of the same panels
           umma::mma_f16(tm + COL_R1, ah, al, id1, 1);
@@ -1453,7 +1519,7 @@ size_t segment_workspace(const lin_state_pool_t& pool, const SegPlan& sp) {
 
 template <bool KDA, int ST>
 cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
-                     const SegPlan& sp, float* seg_buf, cudaStream_t s) {
+                     const SegPlan& sp, float* seg_buf, uint32_t* redo, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmap;
@@ -1524,7 +1590,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
     float* mbuf = seg_buf + size_t(sp.nseg) * H * DH * DH;
     // offset runs of segments 0 .. n-2 (segment 0 also with its outputs and
     // snapshots) and transition runs of segments 1 .. n-2, one launch
-    ChunkParams p1{pool, a, nullptr, kSegOffsetAndTransition, sp.seg_len, 0, sp.nseg, bbuf, mbuf, nullptr};
+    ChunkParams p1{pool, a, nullptr, kSegOffsetAndTransition, sp.seg_len, 0, sp.nseg, bbuf, mbuf, nullptr, redo};
     kern<<<unsigned(2 * sp.nseg - 3) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (sp.nseg > 2) {
@@ -1534,11 +1600,11 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
       seg_scan_kernel<<<H * (DH / kScanRows), kScanThreads, kScanSmem, s>>>(bbuf, mbuf, sp.nseg, int(H));
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    ChunkParams p3{pool, a, nullptr, kSegFinal, sp.seg_len, 1, sp.nseg, nullptr, nullptr, bbuf};
+    ChunkParams p3{pool, a, nullptr, kSegFinal, sp.seg_len, 1, sp.nseg, nullptr, nullptr, bbuf, redo};
     kern<<<unsigned(sp.nseg - 1) * H, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p3);
     return cudaGetLastError();
   }
-  ChunkParams p{pool, a, order, kSegOff, 0, 0, 0, nullptr, nullptr, nullptr};
+  ChunkParams p{pool, a, order, kSegOff, 0, 0, 0, nullptr, nullptr, nullptr, redo};
   const unsigned grid = static_cast<unsigned>(a.batch) * H;
   kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, p);
   return cudaGetLastError();
@@ -1561,71 +1627,148 @@ size_t order_workspace(const lin_prefill_args_t& a) {
   return (static_cast<size_t>(a.batch) * sizeof(int32_t) + 255) & ~size_t(255);
 }
 
+// KDA: one bit per (request, head), set for a pair whose decay left the
+// chunk's factored range (the token-by-token rerun redoes those pairs).
+size_t redo_workspace(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
+  if (a.gate_mode != LIN_GATE_PER_KEY) return 0;
+  const size_t words = (static_cast<size_t>(a.batch) * pool.num_heads + 31) / 32;
+  return (words * sizeof(uint32_t) + 255) & ~size_t(255);
+}
+
+// Order (when given), the chunked launch(es), and for KDA the rerun of the
+// pairs the chunked kernel flagged: the flags are cleared first, and the
+// token-by-token launch behind the chunked one runs only the flagged pairs
+// (the others return at once), so no host synchronisation is needed.
 cudaError_t launch_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
-                           const SegPlan& sp, float* seg_buf, cudaStream_t stream) {
+                           const SegPlan& sp, float* seg_buf, uint32_t* redo, cudaStream_t stream) {
   const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
   const bool bf = pool.state_dtype == LIN_BF16;
-  if (kda)
-    return bf ? launch_t<true, LIN_BF16>(pool, a, order, sp, seg_buf, stream)
-              : launch_t<true, LIN_F32>(pool, a, order, sp, seg_buf, stream);
-  return bf ? launch_t<false, LIN_BF16>(pool, a, order, sp, seg_buf, stream)
-            : launch_t<false, LIN_F32>(pool, a, order, sp, seg_buf, stream);
+  cudaError_t e;
+  if (kda) {
+    if (!redo) return cudaErrorInvalidValue;
+    if ((e = cudaMemsetAsync(redo, 0, redo_workspace(pool, a), stream)) != cudaSuccess) return e;
+    e = bf ? launch_t<true, LIN_BF16>(pool, a, order, sp, seg_buf, redo, stream)
+           : launch_t<true, LIN_F32>(pool, a, order, sp, seg_buf, redo, stream);
+    if (e != cudaSuccess) return e;
+    return launch_prefill_recurrent(pool, a, stream, redo);
+  }
+  return bf ? launch_t<false, LIN_BF16>(pool, a, order, sp, seg_buf, nullptr, stream)
+            : launch_t<false, LIN_F32>(pool, a, order, sp, seg_buf, nullptr, stream);
 }
 }  // namespace
 
-// Workspace: the batch order (varlen batches), or the per-segment states of a
-// long single request run in segments.
+// Workspace: the batch order (varlen batches), the per-segment states of a
+// long single request run in segments, and the KDA rerun flags.
 size_t chunked_prefill_workspace(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
-  return order_workspace(a) + segment_workspace(pool, segment_plan(pool, a));
+  return order_workspace(a) + segment_workspace(pool, segment_plan(pool, a)) + redo_workspace(pool, a);
 }
 
 cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  const size_t ow = order_workspace(a);
-  int32_t* order = (ow > 0 && workspace && workspace_bytes >= ow) ? static_cast<int32_t*>(workspace) : nullptr;
+  const size_t ow = order_workspace(a), rw = redo_workspace(pool, a);
   SegPlan sp = segment_plan(pool, a);
-  float* seg_buf = nullptr;
-  const size_t sw = segment_workspace(pool, sp);
-  if (sw > 0 && workspace && workspace_bytes >= ow + sw)
-    seg_buf = reinterpret_cast<float*>(static_cast<char*>(workspace) + ow);
-  else
-    sp = SegPlan{};  // too little workspace: run the request in one piece
-  return launch_chunked(pool, a, order, sp, seg_buf, stream);
+  size_t sw = segment_workspace(pool, sp);
+  if (ow + sw + rw > 0 && (!workspace || workspace_bytes < ow + sw + rw)) return cudaErrorInvalidValue;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* order = ow > 0 ? reinterpret_cast<int32_t*>(ws) : nullptr;
+  float* seg_buf = sw > 0 ? reinterpret_cast<float*>(ws + ow) : nullptr;
+  uint32_t* redo = rw > 0 ? reinterpret_cast<uint32_t*>(ws + ow + sw) : nullptr;
+  if (!seg_buf) sp = SegPlan{};
+  return launch_chunked(pool, a, order, sp, seg_buf, redo, stream);
 }
 
 // ---------------------------------------------------------------------------
-// Allocation-free prefill: the order scratch lives in a fixed device array of
-// this file instead of a caller workspace. Every GPU that loads the library
-// holds the array until exit. Calls share it, so calls that overlap on the GPU
-// race on it; each call rewrites every entry it reads (nothing needs clearing).
+// Allocation-free prefill: its scratch (the batch order, the KDA rerun flags)
+// lives in fixed device arrays of this file instead of a caller workspace.
+// Every GPU that loads the library holds them until exit. All calls share
+// them, so calls that overlap on the GPU race on them. Each call rewrites the
+// order entries it reads and clears the flags it uses before its launch.
 // ---------------------------------------------------------------------------
-constexpr int kNoAllocMaxBatch = kOrderMax;  // 4096 requests
+constexpr int kNoAllocMaxBatch = kOrderMax;        // requests of a sorted batch: 16 KB
+constexpr int64_t kNoAllocMaxPairs = int64_t(1) << 18;  // (request, head) pairs of a KDA call: 32 KB
 static __device__ __align__(256) int32_t g_noalloc_order[kNoAllocMaxBatch];
+static __device__ __align__(256) uint32_t g_noalloc_redo[kNoAllocMaxPairs / 32];
 
 namespace {
-std::atomic<int32_t*> g_noalloc_ptr[kMaxDevices];
+// In host code the arrays' names are stand-ins, not device addresses: the
+// addresses are looked up with the device current, once per device and
+// context (a new context of the device, e.g. after cudaDeviceReset, may load
+// the module elsewhere), and cached.
+struct NoAllocAddrs {
+  unsigned long long ctx = 0;  // id of the context the addresses belong to (0: none yet)
+  int32_t* order = nullptr;
+  uint32_t* redo = nullptr;
+};
+std::mutex g_noalloc_mu;
+NoAllocAddrs g_noalloc_addrs[kMaxDevices];
+
+// Id of the calling thread's current context, 0 when it cannot be read (the
+// addresses are then looked up on every call).
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+cudaError_t noalloc_addresses(int32_t** order, uint32_t** redo) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocAddrs& c = g_noalloc_addrs[dev];
+  if (ctx == 0 || c.ctx != ctx) {
+    NoAllocAddrs n;
+    if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&n.order), g_noalloc_order)) != cudaSuccess) return e;
+    if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&n.redo), g_noalloc_redo)) != cudaSuccess) return e;
+    n.ctx = ctx;
+    c = n;
+  }
+  *order = c.order;
+  *redo = c.redo;
+  return cudaSuccess;
+}
 }  // namespace
 
 int noalloc_max_batch() { return kNoAllocMaxBatch; }
+int64_t noalloc_max_pairs() { return kNoAllocMaxPairs; }
 
 cudaError_t launch_prefill_noalloc(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
                                    cudaStream_t stream) {
   if (!chunked_prefill_supported(pool, a) || (a.flags & LIN_PREFILL_RECURRENT))
     return launch_prefill_recurrent(pool, a, stream);  // needs no scratch
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  int32_t* ptr = g_noalloc_ptr[dev].load(std::memory_order_acquire);
-  if (!ptr) {
-    // Set-up, once per device with that device current: in host code the
-    // array's name is only a stand-in, so its device address is looked up.
-    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_order);
+  const bool sorted = order_workspace(a) > 0;
+  const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
+  if (sorted && a.batch > kNoAllocMaxBatch) return cudaErrorInvalidValue;
+  if (kda && int64_t(a.batch) * pool.num_heads > kNoAllocMaxPairs) return cudaErrorInvalidValue;
+  int32_t* order = nullptr;
+  uint32_t* redo = nullptr;
+  if (sorted || kda) {
+    cudaError_t e = noalloc_addresses(&order, &redo);
     if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev].store(ptr, std::memory_order_release);
   }
-  const size_t need = order_workspace(a);
-  return launch_chunked(pool, a, need ? ptr : nullptr, SegPlan{}, nullptr, stream);
+  // a single long request runs in one piece: the segmented mode needs
+  // per-segment state scratch that grows with the request
+  return launch_chunked(pool, a, sorted ? order : nullptr, SegPlan{}, nullptr, kda ? redo : nullptr, stream);
 }
 
 }  // namespace lin

@@ -36,8 +36,11 @@ constexpr int kDecodeMaxStage = 110 * 1024;
 // replay commit (in place, no outputs).
 cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t& a,
                           const int32_t* accept, cudaStream_t stream);
+// redo: when given, one bit per (request, head) (bit r * H + h); only the
+// pairs whose bit is set run (the rerun behind a KDA chunked launch).
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,
-                                     const lin_prefill_args_t& a, cudaStream_t stream);
+                                     const lin_prefill_args_t& a, cudaStream_t stream,
+                                     const uint32_t* redo = nullptr);
 
 // Chunked tensor-core prefill (chunked_prefill.cu).
 bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_args_t& a);
@@ -46,8 +49,12 @@ cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefi
                                    void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
 
-// Prefill whose scratch is a fixed device array (chunked_prefill.cu).
+// Prefill whose scratch is fixed device arrays (chunked_prefill.cu): at most
+// noalloc_max_batch() requests when the chunked kernel sorts the batch (more
+// than one request), at most noalloc_max_pairs() (request, head) pairs for
+// per-key (KDA) gates on the chunked kernel.
 int noalloc_max_batch();
+int64_t noalloc_max_pairs();
 cudaError_t launch_prefill_noalloc(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
                                    cudaStream_t stream);
 

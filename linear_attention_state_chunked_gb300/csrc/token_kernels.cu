@@ -1020,6 +1020,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
 struct PrefillParams {
   lin_state_pool_t pool;
   lin_prefill_args_t a;
+  const uint32_t* redo;  // when set: run only the (request, head) pairs whose bit is set
 };
 
 template <int D, int V, int ST>
@@ -1031,6 +1032,10 @@ __global__ void __launch_bounds__(TokCfg<D, V>::NT) prefill_recurrent_kernel(Pre
   const int r = blockIdx.x, h = blockIdx.y;
   const int H = pool.num_heads;
   const int ns = pool.num_slots;
+  if (p.redo) {
+    const int64_t idx = int64_t(r) * H + h;
+    if (!((p.redo[idx >> 5] >> (idx & 31)) & 1u)) return;
+  }
   const bool rep = (h == 0 && threadIdx.x == 0);
   const int slot = a.slot[r];
   if (slot < 0) return;
@@ -1202,8 +1207,8 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
 
 template <int D, int V, int ST>
 cudaError_t prefill_launch(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
-                           cudaStream_t stream) {
-  PrefillParams p{pool, a};
+                           cudaStream_t stream, const uint32_t* redo) {
+  PrefillParams p{pool, a, redo};
   prefill_recurrent_kernel<D, V, ST><<<dim3(a.batch, pool.num_heads), TokCfg<D, V>::NT, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -1250,9 +1255,10 @@ cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t&
 }
 
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,
-                                     const lin_prefill_args_t& a, cudaStream_t stream) {
+                                     const lin_prefill_args_t& a, cudaStream_t stream,
+                                     const uint32_t* redo) {
   if (a.batch <= 0) return cudaSuccess;
-  LIN_DISPATCH_D_ST(prefill_launch, pool.head_k, pool.head_v, pool.state_dtype, pool, a, stream);
+  LIN_DISPATCH_D_ST(prefill_launch, pool.head_k, pool.head_v, pool.state_dtype, pool, a, stream, redo);
 }
 
 }  // namespace lin

@@ -91,6 +91,28 @@ def test_kimi_k3_kda_varlen_full_size_sampled():
     check_prefill_slice(wl2, warm[0], [0], TOL_BF16)
 
 
+def test_kimi_k3_kda_varlen_fp32_state_full_size_sampled():
+    """The Kimi-K3 varlen workload (32 requests of U{1k..16k} tokens, half warm
+    at a 64-multiple prefix, per-key decay, snapshots every 256) with an fp32
+    pool and fp32 outputs: the chunked kernel's fp32-state path holds the fp32
+    bar at full size, on the longest request and on a warm one."""
+    Ls, Ps = W.kp_lengths(0)
+    ext = [l - p for l, p in zip(Ls, Ps)]
+    warm = [1 if p else 0 for p in Ps]
+
+    def make():
+        return bench.PrefillWorkload(L, DEV, "kimi_k3_kda_varlen_prefill", W.KIMI_K3_TP8, ext, Ps,
+                                     warm, W.GATE_PER_KEY, torch.bfloat16, torch.float32,
+                                     torch.float32, 256, 2, "softplus")
+
+    wl = make()
+    assert wl.kernel_kind == L.LIN_KERNEL_CHUNKED
+    longest = int(torch.argmax(torch.tensor(ext)))
+    check_prefill_slice(wl, longest, [3, 11], TOL_F32)
+    wl2 = make()
+    check_prefill_slice(wl2, warm.index(1), [5], TOL_F32)
+
+
 def test_long_single_request_full_size_snapshots():
     """131,072 tokens, 12 heads, snapshots every 64 into 2,048 distinct slots:
     every snapshot's conv window equals the 3 inputs before its boundary (bit for

@@ -144,29 +144,51 @@ def test_single_request_in_segments(gate, pingpong):
     assert (out - out1).norm() <= tol * out1.norm()
 
 
-def test_kda_decay_beyond_chunk_range_is_reported():
-    """KDA with log-decay -30 * softplus(N(0,1)) per key channel: across half a
-    chunk some channel decays by far more than e^80, outside the chunked
-    kernel's factored range. The chunked call must say so in the status
-    (LIN_ST_DECAY_RANGE) rather than return silently wrong values, and the
-    recurrent kernel must still match the oracle on the same inputs."""
+@pytest.mark.parametrize("sdt", [torch.bfloat16, torch.float32])
+def test_kda_decay_beyond_chunk_range_is_rerun(sdt):
+    """KDA where some (request, head) pairs decay far faster than the chunked
+    kernel's factored range allows (log-decay -30 * softplus(N(0,1)) per key
+    channel: across half a chunk a channel decays by far more than e^80). The
+    chunked call itself must return the right outputs, states and snapshots for
+    every pair: the out-of-range pairs through the token-by-token rerun the call
+    queues, the others through the chunked kernel; no status bit is set."""
     dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
-    b = W.make_prefill_batch(dims, [200], W.GATE_PER_KEY, dtype=torch.bfloat16, seed=5,
-                             gate="softplus", tag="dr")
-    b.g = b.g * 30.0
-    pool = L.StatePool(1, 4, 2, 128, state_dtype=torch.bfloat16, conv_dtype=torch.bfloat16, device=DEV)
-    st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out = torch.zeros((200, 2, 128), device=DEV)
-    kw = dict(layer=0, x=b.x.to(DEV), conv_w=b.conv_w.to(DEV), g=b.g.to(DEV), beta=b.beta.to(DEV),
-              out=out, cu_seqlens=b.cu_seqlens.to(DEV), prefix_len=b.prefix_len.to(DEV), slot=_i32([1]),
-              has_initial_state=b.has_initial_state.to(DEV), track_slots=None, cu_track=None,
-              track_stride=0, gate_mode=W.GATE_PER_KEY, flags=FLAGS, status=st)
-    assert L.lin_state_prefill_kernel(pool, **kw) == L.LIN_KERNEL_CHUNKED
-    L.lin_state_prefill(pool, **kw)
-    assert L.lin_state_read_status(st) & L.LIN_ST_DECAY_RANGE
+    lengths, prefixes, warm = [200, 333, 130], [0, 64, 128], [0, 1, 1]
+    b = W.make_prefill_batch(dims, lengths, W.GATE_PER_KEY, dtype=torch.bfloat16, seed=5,
+                             gate="softplus", tag="dr", prefixes=prefixes, warm=warm)
+    cu = b.cu_seqlens.tolist()
+    b.g[cu[0]:cu[1]] *= 30.0              # request 0: both heads out of range
+    b.g[cu[1] + 150:cu[1] + 260, 1] *= 30.0  # request 1: head 1 from its third chunk on
+    pool = L.StatePool(1, 12, 2, 128, state_dtype=sdt, conv_dtype=torch.bfloat16, device=DEV)
+    fill_pool(pool, 6)
     op = oracle_pool(pool)
-    out2, oo = run_both(pool, op, b, [2], [], [0, 0], 0, "recurrent", out_dtype=torch.float32)
-    compare_outputs(out2, oo, b.cu_seqlens.tolist(), TOL_BF16)
+    out, oo = run_both(pool, op, b, [1, 2, 3], [4, 5, 6, 7, 8, 9], [0, 2, 4, 6], 64, "chunked")
+    tol = TOL_BF16 if sdt == torch.bfloat16 else TOL_F32
+    compare_outputs(out, oo, cu, tol)
+    compare_slots(pool, op, list(range(1, 10)), tol)
+
+
+@pytest.mark.parametrize("where", ["middle", "last"])
+def test_kda_decay_beyond_range_in_segments(where):
+    """The same in the segmented mode of a long single request: an out-of-range
+    stretch inside a middle segment (caught by the offset and transition runs,
+    so the final runs skip the head) or inside the last segment (caught by its
+    final run, which stops before the write-back); the rerun redoes that head."""
+    dims = W.LayerDims(num_heads=2, head_k=128, head_v=128)
+    L_ = 1500
+    b = W.make_prefill_batch(dims, [L_], W.GATE_PER_KEY, dtype=torch.bfloat16, seed=7,
+                             gate="softplus", tag="drs")
+    lo = 600 if where == "middle" else 1400
+    b.g[lo:lo + 60, 0] *= 30.0
+    n_tr = L_ // 64
+    pool = L.StatePool(1, 2 + n_tr, 2, 128, state_dtype=torch.float32, conv_dtype=torch.bfloat16,
+                       device=DEV)
+    op = oracle_pool(pool)
+    tracks = list(range(2, 2 + n_tr))
+    out, oo = run_both(pool, op, b, [1], tracks, [0, n_tr], 64, "chunked",
+                       flags=FLAGS | L.LIN_PREFILL_SEGMENTED)
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), TOL_F32)
+    compare_slots(pool, op, [1] + tracks, TOL_F32)
 
 
 @pytest.mark.parametrize("path", list(PATHS))
@@ -246,14 +268,6 @@ def test_long_request_placement_page_example(path):
         assert d <= tol * pool.temporal[0, s].abs().max().item() + (0 if path == "chunked" else 1e-6)
 
 
-def tol_for(path, gate_mode, state_dtype):
-    """The chunked kernel runs KDA products with bf16 operands (the per-channel
-    decay ratios overflow fp16), so KDA is held to the bf16 bar there."""
-    if state_dtype == torch.bfloat16 or (path == "chunked" and gate_mode == W.GATE_PER_KEY):
-        return TOL_BF16
-    return TOL_F32
-
-
 @pytest.mark.parametrize("gate", [W.GATE_PER_HEAD, W.GATE_PER_KEY])
 @pytest.mark.parametrize("path", list(PATHS))
 def test_edge_cases(path, gate):
@@ -277,9 +291,8 @@ def test_edge_cases(path, gate):
     out, oo = run_both(pool, op, b, slots, tracks, cu_track, 64, path, expect_status=expect)
     ok_reqs = [0, 1, 2, 7]
     skip = [r for r in range(len(lengths)) if r not in ok_reqs]
-    tol = tol_for(path, gate, torch.float32)
-    compare_outputs(out, oo, b.cu_seqlens.tolist(), tol, skip=skip)
-    compare_slots(pool, op, list(range(16)), tol)
+    compare_outputs(out, oo, b.cu_seqlens.tolist(), TOL_F32, skip=skip)
+    compare_slots(pool, op, list(range(16)), TOL_F32)
     o = np64(out)
     for r in skip:
         a, e = int(b.cu_seqlens[r]), int(b.cu_seqlens[r + 1])
