@@ -18,8 +18,9 @@ no collective on the data path (requests and their slots are independent),
 so the aggregate is the sum over ranks ("scaling": "weak"); time is the max
 over ranks.
 
---impl reference times the CPU oracle (the plain fp64 recurrence) on a
-bounded sample of the same workload on the host cores.
+--impl reference times the oracle's plain C restatement (float32, every
+host thread) on a bounded sample of the same workload; each workload line
+also carries that CPU baseline on a sample of its own inputs.
 """
 
 from __future__ import annotations
@@ -657,7 +658,7 @@ def reduce_over_ranks(rank_ms, units_per_rank, world, device):
     return rank_ms, units_per_rank * world / (rank_ms / 1e3)
 
 
-def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=False):
+def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=False, cpu=False):
     wl = make_workload(name, L, dev)
     # decode rotates 4 pool replicas: a replica's 108 MB working set is never
     # L2-resident when it comes back, so no flush is needed (a written flush
@@ -696,6 +697,8 @@ def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=Fals
                                         dist_info["world"], dev)
         res["e2e"] = {"value": e_val, "unit": wl.unit,
                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e_ms}
+    if cpu and name in CPU_LEGS:
+        res["cpu_baseline"] = CPU_LEGS[name](wl)
     del wl
     torch.cuda.empty_cache()
     return res
@@ -765,61 +768,190 @@ def measured_traffic(workload):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle legs
+# CPU baseline: the C restatement of the oracle (oracle/lin_state_ref.c) in
+# float32 on every host thread, on a bounded sample of each workload's own
+# inputs. A baseline beside the GPU figures, not a target.
 # ---------------------------------------------------------------------------
-def oracle_prefill_sample(seconds_budget=15.0):
-    """The oracle on a bounded sample of the headline workload: its 4096-token
-    requests one after another (all 32 heads), 64 tokens at a time, until the
-    time budget is spent."""
-    from oracle import lin_state_oracle as O
-    try:
-        from threadpoolctl import threadpool_limits
-        lim = threadpool_limits(1)
-    except Exception:  # noqa: BLE001
-        lim = None
-    dims = W.QWEN35_GDN
-    n = 4096
-    done, nreq, dt = 0, 0, 0.0  # dt: oracle time only (input generation is not timed)
-    step = 64
-    while nreq < 8 and dt < seconds_budget:
-        b = W.make_prefill_batch(dims, [n], W.GATE_PER_HEAD, dtype=torch.bfloat16, seed=0,
-                                 gate="uniform", tag=f"{HEADLINE}.cpu{nreq}")
-        x, cw, g, beta = (t.double().numpy() for t in (b.x, b.conv_w, b.g, b.beta))
-        pool = O.make_pool(1, 4, 32, 128, 128, dims.conv_channels, state_dtype="f32", conv_dtype="bf16")
-        nreq += 1
-        pos = 0
-        t0 = time.perf_counter()
-        while pos < n and dt + (time.perf_counter() - t0) < seconds_budget:
-            m = min(step, n - pos)
-            O.prefill(pool, 0, x[pos:pos + m], cw, g[pos:pos + m], beta[pos:pos + m], [0, m],
-                      [pos], [1], [1 if pos else 0], [2, 3], [0, 2], 64, O.GATE_PER_HEAD,
-                      O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU, 1.0, "f32")
-            pos += m
-        dt += time.perf_counter() - t0
-        done += pos
-    if lim is not None:
-        lim.unregister() if hasattr(lim, "unregister") else None
-    return {"value": done / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} tokens of the headline workload ({nreq} of its 4096-token requests, "
-                      f"all 32 heads), fp64 numpy oracle, {dt:.1f} s"}
+def _host_f32(t):
+    import numpy as np
+    return np.ascontiguousarray(t.detach().to(torch.float32).cpu().numpy())
+
+
+def _rname(dtype):
+    return "bf16" if dtype == torch.bfloat16 else "f32"
+
+
+def _cpu_result(value, unit, sample, seconds):
+    from oracle import lin_state_ref as R
+    return {"value": value, "unit": unit, "cores": R.host_threads(), "cpu_model": R.cpu_model(),
+            "kind": "oracle", "precision": "f32",
+            "sample": f"{sample}; C restatement of the oracle, float32, {R.host_threads()} threads, "
+                      f"{seconds:.2f} s"}
+
+
+def cpu_prefill(wl, max_tokens):
+    """Requests of the prefill workload in batch order (the first request cut
+    at max_tokens if it alone is longer) until max_tokens extend tokens, all
+    heads, with the workload's snapshots, dtypes and flags."""
+    import numpy as np
+    from oracle import lin_state_ref as R
+    b = wl.b
+    cu = b.cu_seqlens.tolist()
+    n = 0
+    while n < wl.B and cu[n + 1] - cu[0] <= max_tokens:
+        n += 1
+    if n == 0:  # one request longer than the sample: its first max_tokens tokens
+        n, cu_s = 1, [0, max_tokens]
+    else:
+        cu_s = cu[:n + 1]
+    T = cu_s[-1]
+    x, g, beta = (_host_f32(t[:T]) for t in (b.x, b.g, b.beta))
+    cw = _host_f32(b.conv_w)
+    ctr = wl.cu_track.tolist()[:n + 1]
+    # the sample's live and track slots, gathered into a compact host pool
+    slots, tracks = wl.slot.tolist()[:n], wl.track.tolist()[:ctr[-1]]
+    used = sorted(set(slots) | set(t for t in tracks if t >= 0))
+    remap = {s_: i for i, s_ in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=wl.pool.temporal.device)
+    temporal = _host_f32(wl.pool.temporal[0].index_select(0, idx))
+    conv = _host_f32(wl.pool.conv[0].index_select(0, idx))
+    out = np.zeros((T,) + tuple(wl.out.shape[1:]), np.float32)
+    args = (temporal, conv, x, cw, g, beta, cu_s, b.prefix_len.tolist()[:n], [remap[s_] for s_ in slots],
+            b.has_initial_state.tolist()[:n], [remap[t] if t >= 0 else -1 for t in tracks], ctr,
+            wl.track_stride, b.gate_mode,
+            wl.kw["flags"], 1.0, out, _rname(wl.pool.temporal.dtype), _rname(wl.pool.conv.dtype),
+            _rname(wl.out.dtype))
+    t0 = time.perf_counter()
+    st = R.prefill_arrays("f32", *args)
+    dt = time.perf_counter() - t0
+    assert st == 0, st
+    return _cpu_result(T / dt, "tok/s", f"{n} request(s), {T} tokens x {b.dims.num_heads} heads of the "
+                       f"workload", dt)
+
+
+def cpu_decode(wl, rounds):
+    """`rounds` steps of the decode / verify workload on all 256 requests, its
+    slots gathered into a compact host pool (live slots, then track slots)."""
+    import numpy as np
+    from oracle import lin_state_ref as R
+    B = wl.B
+    slots, tracks = wl.slot.tolist(), wl.track.tolist()
+    idx = torch.tensor(slots + tracks, dtype=torch.long, device=wl.pools[0].temporal.device)
+    temporal = _host_f32(wl.pools[0].temporal[0].index_select(0, idx))
+    conv = _host_f32(wl.pools[0].conv[0].index_select(0, idx))
+    cs, ct = list(range(B)), list(range(B, 2 * B))
+    cw = _host_f32(wl.conv_w)
+    ins = [tuple(_host_f32(t) for t in wl.inputs[k % len(wl.inputs)]) for k in range(rounds)]
+    D = wl.n_draft
+    out = np.zeros((B, D, 12, 128), np.float32)
+    spec_t = spec_c = None
+    if D > 1 and not wl.replay:
+        spec_t = np.zeros((B, D, 12, 128, 128), np.float32)
+        spec_c = np.zeros((B, D, wl.dims.conv_channels, 3), np.float32)
+    acc = wl.acc.tolist() if D > 1 else None
+    pos0 = wl.pos0.tolist()
+    flags = 3  # L2 norm + SiLU, as the workload
+    t0 = time.perf_counter()
+    for k in range(rounds):
+        x, g, beta = ins[k]
+        pos = [p + k for p in pos0]
+        if D == 1:
+            st = R.decode_arrays("f32", temporal, conv, x, cw, g, beta, cs, pos, ct, 256, 1, flags,
+                                 1.0, out, "bf16", "bf16", "bf16")
+        elif not wl.replay:
+            st = R.decode_arrays("f32", temporal, conv, x, cw, g, beta, cs, pos, None, 0, 1, flags,
+                                 1.0, out, "bf16", "bf16", "bf16", spec_t, spec_c)
+            R.commit_arrays("f32", temporal, conv, cs, pos, acc, ct, 256, spec_t, spec_c)
+        else:
+            # verify with outputs only, then the accepted tokens again into the slot
+            st = R.decode_arrays("f32", temporal, conv, x, cw, g, beta, cs, pos, None, 0, 1, flags,
+                                 1.0, out, "bf16", "bf16", "bf16")
+            o1 = np.zeros((B, 1, 12, 128), np.float32)
+            for j in range(D):
+                sl = [s if acc[r] > j else -1 for r, s in enumerate(cs)]
+                R.decode_arrays("f32", temporal, conv, np.ascontiguousarray(x[:, j:j + 1]), cw,
+                                np.ascontiguousarray(g[:, j:j + 1]),
+                                np.ascontiguousarray(beta[:, j:j + 1]), sl,
+                                [p + j for p in pos], ct, 256, 1, flags, 1.0, o1, "bf16", "bf16",
+                                "bf16")
+        assert st == 0, st
+    dt = time.perf_counter() - t0
+    what = "steps" if D == 1 else "verify rounds"
+    unit_val = (B * rounds / dt) if D == 1 else (rounds / dt)
+    return _cpu_result(unit_val, wl.unit, f"{rounds} {what} of all {B} requests x 12 heads", dt)
+
+
+def cpu_copy(wl, pairs_per_batch=16, batches=3):
+    """Slot copies of the copy workload's batches (the first `pairs_per_batch`
+    pairs of each) as a threaded memcpy gather over a compact host pool of the
+    same 69-layer slot layout."""
+    import numpy as np
+    from oracle import lin_state_ref as R
+    H, K, C = 12, 128, W.KIMI_K3_TP8.conv_channels
+    nslot = 2 * pairs_per_batch
+    t_host = np.zeros((wl.layers, nslot, H * K * K), np.uint16)
+    c_host = np.zeros((wl.layers, nslot, C * 3), np.uint16)
+    src = list(range(pairs_per_batch))
+    dst = list(range(pairs_per_batch, nslot))
+    R.copy_slots_bytes(t_host, src, dst)  # first touch of every page
+    R.copy_slots_bytes(c_host, src, dst)
+    t0 = time.perf_counter()
+    for _ in range(batches):
+        R.copy_slots_bytes(t_host, src, dst)
+        R.copy_slots_bytes(c_host, src, dst)
+    dt = time.perf_counter() - t0
+    moved = 2.0 * batches * pairs_per_batch * wl.slot_bytes
+    return _cpu_result(moved / dt / 1e9, "GB/s", f"{batches} batches of {pairs_per_batch} slot copies "
+                       f"over {wl.layers} layers (29,039,616 B per slot), read + write counted", dt)
+
+
+CPU_LEGS = {
+    "qwen35_gdn_prefill": lambda wl: cpu_prefill(wl, 16384),
+    "mamba2_ssd_prefill": lambda wl: cpu_prefill(wl, 16384),
+    "kimi_k3_kda_varlen_prefill": lambda wl: cpu_prefill(wl, 40000),
+    "kda_long_prefill_131k": lambda wl: cpu_prefill(wl, 24576),
+    "kda_decode": lambda wl: cpu_decode(wl, 8),
+    "kda_spec_verify4_commit": lambda wl: cpu_decode(wl, 3),
+    "kda_spec_verify4_replay": lambda wl: cpu_decode(wl, 3),
+    "slot_copy_kimi_k3_69l": cpu_copy,
+    "slot_copy_kimi_k3_8l": cpu_copy,
+}
 
 
 def reference_arm(args, dist_info):
+    """The oracle as the reference arm: the C restatement in float32 on every
+    host thread, one 4096-token request of the headline workload (all 32
+    heads) per step."""
     if dist_info["rank"] != 0:
         return
+    import numpy as np
+    from oracle import lin_state_ref as R
     steps = max(1, args.steps)
-    vals = []
+    dims = W.QWEN35_GDN
+    b = W.make_prefill_batch(dims, [4096], W.GATE_PER_HEAD, dtype=torch.bfloat16, seed=0,
+                             gate="uniform", tag=f"{HEADLINE}.ref")
+    x, cw, g, beta = (_host_f32(t) for t in (b.x, b.conv_w, b.g, b.beta))
+    temporal = np.zeros((4, 32, 128, 128), np.float32)
+    conv = np.zeros((4, dims.conv_channels, 3), np.float32)
+    out = np.zeros((4096, 32, 128), np.float32)
+
+    def one():
+        t0 = time.perf_counter()
+        R.prefill_arrays("f32", temporal, conv, x, cw, g, beta, [0, 4096], [0], [1], [0], [2, 3],
+                         [0, 2], 64, W.GATE_PER_HEAD, 3, 1.0, out, "f32", "bf16", "f32")
+        return time.perf_counter() - t0
+
     for _ in range(max(0, min(args.warmup, 1))):
-        oracle_prefill_sample(2.0)
-    for _ in range(steps):
-        vals.append(oracle_prefill_sample(max(2.0, 60.0 / steps))["value"])
-    v = statistics.median(vals)
-    cb = oracle_prefill_sample(2.0)
-    cb["value"] = v
+        one()
+    times = [one() for _ in range(steps)]
+    dt = statistics.median(times)
+    v = 4096 / dt
+    cb = _cpu_result(v, "tok/s", "one 4096-token request of the headline workload (32 heads) per step",
+                     sum(times))
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s",
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * 64 / v, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "ms_per_step": 1e3 * dt, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": CONFIG_TEXT[HEADLINE], "sample": cb["sample"]},
             "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -866,22 +998,20 @@ def main():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+        # each workload's CPU baseline runs after its GPU legs (the headline's
+        # after its end-to-end leg: host allocations made before that leg
+        # slowed its host-device copies), on rank 0 of a single-GPU run
+        cpu = rank == 0 and world == 1 and not args.no_cpu
         if i == 0:
             with ClockSampler(local) as cs:
                 results[n] = run_workload(n, L, dev, args.steps, args.warmup, peaks, stream,
-                                          dist_info, e2e=True)
+                                          dist_info, e2e=True, cpu=cpu)
             clocks = cs.summary()
         else:
             results[n] = run_workload(n, L, dev, max(3, args.steps), args.warmup, peaks, stream,
-                                      dist_info)
+                                      dist_info, cpu=cpu)
     if world > 1:
         torch.distributed.barrier()
-    # the CPU oracle leg runs after the GPU workloads: before them, its host
-    # allocations were followed by slower host-device copies in the
-    # end-to-end leg (13.5 against 5.5 ms per step)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = oracle_prefill_sample()
     head = results[names[0]]
     if rank == 0:
         line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
@@ -896,7 +1026,7 @@ def main():
                                  "4 pool replicas (432 MB touched per rotation) so no step finds its "
                                  "state in L2"},
                 "roofline": {**head["roofline"], "peak_source": peaks["source"]},
-                "cpu_baseline": cpu,
+                "cpu_baseline": head.get("cpu_baseline"),
                 "e2e": head.get("e2e"),
                 "gpu_launches": head["gpu_launches"],
                 "clocks": clocks,
