@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblinstate.so")
 
-SOURCES = ["api.cu", "copy_kernels.cu", "token_kernels.cu", "chunked_prefill.cu", "selftest.cu"]
+SOURCES = ["api.cu", "copy_kernels.cu", "token_kernels.cu", "chunked_prefill.cu", "verify_chunk.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

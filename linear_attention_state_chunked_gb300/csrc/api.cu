@@ -264,7 +264,20 @@ int lin_state_decode(const lin_state_pool_t* pool, const lin_decode_args_t* a, v
   if (lin::decode_stage_bytes(*pool, *a) > lin::kDecodeMaxStage)
     return fail(LIN_EUNSUPPORTED, "decode: n_draft %d stages %d bytes per (request, head), over %d",
                 a->n_draft, lin::decode_stage_bytes(*pool, *a), lin::kDecodeMaxStage);
-  cudaError_t e = lin::launch_decode(*pool, *a, nullptr, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (a->n_draft > 1 && spec_less) {
+    // outputs only: the drafts as one chunk from the slot state
+    if (a->n_draft > lin::kVerifyChunkMaxDraft)
+      return fail(LIN_EUNSUPPORTED, "decode: a verify without a spec buffer takes at most %d drafts, not %d",
+                  lin::kVerifyChunkMaxDraft, a->n_draft);
+    if (lin::verify_chunk_smem(*pool, *a) > 220 * 1024)
+      return fail(LIN_EUNSUPPORTED, "decode: n_draft %d needs %d bytes of shared memory per (request, head)",
+                  a->n_draft, lin::verify_chunk_smem(*pool, *a));
+    e = lin::launch_verify_chunk(*pool, *a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "lin_state_decode launch");
+    return ok();
+  }
+  e = lin::launch_decode(*pool, *a, nullptr, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "lin_state_decode launch");
   return ok();
 }

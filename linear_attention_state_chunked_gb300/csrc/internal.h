@@ -8,7 +8,7 @@
 
 namespace lin {
 
-inline int dtype_size(int dt) { return dt == LIN_BF16 ? 2 : 4; }
+__host__ __device__ inline int dtype_size(int dt) { return dt == LIN_BF16 ? 2 : 4; }
 
 // Devices a process may address through the per-device caches below.
 constexpr int kMaxDevices = 64;
@@ -41,6 +41,13 @@ cudaError_t launch_decode(const lin_state_pool_t& pool, const lin_decode_args_t&
 cudaError_t launch_prefill_recurrent(const lin_state_pool_t& pool,
                                      const lin_prefill_args_t& a, cudaStream_t stream,
                                      const uint32_t* redo = nullptr);
+
+// Outputs-only verify as one chunk of drafts (verify_chunk.cu): the drafts'
+// outputs from the slot state with the state carried in fp32 across them.
+constexpr int kVerifyChunkMaxDraft = 32;
+int verify_chunk_smem(const lin_state_pool_t& pool, const lin_decode_args_t& a);
+cudaError_t launch_verify_chunk(const lin_state_pool_t& pool, const lin_decode_args_t& a,
+                                cudaStream_t stream);
 
 // Chunked tensor-core prefill (chunked_prefill.cu).
 bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_args_t& a);

@@ -319,12 +319,12 @@ __device__ __forceinline__ bool consumers_sync_or(int nthreads, bool pred) {
 }
 
 // MODE: kDecStates (one token in place), kDecVerify (a chain of drafts into
-// the spec buffer), kDecOutputsOnly (a chain verify without per-step states),
-// kDecReplay (the commit form: accepted tokens per request, in place, no
-// outputs), kDecTree (verify into the spec buffer where draft j starts from
-// the state after draft parent[r][j], -1: the slot's).
+// the spec buffer), kDecReplay (the commit form: accepted tokens per request,
+// in place, no outputs), kDecTree (verify into the spec buffer where draft j
+// starts from the state after draft parent[r][j], -1: the slot's). A chain
+// verify without per-step states runs as one chunk (verify_chunk.cu).
 // All but the one-token mode run the drafts in groups (see the consumer loop).
-enum DecMode { kDecStates = 0, kDecOutputsOnly = 1, kDecReplay = 2, kDecTree = 3, kDecVerify = 4 };
+enum DecMode { kDecStates = 0, kDecReplay = 2, kDecTree = 3, kDecVerify = 4 };
 constexpr int kDecMaxTree = 32;  // drafts per request in a tree verify
 constexpr int kDecGroup = 4;     // drafts per group in the draft modes
 // Dynamic shared memory of one decode CTA: at most the opt-in limit (227 KB)
@@ -1145,10 +1145,9 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
                           const int32_t* accept, cudaStream_t stream) {
   const int mode = accept ? kDecReplay
                    : (a.n_draft > 1 && a.parent && a.spec.temporal) ? kDecTree
-                   : (a.n_draft > 1 && !a.spec.temporal) ? kDecOutputsOnly
                    : a.n_draft > 1                        ? kDecVerify
                                                           : kDecStates;
-  static DecodeLaunchCache caches[5];  // one per DecMode
+  static DecodeLaunchCache caches[5];  // indexed by DecMode
   DecodeLaunchCache& cache = caches[mode];
   DecodeParams p{pool, a, accept};
   const int stage = decode_stage_bytes(pool, a);
@@ -1172,7 +1171,6 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
   }
   auto kern = mode == kDecReplay        ? decode_kernel<D, V, ST, kDecReplay>
               : mode == kDecTree        ? decode_kernel<D, V, ST, kDecTree>
-              : mode == kDecOutputsOnly ? decode_kernel<D, V, ST, kDecOutputsOnly>
               : mode == kDecVerify      ? decode_kernel<D, V, ST, kDecVerify>
                                         : decode_kernel<D, V, ST, kDecStates>;
   int dev = 0;

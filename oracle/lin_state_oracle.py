@@ -35,6 +35,10 @@ What it computes, token by token and in the order the pages state it:
 * Speculative verify into a per-step buffer with the main slot untouched,
   then commit main = buffer[accepted - 1].
   -- MambaRadixCache page sections 8.3, 8.4, 8.6.
+* A verify that keeps no per-step states writes only the drafts' outputs,
+  carrying the state unrounded across the drafts (nothing is stored between
+  them); its commit re-runs the accepted prefix.
+  -- Kimi-K3 notes, "ReplaySSM"; MambaRadixCache page sections 9.2 - 9.10.
 * Slot copies (fork / COW) and restore with has_initial_state.
   -- MambaRadixCache page section 3.2 (copy_from);
      Qwen3.5 Linear-State Prefix Cache sections 6.1, 6.4.
@@ -45,7 +49,9 @@ input; conv tap w[c][3] multiplies the current token; no conv bias; optional
 SiLU after the conv; q and k L2-normalised per head with eps = 1e-6 inside the
 square root; q scaled by q_scale after normalisation; the state is rounded to
 the pool's storage dtype only where it is written to memory (prefill) or after
-every token (decode and verify, which read and write the pool per token).
+every token (decode and verify, which read and write the pool per token); a
+verify without per-step states stores nothing between drafts, so it carries
+the state unrounded, as a prefill does.
 
 Storage dtypes: "f32", "bf16", or "f64" (no rounding; used by the pins).
 """
@@ -324,6 +330,41 @@ def decode(pool, layer, x, conv_w, g, beta, slot, pos, track_slot,
             else:
                 spec["temporal"][layer, r, j] = S
                 spec["conv"][layer, r, j] = cw
+    return out, status
+
+
+def verify_outputs(pool, layer, x, conv_w, g, beta, slot, gate_mode, flags, q_scale=1.0,
+                   out_dtype="f32", out=None):
+    """Outputs of a verify that keeps no per-step states: the replay form of
+    speculative decoding (Kimi-K3 notes, "ReplaySSM"; MambaRadixCache page
+    9.2 - 9.10), whose commit re-runs the accepted prefix later.
+
+    x [B][D][C]; g [B][D][H] or [B][D][H][K]; beta [B][D][H]. The D drafts of
+    request r run in order from the state and window in slot[r]. Nothing is
+    stored between drafts, so the state is carried unrounded across them, as
+    inside a prefill call (only the outputs are written, rounded to
+    out_dtype). The pool is not modified. Returns (out [B][D][H][V], status).
+    """
+    temporal, conv = pool["temporal"], pool["conv"]
+    num_slots = temporal.shape[1]
+    H, V, K = temporal.shape[2], temporal.shape[3], temporal.shape[4]
+    B, D = x.shape[0], x.shape[1]
+    if out is None:
+        out = np.zeros((B, D, H, V), np.float64)
+    status = 0
+    for r in range(B):
+        s = int(slot[r])
+        if s < 0:
+            continue
+        if not _in_range(s, num_slots):
+            status |= ST_BAD_SLOT
+            continue
+        S = temporal[layer, s].copy()
+        cw = conv[layer, s].copy()
+        for j in range(D):
+            S, cw, o = token_step(S, cw, x[r, j], conv_w, g[r, j], beta[r, j],
+                                  H, K, V, gate_mode, flags, q_scale)
+            out[r, j] = round_to(o, out_dtype)
     return out, status
 
 

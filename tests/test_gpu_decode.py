@@ -208,8 +208,10 @@ def test_decode_and_verify_many_items_per_cta():
                                       (torch.float32, L.LIN_GATE_PER_HEAD)])
 def test_replay_commit_equals_spec_commit(sdt, gate):
     """The replay form of speculative decoding ([K3] ReplaySSM, [MRC] 9): a
-    verify that keeps no per-step states writes the same outputs, bit for bit,
-    as one that does, and re-running the accepted prefix into the slot leaves
+    verify that keeps no per-step states writes the drafts' outputs with the
+    state carried unrounded across them (the oracle's outputs-only verify; the
+    per-step verify's outputs within the pool dtype's rounding), and
+    re-running the accepted prefix into the slot leaves
     every slot and track slot bit-identical to committing from the per-step
     buffer; both match the oracle. Accept lengths 0 .. D, boundary crossings
     at 256, a padding request, layer 1 of a 2-layer pool."""
@@ -233,7 +235,11 @@ def test_replay_commit_equals_spec_commit(sdt, gate):
                   gate_mode=gate, flags=FLAGS)
     L.lin_state_decode(pa, out=oa, spec=spec, **common)
     L.lin_state_decode(pb, out=ob, **common)  # no spec buffer: outputs only
-    assert torch.equal(oa, ob)
+    # the outputs-only verify carries the state unrounded across its drafts
+    ov, ost = O.verify_outputs(op, 1, np64(x), np64(conv_w), np64(g), np64(beta), slots, gate, FLAGS)
+    assert ost == 0
+    assert max_rel_per_head(np64(ob), ov, 2) < TOL_F32
+    assert max_rel_per_head(np64(ob), np64(oa), 2) < (TOL_F32 if sdt == torch.float32 else TOL_BF16)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     L.lin_state_spec_commit(pa, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
                             n_draft=ND, track_slot=_i32(track), track_interval=256, layer_begin=1,
@@ -362,8 +368,9 @@ def test_decode_status_bits():
     (128, torch.float32, torch.float32, 17, L.LIN_GATE_PER_KEY),    # the staging limit: smaller groups
 ])
 def test_long_chains_in_groups(D, sdt, io, ND, gate):
-    """Chains longer than one group of drafts: verify with and without a
-    per-step buffer (same outputs bit for bit), buffer commit and replay commit
+    """Chains longer than one group of drafts: verify with a per-step buffer
+    and without one (the latter against the oracle's outputs-only verify),
+    buffer commit and replay commit
     (same pools bit for bit), both equal to running the accepted tokens as
     single-token decodes, bit for bit, and to the oracle. Accept lengths span
     the groups; positions cross the 256 boundary inside later groups."""
@@ -391,7 +398,10 @@ def test_long_chains_in_groups(D, sdt, io, ND, gate):
     L.lin_state_decode(pa, out=oa, spec=spec, status=st, **common)
     L.lin_state_decode(pb, out=ob, status=st, **common)
     assert L.lin_state_read_status(st) == 0
-    assert torch.equal(oa, ob)
+    # without a spec buffer: the drafts as one chunk, the state unrounded across them
+    ov, _ = O.verify_outputs(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots, gate, FLAGS)
+    assert max_rel_per_head(np64(ob), ov, 2) < TOL_F32
+    assert max_rel_per_head(np64(ob), np64(oa), 2) < (TOL_F32 if sdt == torch.float32 else TOL_BF16)
     L.lin_state_spec_commit(pa, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
                             n_draft=ND, track_slot=_i32(track), track_interval=256, status=st)
     L.lin_state_replay_commit(pb, layer=0, x=x, conv_w=conv_w, g=g, beta=beta, slot=_i32(slots),

@@ -206,8 +206,14 @@ def test_kda_verify4_replay_full_size_sampled():
                          [slot], [pos], None, 0, O.GATE_PER_KEY, FLAGS, 1.0, "bf16", spec=ospec)
         assert st == 0
         got = np64(wl.out[req][:, heads])
+        # the outputs-only verify: the state unrounded across the drafts
+        ov, _ = O.verify_outputs(pool, 0, np64(x[req:req + 1])[:, :, ch], np64(wl.conv_w)[ch],
+                                 np64(g[req:req + 1])[:, :, heads],
+                                 np64(beta[req:req + 1])[:, :, heads], [slot], O.GATE_PER_KEY,
+                                 FLAGS, 1.0, "bf16")
         for k in range(2):
             assert rel_l2(got[:, k], o[0, :, k]) <= TOL_BF16
+            assert rel_l2(got[:, k], ov[0, :, k]) <= TOL_BF16
         O.spec_commit(pool, ospec, 0, 1, [slot], [pos], [acc[req]], [ts], 256, 4)
         gt = np64(wl.pools[0].temporal[0, slot][heads])
         for k in range(2):

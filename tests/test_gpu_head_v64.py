@@ -107,8 +107,8 @@ def test_decode_head_v64(sdt, gate, flags):
 
 
 def test_verify_replay_and_spec_commit_head_v64():
-    """Verify 4 drafts into a per-step buffer and without one (identical
-    outputs), commit from the buffer on one pool and replay the accepted
+    """Verify 4 drafts into a per-step buffer and without one (against the
+    oracle's outputs-only verify, the state unrounded across the drafts), commit from the buffer on one pool and replay the accepted
     prefix on the other: identical pools, equal to the oracle's verify and
     commit (bf16 state, per-key gates)."""
     ND, B, S = 4, 5, 16
@@ -129,7 +129,10 @@ def test_verify_replay_and_spec_commit_head_v64():
                   gate_mode=L.LIN_GATE_PER_KEY, flags=GDN)
     L.lin_state_decode(pa, out=oa, spec=spec, **common)
     L.lin_state_decode(pb, out=ob, **common)
-    assert torch.equal(oa, ob)
+    ov, _ = O.verify_outputs(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots,
+                             O.GATE_PER_KEY, GDN)
+    assert max_rel_per_head(np64(ob), ov, 2) < TOL_F32
+    assert max_rel_per_head(np64(ob), np64(oa), 2) < TOL_BF16
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     L.lin_state_spec_commit(pa, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
                             n_draft=ND, track_slot=_i32(track), track_interval=256, status=st)

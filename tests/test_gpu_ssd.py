@@ -135,8 +135,8 @@ def test_ssd_decode_vs_oracle(D):
 
 
 def test_ssd_verify_replay_and_spec_commit():
-    """Verify 4 drafts with and without a per-step buffer (same outputs bit for
-    bit), then commit from the buffer on one pool and replay the accepted
+    """Verify 4 drafts with a per-step buffer and without one (against the
+    oracle's outputs-only verify), then commit from the buffer on one pool and replay the accepted
     prefix on the other: identical slots and track slots, equal to the
     oracle's verify + commit."""
     H, D, ND, B, S = 2, 128, 4, 5, 16
@@ -160,7 +160,10 @@ def test_ssd_verify_replay_and_spec_commit():
                   gate_mode=L.LIN_GATE_PER_HEAD, flags=FLAGS)
     L.lin_state_decode(pa, out=oa, spec=spec, **common)
     L.lin_state_decode(pb, out=ob, **common)
-    assert torch.equal(oa, ob)
+    ov, _ = O.verify_outputs(op, 0, np64(x), np64(conv_w), np64(g), np64(beta), slots,
+                             O.GATE_PER_HEAD, FLAGS)
+    assert max_rel_per_head(np64(ob), ov, 2) < TOL_F32
+    assert max_rel_per_head(np64(ob), np64(oa), 2) < TOL_BF16
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     L.lin_state_spec_commit(pa, spec=spec, slot=_i32(slots), pos=_i32(pos), accept_len=_i32(acc),
                             n_draft=ND, track_slot=_i32(track), track_interval=256, status=st)

@@ -443,6 +443,48 @@ def test_spec_commit_equals_sequential_decode(dtype):
                 assert np.all(pa["temporal"][0, 3] == -1)
 
 
+@pytest.mark.parametrize("gate_mode", [O.GATE_PER_HEAD, O.GATE_PER_KEY])
+def test_verify_outputs_is_a_prefill_of_the_drafts(gate_mode):
+    """A verify that keeps no per-step states (Kimi-K3 notes "ReplaySSM";
+    MambaRadixCache page 9.2 - 9.10) carries the state unrounded across its
+    drafts: on a bf16 pool its outputs equal those of a prefill of the same
+    tokens from the slot (which carries the state unrounded inside the call,
+    storing nothing); with unrounded storage they equal the per-step verify's
+    outputs (whose per-token rounding is then the identity), and with bf16
+    storage they differ from them only by that rounding. The pool is left
+    as it was."""
+    H, K, V, D = 2, 8, 6, 5
+    C = 2 * H * K + H * V
+    r = rng(43)
+    w = r.standard_normal((C, 4)) * 0.5
+    x = O.round_to(r.standard_normal((2, D, C)), "bf16")
+    g = -np.log1p(np.exp(r.standard_normal((2, D, H) if gate_mode == O.GATE_PER_HEAD else (2, D, H, K))))
+    b = 1 / (1 + np.exp(-r.standard_normal((2, D, H))))
+    f = O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU
+    for dtype in ("bf16", "f64"):
+        pool = O.make_pool(1, 5, H, K, V, C, state_dtype=dtype, conv_dtype=dtype)
+        pool["temporal"][0, 1:3] = O.round_to(r.standard_normal((2, H, V, K)) * 0.2, dtype)
+        pool["conv"][0, 1:3] = O.round_to(r.standard_normal((2, C, 3)), dtype)
+        before = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in pool.items()}
+        out, st = O.verify_outputs(pool, 0, x, w, g, b, [1, 2], gate_mode, f)
+        assert st == 0
+        assert np.array_equal(pool["temporal"], before["temporal"])
+        assert np.array_equal(pool["conv"], before["conv"])
+        for req in range(2):
+            pp = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in before.items()}
+            op, _ = O.prefill(pp, 0, x[req], w, g[req], b[req], [0, D], [0], [1 + req], [1], [],
+                              [0, 0], 0, gate_mode, f)
+            assert np.array_equal(op, out[req])
+        pv = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in before.items()}
+        spec = O.make_spec_buffer(1, 2, D, H, K, V, C)
+        ov, _ = O.decode(pv, 0, x, w, g, b, [1, 2], [0, 0], None, 0, gate_mode, f, spec=spec)
+        if dtype == "f64":
+            assert np.array_equal(ov, out)
+        else:
+            assert not np.array_equal(ov, out)
+            assert np.linalg.norm(ov - out) <= 2e-2 * np.linalg.norm(out)
+
+
 # a draft tree in the shape of the MambaRadixCache page's example (9.6): two
 # roots, children of both, a grandchild; parent index per draft, -1 = the slot
 TREE_PARENT = [-1, -1, 0, 0, 1, 2, 2, 5]
