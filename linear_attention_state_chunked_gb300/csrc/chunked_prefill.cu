@@ -16,18 +16,22 @@
 //     P[t][i] = sum_c q_tc k_ic exp(b_tc - b_ic)          (i <= t)
 //     O       = (gamma . Q) S0^T + P U
 //     S_end   = S0 Diag(gamma_last) + U^T ((gamma_last / gamma) . K)
-// Every product runs with V (= 128) as the MMA M dimension, so the state row v
-// is TMEM lane v and all MMAs are M = 128 (cta_group::1):
+// Since U = U' - W S0^T = T (V - Khat S0^T), the correction by the incoming
+// state is applied to V before the solve's result is used: V' = V - Khat S0^T
+// needs only S0 and gamma . K, so it runs next to MMA1 while the solve does,
+// and W is never formed. Every product runs with V (= 128) as the MMA M
+// dimension, so the state row v is TMEM lane v and all MMAs are M = 128
+// (cta_group::1):
 //     MMA1  [A';P'] = [K_l;Q_l] K_r^T            N = 64,  K = 128
-//     MMA2  W^T = Khat^T T^T,  U'^T = V^T T^T     N = 64,  K = 64
-//     MMA3  U^T = U'^T + S0 (-W)^T                N = 64,  K = 128
+//     MMAV  V'^T = V^T + S0 (-Khat)^T             N = 64,  K = 128 (from V^T in TMEM)
+//     MMA2  U^T = V'^T T^T                        N = 64,  K = 64
 // (MMA4a needs only S0 and gamma . Q, so it is issued right after MMA1 and runs
 // while the solve does; MMA4b accumulates onto it.)
 //     MMA4  O^T = S0 Qhat^T + U^T P^T             N = 64,  K = 128 + 64
 //     MMA5  S   = S0 Diag(gamma_last) + U^T Ktil  N = 128, K = 64
 // The additive (Mamba2 SSD) form S_t = S_{t-1} Diag(alpha_t) + beta_t v_t k_t^T of
 // the MambaRadixCache page (section 9.3) is the same with A = 0: T = Diag(beta),
-// U = U' (no W, no solve, no MMA3 term).
+// U = T V (no solve, no MMAV).
 // (KDA: K_l = k exp(b - b_ref), Q_l = q exp(b - b_ref), K_r = k exp(b_ref - b)
 // with b_ref the chunk's middle row, so no exponent leaves +-(half a chunk);
 // GDN: the scalar decay exp(b_t - b_i) is applied in fp32 to A' and P'.)
@@ -36,9 +40,11 @@
 // Operand precision follows the pool's state dtype:
 //   - fp32 pools (and every GDN pool): fp16 operands (10-bit mantissa; every
 //     decay-scaled factor stays within [0, 1]) with high / low splits on the
-//     products that set the error. KDA's MMA1 factors exp(+-(b - b_ref)) leave
-//     fp16 range, so that one product takes bf16 operands, split likewise
-//     (hi = bf16(x), lo = bf16(x - hi): 16 significant bits, fp32 range).
+//     products that set the error: T, V', P and U. GDN's MMA1 takes single
+//     fp16 operands (its products enter A and P with fp32 decay factors); KDA's
+//     MMA1 factors exp(+-(b - b_ref)) leave fp16 range, so that product takes
+//     bf16 operands with a split (hi = bf16(x), lo = bf16(x - hi): 16
+//     significant bits, fp32 range).
 //   - KDA with a bf16 pool: bf16 operands, single products (the pool itself
 //     holds 8 significant bits).
 // A KDA (request, head) whose decay leaves the factored range (some key
@@ -89,14 +95,15 @@ constexpr uint32_t OFF_YB = OFF_XD + 4 * XBS * 4;    //   after MMA1: fp32 A_10 
 constexpr uint32_t OFF_ZB = OFF_YB + 2 * XBS * 4;    //   after MMA1: fp32 A_BA X_A [32][ZS]
 constexpr uint32_t OFF_OSTG = 98304;            // epilogue: output tile for a TMA store (32 KB)
 constexpr uint32_t OFF_KR = 98304;              // K_r (KDA), 64 x 128
-constexpr uint32_t OFF_UTL = OFF_KR;            //   after MMA2: U^T low part (GDN), rows v
-constexpr uint32_t OFF_KH = 114688;             // gamma . K, rows i (MN-major A)
-constexpr uint32_t OFF_WW = OFF_KH;             //   after MMA2: -W, rows c (MN-major B)
-constexpr uint32_t OFF_VV = 131072;             // V, rows i (MN-major A)
-constexpr uint32_t OFF_UT = OFF_VV;             //   after MMA2: U^T (high), rows v (K-major A)
-constexpr uint32_t OFF_QH = 147456;             // gamma . Q, rows t (K-major B)
+constexpr uint32_t OFF_UTL = OFF_KR;            //   after MMA2: U^T low part (split products), rows v
+constexpr uint32_t OFF_KQH = 114688;            // [-gamma . K; gamma . Q], rows t and 64 + t (K-major B
+                                                // of MMAV and MMA4a: one N = 128 product), 128 x 128
+constexpr uint32_t OFF_VPT = OFF_KQH;           //   after MMAV: V'^T (high), rows v (K-major A of MMA2)
+constexpr uint32_t OFF_UT = OFF_KQH + 16384;    //   after MMA2: U^T (high), rows v (K-major A)
+constexpr uint32_t OFF_VV = 147456;             // V, rows t (read into TMEM for MMAV; MN-major A of the additive MMA2)
 constexpr uint32_t OFF_KT = 163840;             // (gamma_last/gamma) . K, rows i (MN-major B)
 constexpr uint32_t OFF_KRL = 180224;            // K_r low part (KDA with fp32 state), 64 x 128
+constexpr uint32_t OFF_VPTL = OFF_KRL;          //   after MMA1: V'^T low part (split products), rows v
 constexpr uint32_t OFF_WC = OFF_KRL + 16384;    // conv taps, fp32 [4][384] (tap-major)
 constexpr uint32_t OFF_HALO = OFF_WC + 6144;    // initial conv window, fp32 [3][384]
 constexpr uint32_t OFF_WTOT = OFF_HALO + 4608;  // per-warp gate sums, fp32 [16][128]
@@ -107,18 +114,18 @@ constexpr uint32_t OFF_CF = OFF_GLAST + 512;    // GDN column decay factors, fp3
 constexpr uint32_t OFF_WIN = OFF_CF + 256;      // last 3 inputs of chunks j even / odd, fp32 [2][3][384]
 constexpr uint32_t SMEM_USED = OFF_WIN + 2 * 3 * 384 * 4;
 // The next chunk's x tile (q | k | v parts of this head, 64 rows x 128 bf16
-// each, row-major) lands in the V / gamma.Q / K-tilde operand regions, which
+// each, row-major) lands in the V / K-tilde / K_r-low operand regions, which
 // are free once a chunk's last MMA has completed.
 constexpr uint32_t OFF_XT = OFF_VV;
-static_assert(OFF_QH == OFF_VV + 16384 && OFF_KT == OFF_QH + 16384, "x tile spans three regions");
+static_assert(OFF_KT == OFF_VV + 16384 && OFF_KRL == OFF_KT + 16384, "x tile spans three regions");
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_ZB + 32 * ZS * 4 <= OFF_KR, "solve scratch inside the low-part region");
 
 // Tensor-memory columns (all 512 of the SM; the kernel runs one CTA per SM).
 constexpr uint32_t COL_S = 0;    // state, fp32, lanes v
-constexpr uint32_t COL_R1 = 128; // [A';P'] -> U'^T -> U^T
-constexpr uint32_t COL_R2 = 192; // W^T
+constexpr uint32_t COL_R1 = 128; // [A';P'] -> U^T
+constexpr uint32_t COL_R2 = 192; // V^T -> V'^T
 constexpr uint32_t COL_RO = 256; // O^T (MMA4a is issued with MMA1)
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -386,6 +393,7 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr bool BF1 = KDA;           // operand type of MMA1 ([K_l; Q_l] K_r^T)
   extern __shared__ uint8_t dsm[];
   __shared__ uint64_t bar_mma;
+  __shared__ uint64_t bar_v;  // MMA-V' of the chunk (and MMA4a) completed
   __shared__ uint64_t bar_x;  // x tile of the next chunk landed
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -521,6 +529,7 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (tid == 0) {
     umma::mbar_init(&bar_mma, 1);
+    umma::mbar_init(&bar_v, 1);
     umma::mbar_init(&bar_x, 1);
     umma::mbar_fence_init();
     abort_sh = 0;
@@ -605,6 +614,7 @@ __global__ void __launch_bounds__(NT, 1)
     return abort_sh == 0;
   };
 
+  uint32_t ph_v = 0;
   // The x tile of the chunk starting at token r0 (thread 0): one TMA load per
   // q | k | v part, completing on bar_x.
   int x_issued = 0;
@@ -675,6 +685,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
+
     // the previous chunk's TMA stores must have read their staging tiles before
     // the conv writes operands over them (after the barrier in the gate sums)
     if (tid == 0) bulk_wait_read();
@@ -857,22 +868,15 @@ __global__ void __launch_bounds__(NT, 1)
           split4_bf(kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3], hi, lo);
           st_shared_v2(sb + OFF_KR + umma::rp_offset(t, c, 64), hi[0], hi[1]);
           st_shared_v2(sb + OFF_KRL + umma::rp_offset(t, c, 64), lo[0], lo[1]);
-        } else if (SPLIT) {
-          uint32_t hi[2], lo[2];
-          split4(kn[0], kn[1], kn[2], kn[3], hi, lo);
-          st_shared_v2(sb + OFF_KQ + umma::rp_offset(t, c, 128), hi[0], hi[1]);
-          st_shared_v2(sb + OFF_KQL + umma::rp_offset(t, c, 128), lo[0], lo[1]);
-          split4(qn[0], qn[1], qn[2], qn[3], hi, lo);
-          st_shared_v2(sb + OFF_KQ + umma::rp_offset(CH + t, c, 128), hi[0], hi[1]);
-          st_shared_v2(sb + OFF_KQL + umma::rp_offset(CH + t, c, 128), lo[0], lo[1]);
         } else {
           put4<BF1>(sb + OFF_KQ, 128, t, c, kn[0] * eL[0], kn[1] * eL[1], kn[2] * eL[2], kn[3] * eL[3]);
           put4<BF1>(sb + OFF_KQ, 128, CH + t, c, qn[0] * eL[0], qn[1] * eL[1], qn[2] * eL[2], qn[3] * eL[3]);
-          put4<BF1>(sb + OFF_KR, 64, t, c, kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3]);
+          if (KDA)
+            put4<BF1>(sb + OFF_KR, 64, t, c, kn[0] * eR[0], kn[1] * eR[1], kn[2] * eR[2], kn[3] * eR[3]);
         }
-        put4<BF>(sb + OFF_KH, 64, t, c, kn[0] * eH[0], kn[1] * eH[1], kn[2] * eH[2], kn[3] * eH[3]);
+        put4<BF>(sb + OFF_KQH, 128, t, c, -kn[0] * eH[0], -kn[1] * eH[1], -kn[2] * eH[2], -kn[3] * eH[3]);
+        put4<BF>(sb + OFF_KQH, 128, CH + t, c, qn[0] * eH[0], qn[1] * eH[1], qn[2] * eH[2], qn[3] * eH[3]);
         put4<BF>(sb + OFF_VV, 64, t, c, vv[0], vv[1], vv[2], vv[3]);
-        put4<BF>(sb + OFF_QH, 64, t, c, qn[0] * eH[0], qn[1] * eH[1], qn[2] * eH[2], qn[3] * eH[3]);
         put4<BF>(sb + OFF_KT, 64, t, c, kn[0] * eT[0], kn[1] * eT[1], kn[2] * eT[2], kn[3] * eT[3]);
       }
       if (KDA && __any_sync(0xffffffffu, range_bad) && lane == 0) range_sh = 1;
@@ -905,23 +909,22 @@ __global__ void __launch_bounds__(NT, 1)
           umma::mma_f16(tm + COL_R1, ah, bh, id1, k0 > 0);
           umma::mma_f16(tm + COL_R1, ah, umma::desc_kmajor(sb + OFF_KRL, 64, k0), id1, 1);
           umma::mma_f16(tm + COL_R1, al, bh, id1, 1);
-        } else if (SPLIT) {
-          const uint64_t al = umma::desc_kmajor(sb + OFF_KQL, 128, k0);
-          umma::mma_f16(tm + COL_R1, ah, ah, id1, k0 > 0);  // B: rows 0..63 of the same panels
-          umma::mma_f16(tm + COL_R1, ah, al, id1, 1);
-          umma::mma_f16(tm + COL_R1, al, ah, id1, 1);
-        } else {
+        } else if (KDA) {
           umma::mma_f16(tm + COL_R1, ah, umma::desc_kmajor(sb + OFF_KR, 64, k0), id1, k0 > 0);
+        } else {
+          umma::mma_f16(tm + COL_R1, ah, ah, id1, k0 > 0);  // B: rows 0..63 (K) of the same panels
         }
       }
       umma::mma_commit(&bar_mma);
-      // MMA4a: O^T = S0 Qhat^T (RO); completes before MMA2's commit fires
-      if (outputs_on) {
+      // the additive form has no MMAV: MMA4a alone, O^T = S0 Qhat^T (RO), B
+      // the Qhat rows of the [-Khat; Qhat] panels; it completes before MMA2's
+      // commit fires
+      if (outputs_on && additive) {
         constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
 #pragma unroll
         for (int k0 = 0; k0 < DH; k0 += 16)
           umma::mma_f16(tm + COL_RO, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
-                        umma::desc_kmajor(sb + OFF_QH, 64, k0), id4, k0 > 0);
+                        umma::desc_kmajor(sb + OFF_KQH + CH * 128, 128, k0), id4, k0 > 0);
       }
     }
     if (!KDA && tid >= 32 && tid < 96) {
@@ -932,9 +935,43 @@ __global__ void __launch_bounds__(NT, 1)
       const float d = SB[i & ~15] - SB[i];
       CF[i] = d <= 80.f ? __expf(d) : -1.f;
     }
+    if (!additive) {
+      // V^T (lanes v, columns t) into tensor memory: the accumulator MMAV
+      // starts from; zeros where MMA4a accumulates (the two run as one product)
+      float v16[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint16_t u = *reinterpret_cast<const uint16_t*>(sm + OFF_VV + umma::rp_offset(slice * 16 + k, vrow, 64));
+        v16[k] = BF ? __uint_as_float(static_cast<uint32_t>(u) << 16) : __half2float(__ushort_as_half(u));
+      }
+      umma::tmem_st16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), v16);
+      if (outputs_on) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v16[k] = 0.f;
+        umma::tmem_st16(tmem_addr(tm, quarter * 32, COL_RO + slice * 16), v16);
+      }
+      umma::fence_before_sync();
+    }
     if (j + 1 < nch) {
       const int n2 = (L - (j + 1) * CH) < CH ? (L - (j + 1) * CH) : CH;
       load_gates<KDA>(a, row0 + CH, n2, h, H, warp, lane, gk, bt);
+    }
+    if (!additive) {
+      __syncthreads();  // V^T is in tensor memory
+      if (tid == 0) {
+        // MMAV and MMA4a as one product S0 [-Khat; Qhat]^T into the adjacent
+        // columns R2 | RO: V'^T = V^T - S0 Khat^T (U = T V' below makes the
+        // delta-rule correction U = U' - W S0^T without forming W) and
+        // O^T = S0 Qhat^T; without outputs, MMAV alone
+        umma::fence_after_sync();
+        constexpr uint32_t idvo = umma::idesc_f16(128, 128, BF, false, false);
+        constexpr uint32_t idv = umma::idesc_f16(128, 64, BF, false, false);
+#pragma unroll
+        for (int k0 = 0; k0 < DH; k0 += 16)
+          umma::mma_f16(tm + COL_R2, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
+                        umma::desc_kmajor(sb + OFF_KQH, 128, k0), outputs_on ? idvo : idv, 1);
+        umma::mma_commit(&bar_v);
+      }
     }
     if (!wait_mma()) break;
 
@@ -1013,8 +1050,6 @@ __global__ void __launch_bounds__(NT, 1)
           put16<BF>(sb + OFF_PP, 64, t, slice * 16, pv, 1.f);
       }
     }
-    __syncthreads();
-
     // ---- T = (I + A)^-1 Diag(beta). X = (I + A)^-1 (unit lower triangular) is
     // built in three levels: its four 16 x 16 diagonal blocks X_aa by forward
     // substitution (one thread per column); the two 32 x 32 diagonal blocks,
@@ -1022,40 +1057,87 @@ __global__ void __launch_bounds__(NT, 1)
     // 32 x 32 quarter X_BA = -X_B (A_BA X_A), A and B the two halves. Each
     // off-diagonal X block overwrites its A block in AX once that is used;
     // above the diagonal AX holds zeros throughout.
+    // Level 1 runs on warps 0 and 1 while warps 4 .. 15 move V'^T into shared
+    // memory (rows v: the A operand of MMA2, high / low parts for the split
+    // products) and rescale S0 <- S0 Diag(gamma_last) in tensor memory (MMA5
+    // accumulates onto it; this chunk's MMAs read S0 from its shared copy):
+    // three warps per TMEM lane quarter, 64 columns each.
     static_assert(NT == 512, "solve thread mapping");
-    if (!additive) {
-    if (tid < 64) {
-      const int blk = tid >> 4, jj = tid & 15, base = blk * 16;
-      float x[16];
+    __syncthreads();  // A (and P) are complete
+    if (warp >= 4) {
+      if (!additive && warp == 4 && lane == 0) {
+        if (!umma::mbar_wait(&bar_v, ph_v, kWaitTries)) {
+          abort_sh = 1;
+          report(a.status, LIN_ST_TIMEOUT);
+        }
+      }
+      asm volatile("bar.sync 1, 384;" ::: "memory");  // warps 4 .. 15
+      umma::fence_after_sync();
+      if (!abort_sh) {
+        const int part = (warp - 4) >> 2;
+        if (part == 0) {
+          if (!additive) {
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float av[16];
-        const float4* ar4 = reinterpret_cast<const float4*>(AX + (base + r) * AXS + base);
+            for (int m = 0; m < 4; ++m) {
+              float v16[16];
+              umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + 16 * m), v16);
+              if (SPLIT)
+                put16_split(sb + OFF_VPT, sb + OFF_VPTL, 128, vrow, 16 * m, v16, 1.f);
+              else
+                put16<BF>(sb + OFF_VPT, 128, vrow, 16 * m, v16, 1.f);
+            }
+          }
+        } else {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          if (4 * q4 < r) {
-            const float4 f = ar4[q4];
-            av[4 * q4] = f.x;
-            av[4 * q4 + 1] = f.y;
-            av[4 * q4 + 2] = f.z;
-            av[4 * q4 + 3] = f.w;
+          for (int m = 0; m < 2; ++m) {
+            float v[32];
+            const int cc = (part - 1) * 64 + 32 * m;
+            umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= GLAST[KDA ? cc + k : 0];
+            umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
           }
         }
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < r; ++i) {
-          if (i & 1)
-            s1 = fmaf(av[i], x[i], s1);
-          else
-            s0 = fmaf(av[i], x[i], s0);
-        }
-        // x[i] = 0 for i < jj, so the sum is 0 at and above the diagonal
-        x[r] = (r == jj) ? 1.f : -(s0 + s1);
       }
+      umma::fence_smem_to_async();
+      umma::fence_before_sync();
+    } else if (!additive) {
+      if (tid < 64) {
+        const int blk = tid >> 4, jj = tid & 15, base = blk * 16;
+        float x[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) XD[blk * XBS + r * XDS + jj] = x[r];
+        for (int r = 0; r < 16; ++r) {
+          float av[16];
+          const float4* ar4 = reinterpret_cast<const float4*>(AX + (base + r) * AXS + base);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            if (4 * q4 < r) {
+              const float4 f = ar4[q4];
+              av[4 * q4] = f.x;
+              av[4 * q4 + 1] = f.y;
+              av[4 * q4 + 2] = f.z;
+              av[4 * q4 + 3] = f.w;
+            }
+          }
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < r; ++i) {
+            if (i & 1)
+              s1 = fmaf(av[i], x[i], s1);
+            else
+              s0 = fmaf(av[i], x[i], s0);
+          }
+          // x[i] = 0 for i < jj, so the sum is 0 at and above the diagonal
+          x[r] = (r == jj) ? 1.f : -(s0 + s1);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) XD[blk * XBS + r * XDS + jj] = x[r];
+      }
     }
+    if (!additive) ph_v ^= 1;
     __syncthreads();
+    if (abort_sh) break;
+    if (!additive) {
     {
       // Y_s = A_{2s+1,2s} X_{2s,2s}
       const int s2 = tid >> 8, r = (tid >> 4) & 15, c = tid & 15;
@@ -1182,58 +1264,26 @@ __global__ void __launch_bounds__(NT, 1)
     umma::fence_before_sync();
     __syncthreads();
 
-    // ---- MMA2: W^T = Khat^T T^T (R2), U'^T = V^T T^T (R1)
+    // ---- MMA2: U^T = V'^T T^T (R1); the additive form: U^T = V^T T^T
     if (tid == 0) {
       umma::fence_after_sync();
-      constexpr uint32_t id2 = umma::idesc_f16(128, 64, BF, true, false);
+      constexpr uint32_t id2k = umma::idesc_f16(128, 64, BF, false, false);  // A: V'^T, rows v
+      constexpr uint32_t id2m = umma::idesc_f16(128, 64, BF, true, false);   // A: V, rows t
+      const uint32_t id2 = additive ? id2m : id2k;
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16) {
-        const uint64_t bd = umma::desc_kmajor(sb + OFF_TT, 64, k0);
-        const uint64_t akh = umma::desc_mnmajor(sb + OFF_KH, 64, k0);
-        const uint64_t avv = umma::desc_mnmajor(sb + OFF_VV, 64, k0);
-        if (!additive) umma::mma_f16(tm + COL_R2, akh, bd, id2, k0 > 0);
-        umma::mma_f16(tm + COL_R1, avv, bd, id2, k0 > 0);
+        const uint64_t av = additive ? umma::desc_mnmajor(sb + OFF_VV, 64, k0)
+                                     : umma::desc_kmajor(sb + OFF_VPT, 128, k0);
+        const uint64_t bt = umma::desc_kmajor(sb + OFF_TT, 64, k0);
+        umma::mma_f16(tm + COL_R1, av, bt, id2, k0 > 0);
         if (SPLIT) {
-          const uint64_t bl = umma::desc_kmajor(sb + OFF_TTL, 64, k0);
-          if (!additive) umma::mma_f16(tm + COL_R2, akh, bl, id2, 1);
-          umma::mma_f16(tm + COL_R1, avv, bl, id2, 1);
+          umma::mma_f16(tm + COL_R1, av, umma::desc_kmajor(sb + OFF_TTL, 64, k0), id2, 1);
+          if (!additive) umma::mma_f16(tm + COL_R1, umma::desc_kmajor(sb + OFF_VPTL, 128, k0), bt, id2, 1);
         }
       }
       umma::mma_commit(&bar_mma);
     }
     if (!wait_mma()) break;
-
-    // ---- -W into shared memory (rows c); S0 <- S0 Diag(gamma_last) in TMEM
-    {
-      if (!additive) {
-        float w16[16];
-        umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_R2 + slice * 16), w16);
-        put16<BF>(sb + OFF_WW, 128, vrow, slice * 16, w16, -1.f);
-      }
-      float v[32];
-      const int cc = slice * 32;
-      umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] *= GLAST[KDA ? cc + k : 0];
-      umma::tmem_st32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
-    }
-    umma::fence_smem_to_async();
-    umma::fence_before_sync();
-    __syncthreads();
-
-    // ---- MMA3: U^T = U'^T + S0 (-W)^T (R1); the additive form has no such term
-    if (!additive) {
-      if (tid == 0) {
-        umma::fence_after_sync();
-        constexpr uint32_t id3 = umma::idesc_f16(128, 64, BF, false, true);
-#pragma unroll
-        for (int k0 = 0; k0 < DH; k0 += 16)
-          umma::mma_f16(tm + COL_R1, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
-                        umma::desc_mnmajor(sb + OFF_WW, 128, k0), id3, 1);
-        umma::mma_commit(&bar_mma);
-      }
-      if (!wait_mma()) break;
-    }
 
     // ---- U^T into shared memory (rows v)
     {
