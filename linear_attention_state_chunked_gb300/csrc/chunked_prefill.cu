@@ -540,6 +540,20 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tm = tmem_base_sh;
+  // Shared-memory descriptors of sb + off differ from those of sb only in the
+  // start-address field, (addr >> 4) in the low 14 bits (addresses stay below
+  // 2^18), so the issuing thread adds a constant instead of rebuilding them.
+  const uint64_t dk0 = umma::smem_desc(sb, 16, 1024);
+  const uint64_t dm64 = umma::smem_desc(sb, 64 * 128, 1024);
+  const uint64_t dm128 = umma::smem_desc(sb, 128 * 128, 1024);
+  // K-major operand at sb + off with `rows` rows: K-step k0 (as umma::desc_kmajor)
+  auto kdesc = [&](uint32_t off, int rows, int k0) -> uint64_t {
+    return dk0 + ((off + static_cast<uint32_t>(k0 >> 6) * rows * 128 + static_cast<uint32_t>(k0 & 63) * 2) >> 4);
+  };
+  // MN-major operand at sb + off with `krows` K rows (as umma::desc_mnmajor)
+  auto mdesc = [&](uint32_t off, int krows, int k0) -> uint64_t {
+    return (krows == 64 ? dm64 : dm128) + ((off + static_cast<uint32_t>(k0) * 128) >> 4);
+  };
 
   // ---- initial state: fp32 into TMEM, 16-bit operand copy into shared memory
   {
@@ -902,15 +916,15 @@ __global__ void __launch_bounds__(NT, 1)
       constexpr uint32_t id1 = umma::idesc_f16(128, 64, BF1, false, false);
 #pragma unroll
       for (int k0 = 0; k0 < DH; k0 += 16) {
-        const uint64_t ah = umma::desc_kmajor(sb + OFF_KQ, 128, k0);
+        const uint64_t ah = kdesc(OFF_KQ, 128, k0);
         if (SPLIT && KDA) {
-          const uint64_t al = umma::desc_kmajor(sb + OFF_KQL, 128, k0);
-          const uint64_t bh = umma::desc_kmajor(sb + OFF_KR, 64, k0);
+          const uint64_t al = kdesc(OFF_KQL, 128, k0);
+          const uint64_t bh = kdesc(OFF_KR, 64, k0);
           umma::mma_f16(tm + COL_R1, ah, bh, id1, k0 > 0);
-          umma::mma_f16(tm + COL_R1, ah, umma::desc_kmajor(sb + OFF_KRL, 64, k0), id1, 1);
+          umma::mma_f16(tm + COL_R1, ah, kdesc(OFF_KRL, 64, k0), id1, 1);
           umma::mma_f16(tm + COL_R1, al, bh, id1, 1);
         } else if (KDA) {
-          umma::mma_f16(tm + COL_R1, ah, umma::desc_kmajor(sb + OFF_KR, 64, k0), id1, k0 > 0);
+          umma::mma_f16(tm + COL_R1, ah, kdesc(OFF_KR, 64, k0), id1, k0 > 0);
         } else {
           umma::mma_f16(tm + COL_R1, ah, ah, id1, k0 > 0);  // B: rows 0..63 (K) of the same panels
         }
@@ -923,8 +937,8 @@ __global__ void __launch_bounds__(NT, 1)
         constexpr uint32_t id4 = umma::idesc_f16(128, 64, BF, false, false);
 #pragma unroll
         for (int k0 = 0; k0 < DH; k0 += 16)
-          umma::mma_f16(tm + COL_RO, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
-                        umma::desc_kmajor(sb + OFF_KQH + CH * 128, 128, k0), id4, k0 > 0);
+          umma::mma_f16(tm + COL_RO, kdesc(OFF_SOP, 128, k0),
+                        kdesc(OFF_KQH + CH * 128, 128, k0), id4, k0 > 0);
       }
     }
     if (!KDA && tid >= 32 && tid < 96) {
@@ -968,8 +982,8 @@ __global__ void __launch_bounds__(NT, 1)
         constexpr uint32_t idv = umma::idesc_f16(128, 64, BF, false, false);
 #pragma unroll
         for (int k0 = 0; k0 < DH; k0 += 16)
-          umma::mma_f16(tm + COL_R2, umma::desc_kmajor(sb + OFF_SOP, 128, k0),
-                        umma::desc_kmajor(sb + OFF_KQH, 128, k0), outputs_on ? idvo : idv, 1);
+          umma::mma_f16(tm + COL_R2, kdesc(OFF_SOP, 128, k0),
+                        kdesc(OFF_KQH, 128, k0), outputs_on ? idvo : idv, 1);
         umma::mma_commit(&bar_v);
       }
     }
@@ -1272,13 +1286,13 @@ __global__ void __launch_bounds__(NT, 1)
       const uint32_t id2 = additive ? id2m : id2k;
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16) {
-        const uint64_t av = additive ? umma::desc_mnmajor(sb + OFF_VV, 64, k0)
-                                     : umma::desc_kmajor(sb + OFF_VPT, 128, k0);
-        const uint64_t bt = umma::desc_kmajor(sb + OFF_TT, 64, k0);
+        const uint64_t av = additive ? mdesc(OFF_VV, 64, k0)
+                                     : kdesc(OFF_VPT, 128, k0);
+        const uint64_t bt = kdesc(OFF_TT, 64, k0);
         umma::mma_f16(tm + COL_R1, av, bt, id2, k0 > 0);
         if (SPLIT) {
-          umma::mma_f16(tm + COL_R1, av, umma::desc_kmajor(sb + OFF_TTL, 64, k0), id2, 1);
-          if (!additive) umma::mma_f16(tm + COL_R1, umma::desc_kmajor(sb + OFF_VPTL, 128, k0), bt, id2, 1);
+          umma::mma_f16(tm + COL_R1, av, kdesc(OFF_TTL, 64, k0), id2, 1);
+          if (!additive) umma::mma_f16(tm + COL_R1, kdesc(OFF_VPTL, 128, k0), bt, id2, 1);
         }
       }
       umma::mma_commit(&bar_mma);
@@ -1305,15 +1319,15 @@ __global__ void __launch_bounds__(NT, 1)
       constexpr uint32_t id5 = umma::idesc_f16(128, 128, BF, false, true);
 #pragma unroll
       for (int k0 = 0; k0 < CH; k0 += 16) {
-        const uint64_t ad = umma::desc_kmajor(sb + OFF_UT, 128, k0);
-        const uint64_t bp = umma::desc_kmajor(sb + OFF_PP, 64, k0);
-        const uint64_t bk = umma::desc_mnmajor(sb + OFF_KT, 64, k0);
+        const uint64_t ad = kdesc(OFF_UT, 128, k0);
+        const uint64_t bp = kdesc(OFF_PP, 64, k0);
+        const uint64_t bk = mdesc(OFF_KT, 64, k0);
         if (outputs_on) umma::mma_f16(tm + COL_RO, ad, bp, id4, 1);
         umma::mma_f16(tm + COL_S, ad, bk, id5, 1);
         if (SPLIT) {
-          const uint64_t al = umma::desc_kmajor(sb + OFF_UTL, 128, k0);
+          const uint64_t al = kdesc(OFF_UTL, 128, k0);
           if (outputs_on) {
-            umma::mma_f16(tm + COL_RO, ad, umma::desc_kmajor(sb + OFF_PPL, 64, k0), id4, 1);
+            umma::mma_f16(tm + COL_RO, ad, kdesc(OFF_PPL, 64, k0), id4, 1);
             umma::mma_f16(tm + COL_RO, al, bp, id4, 1);
           }
           umma::mma_f16(tm + COL_S, al, bk, id5, 1);
