@@ -763,13 +763,9 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- conv, activation, q/k normalisation, operand rows
     {
-      // tile value of window row m (chunk row tfirst - 3 + m), part, channel
-      // lane*4+e; rows before the chunk (warp 0, m < 3) hold zeros here and
-      // their terms are added from the previous window below
-      auto xv = [&](int m, int part, int e) -> float {
-        const uint32_t w = (e < 2) ? xr[m][part].x : xr[m][part].y;
-        return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-      };
+      // xr[m]: window row m (chunk row tfirst - 3 + m) of the tile, channels
+      // lane*4 .. lane*4+3 per part; rows before the chunk (warp 0, m < 3) hold
+      // zeros there and their terms are added from the previous window below
       // part-major: the taps of one part are loaded once and applied to all
       // of this warp's tokens; q and k get their per-token norms
       float yq[TPW][4], yk[TPW][4], yv[TPW][4], rq[TPW], rk[TPW];
@@ -792,18 +788,35 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int tap = 0; tap < 4; ++tap)
           w4[tap] = *reinterpret_cast<const float4*>(WC + tap * 384 + part * 128 + lane * 4);
+        // the taps on channel pairs (lane*4 + 0, 1) and (lane*4 + 2, 3), two
+        // lanes of fp32 arithmetic per instruction; the x tile's bf16 pairs
+        // unpack straight into such pairs
         float ypre[TPW][4];
+        {
+          uint64_t wp[4][2];
 #pragma unroll
-        for (int i = 0; i < TPW; ++i)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float w0 = e == 0 ? w4[0].x : e == 1 ? w4[0].y : e == 2 ? w4[0].z : w4[0].w;
-            const float w1 = e == 0 ? w4[1].x : e == 1 ? w4[1].y : e == 2 ? w4[1].z : w4[1].w;
-            const float w2 = e == 0 ? w4[2].x : e == 1 ? w4[2].y : e == 2 ? w4[2].z : w4[2].w;
-            const float w3 = e == 0 ? w4[3].x : e == 1 ? w4[3].y : e == 2 ? w4[3].z : w4[3].w;
-            ypre[i][e] = w0 * xv(i, part, e) + w1 * xv(i + 1, part, e) + w2 * xv(i + 2, part, e) +
-                         w3 * xv(i + 3, part, e);
+          for (int tap = 0; tap < 4; ++tap) {
+            wp[tap][0] = f2pack(w4[tap].x, w4[tap].y);
+            wp[tap][1] = f2pack(w4[tap].z, w4[tap].w);
           }
+          auto xp = [&](int m, int hp) -> uint64_t {
+            const uint32_t w = hp ? xr[m][part].y : xr[m][part].x;
+            return f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+          };
+#pragma unroll
+          for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+              uint64_t y = fmul2(wp[0][hp], xp(i, hp));
+              y = ffma2(wp[1][hp], xp(i + 1, hp), y);
+              y = ffma2(wp[2][hp], xp(i + 2, hp), y);
+              y = ffma2(wp[3][hp], xp(i + 3, hp), y);
+              float lo, hi;
+              asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y));
+              ypre[i][2 * hp] = lo;
+              ypre[i][2 * hp + 1] = hi;
+            }
+        }
         if (warp == 0) {
           // tokens 0..2: the taps on the 3 rows before the chunk
           const float* hp = wprev + part * 128 + lane * 4;
