@@ -171,7 +171,7 @@ class PrefillWorkload(Workload):
             n_tr = [tracks_per_req] * B
         n_slots = 1 + B + sum(n_tr)
         self.pool = L.StatePool(1, n_slots, dims.num_heads, dims.head_k, state_dtype=state_dtype,
-                                conv_dtype=io_dtype, device=dev)
+                                conv_dtype=io_dtype, device=dev, head_v=dims.head_v)
         if any(warm):
             g = torch.Generator(device=dev)
             g.manual_seed(seed + 17)
@@ -562,6 +562,10 @@ def make_workload(name, L, dev):
         return PrefillWorkload(L, dev, name, W.QWEN35_GDN, [4096] * 8, [0] * 8, [0] * 8,
                                W.GATE_PER_HEAD, torch.bfloat16, torch.float32, torch.float32,
                                64, 2, "ssd", flags=L.LIN_CONV_SILU | L.LIN_UPDATE_ADDITIVE)
+    if name == "mamba2_ssd_prefill_hd64":
+        return PrefillWorkload(L, dev, name, W.MAMBA2_HD64, [4096] * 8, [0] * 8, [0] * 8,
+                               W.GATE_PER_HEAD, torch.bfloat16, torch.float32, torch.float32,
+                               64, 2, "ssd", flags=L.LIN_CONV_SILU | L.LIN_UPDATE_ADDITIVE)
     if name == "kda_decode":
         return DecodeWorkload(L, dev, 1)
     if name == "kda_spec_verify4_commit":
@@ -582,7 +586,8 @@ def make_workload(name, L, dev):
 HEADLINE = "qwen35_gdn_prefill"
 DEFAULT_EXTRA = ["kimi_k3_kda_varlen_prefill", "kda_decode", "kda_spec_verify4_commit",
                  "kda_spec_verify4_replay", "kda_tree_verify8_commit",
-                 "slot_copy_kimi_k3_69l", "kda_long_prefill_131k", "mamba2_ssd_prefill"]
+                 "slot_copy_kimi_k3_69l", "kda_long_prefill_131k", "mamba2_ssd_prefill",
+                 "mamba2_ssd_prefill_hd64"]
 
 CONFIG_TEXT = {
     "qwen35_gdn_prefill": "Qwen3.5-style GDN prefill: 1 linear layer, 32 heads, K=V=128, conv 4 over "
@@ -609,6 +614,11 @@ CONFIG_TEXT = {
                           "headdim = d_state = 128, conv 4 + SiLU over x|B|C, no q/k norm, "
                           "dt = softplus(N(0,1)-3), A = -U[1,16] per head, bf16 inputs, fp32 state "
                           "and outputs, 8 requests x 4096 tokens, snapshot every 64 (ping-pong)",
+    "mamba2_ssd_prefill_hd64": "Mamba2-style SSD prefill with head dim 64 and state size 128 (additive "
+                               "update): 64 heads of 128 key (B, C) and 64 value (x) channels, conv 4 + "
+                               "SiLU over x|B|C, no q/k norm, dt = softplus(N(0,1)-3), A = -U[1,16] per "
+                               "head, bf16 inputs, fp32 state and outputs, 8 requests x 4096 tokens, "
+                               "snapshot every 64 (ping-pong)",
     "kda_long_prefill_131k": "single-request KDA prefill, 131072 tokens, 12 heads, bf16, cold, "
                              "snapshots every 64 into 2048 distinct track slots",
 }
@@ -908,6 +918,7 @@ def cpu_copy(wl, pairs_per_batch=16, batches=3):
 CPU_LEGS = {
     "qwen35_gdn_prefill": lambda wl: cpu_prefill(wl, 16384),
     "mamba2_ssd_prefill": lambda wl: cpu_prefill(wl, 16384),
+    "mamba2_ssd_prefill_hd64": lambda wl: cpu_prefill(wl, 8192),
     "kimi_k3_kda_varlen_prefill": lambda wl: cpu_prefill(wl, 40000),
     "kda_long_prefill_131k": lambda wl: cpu_prefill(wl, 24576),
     "kda_decode": lambda wl: cpu_decode(wl, 8),

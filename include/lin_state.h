@@ -103,8 +103,8 @@ enum {
  * C = conv_channels = 2*H*K + H*V, ordered q | k | v, head-major inside each.
  * Requirements: conv_width == 4; (head_k, head_v) one of (16,16), (32,32),
  * (64,64), (128,128), or (128,64) (128 key channels with 64 value channels:
- * the SSD head, state size 128 and head dim 64; prefill of that shape runs
- * token by token). Anything else is LIN_EUNSUPPORTED. */
+ * the SSD head, state size 128 and head dim 64). Anything else is
+ * LIN_EUNSUPPORTED. */
 typedef struct {
   int32_t num_layers, num_slots, num_heads, head_k, head_v;
   int32_t conv_channels, conv_width;
@@ -191,7 +191,8 @@ typedef struct {
 } lin_prefill_args_t;
 
 /* Which kernel lin_state_prefill would run for these arguments:
- * LIN_KERNEL_CHUNKED (the tensor-core chunked kernel: head_k == head_v == 128, bf16 x)
+ * LIN_KERNEL_CHUNKED (the tensor-core chunked kernel: head_k == 128 and
+ * head_v 128 or 64, bf16 x)
  * or LIN_KERNEL_RECURRENT (token by token; any supported head dim, or when
  * LIN_PREFILL_RECURRENT is set). A negative LIN_E* code for invalid args. */
 #define LIN_KERNEL_RECURRENT 0

@@ -197,9 +197,17 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__
   for (int i = threadIdx.x; i < batch; i += blockDim.x) order[i] = static_cast<int32_t>(key[i] & 0xffffffffu);
 }
 
+// Global channel of the head's channel cl in [0, 384): q, k and v parts of
+// 128 each; a value part of VD < 128 channels takes the first VD (the rest are
+// padding: see valid_channel).
+template <int VD>
 __device__ __forceinline__ int head_channel(int cl, int h, int H) {
   const int part = cl >> 7, c = cl & 127;
-  return part * H * DH + h * DH + c;
+  return part < 2 ? part * H * DH + h * DH + c : 2 * H * DH + h * VD + c;
+}
+template <int VD>
+__device__ __forceinline__ bool valid_channel(int cl) {
+  return VD == DH || cl < 2 * DH + VD;
 }
 
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
@@ -250,11 +258,12 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane0, uint32_t
 
 // Prefetch x rows [row0 - 3, row0 + 64) of the head's q | k | v channel blocks
 // into L2 (tensor-map prefetch; the conv phase then reads them from L2).
+template <int VD>
 __device__ __forceinline__ void prefetch_x_tile(const CUtensorMap* tmap, int64_t row0, int h, int H) {
   const int y = static_cast<int>(row0) - 3;
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
-    const int x = part * H * DH + h * DH;
+    const int x = part < 2 ? part * H * DH + h * DH : 2 * H * DH + h * VD;
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
                  "r"(x), "r"(y)
@@ -379,7 +388,12 @@ __device__ __forceinline__ void put16_split(uint32_t hi_buf, uint32_t lo_buf, in
 // first segment) and transition runs write no outputs and skip the q (and, in
 // transition runs, the v) part of the conv and the output MMAs; the one-piece
 // launch uses SEG = false, where every run has outputs.
-template <bool KDA, int ST, bool SEG>
+// VD: value channels of a head, 128 or 64 (the Mamba2-style head of head dim
+// 64 with 128 key channels). A 64-channel head runs on the same 128-row tiles
+// with its value side padded by zeros: the padded conv channels have zero
+// taps and window, so v, V', U, the state rows v >= 64 and their outputs stay
+// zero; only the first VD rows are loaded and stored.
+template <bool KDA, int ST, bool SEG, int VD>
 __global__ void __launch_bounds__(NT, 1)
     chunked_prefill_kernel(const __grid_constant__ CUtensorMap tmap_x,
                            const __grid_constant__ CUtensorMap tmap_xt,
@@ -484,7 +498,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int L = static_cast<int>(eos_c - bos);
   const int nch = (L + CH - 1) / CH;
   constexpr int ES = ST == LIN_BF16 ? 2 : 4;
-  const int64_t head_bytes = int64_t(DH) * DH * ES;
+  const int64_t head_bytes = int64_t(VD) * DH * ES;
   char* slot_t = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
                  slot * pool.temporal_slot_stride + h * head_bytes;
   char* slot_c = static_cast<char*>(pool.conv) + a.layer * pool.conv_layer_stride +
@@ -505,24 +519,29 @@ __global__ void __launch_bounds__(NT, 1)
   float* YB = reinterpret_cast<float*>(sm + OFF_YB);
   float* ZB = reinterpret_cast<float*>(sm + OFF_ZB);
 
-  if (tid == 0) prefetch_x_tile(&tmap_x, bos, h, H);
+  if (tid == 0) prefetch_x_tile<VD>(&tmap_x, bos, h, H);
   for (int i = tid; i < 384 * 4; i += NT)
     WC[(i & 3) * 384 + (i >> 2)] =
-        load_elem(a.conv_w, int64_t(head_channel(i >> 2, h, H)) * 4 + (i & 3), a.io_dtype);
+        valid_channel<VD>(i >> 2)
+            ? load_elem(a.conv_w, int64_t(head_channel<VD>(i >> 2, h, H)) * 4 + (i & 3), a.io_dtype)
+            : 0.f;
   for (int i = tid; i < 3 * 384; i += NT) {
     const int rr = i / 384, cl = i % 384;
-    if (seg > 0)  // the 3 inputs before the segment
-      HALO[i] = load_elem(a.x, (bos - 3 + rr) * int64_t(pool.conv_channels) + head_channel(cl, h, H), LIN_BF16);
+    if (!valid_channel<VD>(cl))
+      HALO[i] = 0.f;
+    else if (seg > 0)  // the 3 inputs before the segment
+      HALO[i] = load_elem(a.x, (bos - 3 + rr) * int64_t(pool.conv_channels) + head_channel<VD>(cl, h, H), LIN_BF16);
     else
-      HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
+      HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel<VD>(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
   }
 
   if (nch == 0) {
     // No tokens: the slot keeps its state; a cold start leaves zeros in it.
     if (!warm) {
-      for (int i = tid; i < DH * DH; i += NT) store_elem(slot_t, i, ST, 0.f);
+      for (int i = tid; i < VD * DH; i += NT) store_elem(slot_t, i, ST, 0.f);
       for (int i = tid; i < 3 * 384; i += NT)
-        store_elem(slot_c, int64_t(head_channel(i / 3, h, H)) * 3 + (i % 3), pool.conv_dtype, 0.f);
+        if (valid_channel<VD>(i / 3))
+          store_elem(slot_c, int64_t(head_channel<VD>(i / 3, h, H)) * 3 + (i % 3), pool.conv_dtype, 0.f);
     }
     return;
   }
@@ -559,7 +578,10 @@ __global__ void __launch_bounds__(NT, 1)
   {
     float s[32];
     const int cc = slice * 32;
-    if (warm) {
+    if (warm && vrow >= VD) {
+#pragma unroll
+      for (int m = 0; m < 32; ++m) s[m] = 0.f;  // padding rows of a 64-channel value side
+    } else if (warm) {
       if (ST == LIN_BF16) {
         const uint16_t* src = reinterpret_cast<const uint16_t*>(slot_t) + vrow * DH + cc;
 #pragma unroll
@@ -638,7 +660,8 @@ __global__ void __launch_bounds__(NT, 1)
                  : "memory");
 #pragma unroll
     for (int part = 0; part < 3; ++part)
-      tma_load_2d(&tmap_xt, sb + OFF_XT + part * (CH * DH * 2), part * H * DH + h * DH, static_cast<int>(r0), b);
+      tma_load_2d(&tmap_xt, sb + OFF_XT + part * (CH * DH * 2),
+                  part < 2 ? part * H * DH + h * DH : 2 * H * DH + h * VD, static_cast<int>(r0), b);
     ++x_issued;
   };
   if (tid == 0) issue_x_tile(bos);
@@ -924,7 +947,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- MMA1: [A'; P'] = [K_l; Q_l] K_r^T; prefetch the next chunk's x rows
     if (tid == 0) {
-      if (j + 1 < nch) prefetch_x_tile(&tmap_x, row0 + CH, h, H);
+      if (j + 1 < nch) prefetch_x_tile<VD>(&tmap_x, row0 + CH, h, H);
       umma::fence_after_sync();
       constexpr uint32_t id1 = umma::idesc_f16(128, 64, BF1, false, false);
 #pragma unroll
@@ -1362,19 +1385,21 @@ __global__ void __launch_bounds__(NT, 1)
       if (outputs_on) {
         float o16[16];
         umma::tmem_ld16(tmem_addr(tm, quarter * 32, COL_RO + slice * 16), o16);
-        if (full) {
+        if (vrow >= VD) {
+          // padding rows of a 64-channel value side: nothing to store
+        } else if (full) {
           uint8_t* ost = sm + OFF_OSTG;
           if (oes == 2) {
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-              reinterpret_cast<uint16_t*>(ost)[(slice * 16 + k) * DH + vrow] = f32_to_bf16_bits(o16[k]);
+              reinterpret_cast<uint16_t*>(ost)[(slice * 16 + k) * VD + vrow] = f32_to_bf16_bits(o16[k]);
           } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) reinterpret_cast<float*>(ost)[(slice * 16 + k) * DH + vrow] = o16[k];
+            for (int k = 0; k < 16; ++k) reinterpret_cast<float*>(ost)[(slice * 16 + k) * VD + vrow] = o16[k];
           }
         } else {
-          const int64_t ob = (row0 * H + h) * DH + vrow;
-          const int64_t ostep = int64_t(H) * DH;
+          const int64_t ob = (row0 * H + h) * VD + vrow;
+          const int64_t ostep = int64_t(H) * VD;
           if (oes == 2) {
             uint16_t* op = static_cast<uint16_t*>(a.out) + ob;
 #pragma unroll
@@ -1447,7 +1472,8 @@ __global__ void __launch_bounds__(NT, 1)
                                      : nullptr;
         for (int idx = tid; idx < 3 * 384; idx += NT) {
           const int cl = idx / 3, m = idx % 3;
-          const int ch = head_channel(cl, h, H);
+          if (!valid_channel<VD>(cl)) continue;
+          const int ch = head_channel<VD>(cl, h, H);
           const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
           const int64_t off = int64_t(ch) * 3 + m;
           if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
@@ -1594,7 +1620,7 @@ size_t segment_workspace(const lin_state_pool_t& pool, const SegPlan& sp) {
   return 2 * size_t(sp.nseg) * pool.num_heads * DH * DH * sizeof(float);
 }
 
-template <bool KDA, int ST>
+template <bool KDA, int ST, int VD>
 cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
                      const SegPlan& sp, float* seg_buf, uint32_t* redo, cudaStream_t s) {
   auto enc = encode_fn();
@@ -1623,11 +1649,11 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
   {
     const int es = ST == LIN_BF16 ? 2 : 4;
     char* base = static_cast<char*>(pool.temporal) + a.layer * pool.temporal_layer_stride;
-    const cuuint64_t d[4] = {DH, DH, static_cast<cuuint64_t>(pool.num_heads),
+    const cuuint64_t d[4] = {DH, VD, static_cast<cuuint64_t>(pool.num_heads),
                              static_cast<cuuint64_t>(pool.num_slots)};
-    const cuuint64_t st[3] = {static_cast<cuuint64_t>(DH) * es, static_cast<cuuint64_t>(DH) * DH * es,
+    const cuuint64_t st[3] = {static_cast<cuuint64_t>(DH) * es, static_cast<cuuint64_t>(VD) * DH * es,
                               static_cast<cuuint64_t>(pool.temporal_slot_stride)};
-    const cuuint32_t bx[4] = {static_cast<cuuint32_t>(128 / es), DH, 1, 1};
+    const cuuint32_t bx[4] = {static_cast<cuuint32_t>(128 / es), VD, 1, 1};
     const cuuint32_t es4[4] = {1, 1, 1, 1};
     cr = enc(&tmap_state, ST == LIN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
              4, base, d, st, bx, es4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1638,11 +1664,11 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
   CUtensorMap tmap_out;
   {
     const int es = a.out_dtype == LIN_BF16 ? 2 : 4;
-    const cuuint64_t d[3] = {DH, static_cast<cuuint64_t>(pool.num_heads),
+    const cuuint64_t d[3] = {VD, static_cast<cuuint64_t>(pool.num_heads),
                              static_cast<cuuint64_t>(a.total_tokens)};
-    const cuuint64_t st[2] = {static_cast<cuuint64_t>(DH) * es,
-                              static_cast<cuuint64_t>(DH) * pool.num_heads * es};
-    const cuuint32_t bx[3] = {DH, 1, CH};
+    const cuuint64_t st[2] = {static_cast<cuuint64_t>(VD) * es,
+                              static_cast<cuuint64_t>(VD) * pool.num_heads * es};
+    const cuuint32_t bx[3] = {VD, 1, CH};
     const cuuint32_t es3[3] = {1, 1, 1};
     cr = enc(&tmap_out, a.out_dtype == LIN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
              3, a.out, d, st, bx, es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1650,7 +1676,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   const bool segmented = sp.nseg >= 2 && seg_buf;
-  auto kern = segmented ? chunked_prefill_kernel<KDA, ST, true> : chunked_prefill_kernel<KDA, ST, false>;
+  auto kern = segmented ? chunked_prefill_kernel<KDA, ST, true, VD> : chunked_prefill_kernel<KDA, ST, false, VD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
@@ -1690,7 +1716,8 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
 }  // namespace
 
 bool chunked_prefill_supported(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
-  return pool.head_k == DH && pool.head_v == DH && a.io_dtype == LIN_BF16 && a.total_tokens > 0 &&
+  return pool.head_k == DH && (pool.head_v == DH || pool.head_v == 64) && a.io_dtype == LIN_BF16 &&
+         a.total_tokens > 0 &&
          int64_t(a.batch) * pool.num_heads < (int64_t(1) << 31) &&
          (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
          (reinterpret_cast<uintptr_t>(a.g) & 15) == 0 && encode_fn() != nullptr;
@@ -1720,17 +1747,25 @@ cudaError_t launch_chunked(const lin_state_pool_t& pool, const lin_prefill_args_
                            const SegPlan& sp, float* seg_buf, uint32_t* redo, cudaStream_t stream) {
   const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
   const bool bf = pool.state_dtype == LIN_BF16;
+  const bool v64 = pool.head_v == 64;
   cudaError_t e;
   if (kda) {
     if (!redo) return cudaErrorInvalidValue;
     if ((e = cudaMemsetAsync(redo, 0, redo_workspace(pool, a), stream)) != cudaSuccess) return e;
-    e = bf ? launch_t<true, LIN_BF16>(pool, a, order, sp, seg_buf, redo, stream)
-           : launch_t<true, LIN_F32>(pool, a, order, sp, seg_buf, redo, stream);
+    if (v64)
+      e = bf ? launch_t<true, LIN_BF16, 64>(pool, a, order, sp, seg_buf, redo, stream)
+             : launch_t<true, LIN_F32, 64>(pool, a, order, sp, seg_buf, redo, stream);
+    else
+      e = bf ? launch_t<true, LIN_BF16, DH>(pool, a, order, sp, seg_buf, redo, stream)
+             : launch_t<true, LIN_F32, DH>(pool, a, order, sp, seg_buf, redo, stream);
     if (e != cudaSuccess) return e;
     return launch_prefill_recurrent(pool, a, stream, redo);
   }
-  return bf ? launch_t<false, LIN_BF16>(pool, a, order, sp, seg_buf, nullptr, stream)
-            : launch_t<false, LIN_F32>(pool, a, order, sp, seg_buf, nullptr, stream);
+  if (v64)
+    return bf ? launch_t<false, LIN_BF16, 64>(pool, a, order, sp, seg_buf, nullptr, stream)
+              : launch_t<false, LIN_F32, 64>(pool, a, order, sp, seg_buf, nullptr, stream);
+  return bf ? launch_t<false, LIN_BF16, DH>(pool, a, order, sp, seg_buf, nullptr, stream)
+            : launch_t<false, LIN_F32, DH>(pool, a, order, sp, seg_buf, nullptr, stream);
 }
 }  // namespace
 

@@ -18,19 +18,23 @@ DEV = torch.device("cuda")
 FLAGS = O.FLAG_QK_L2NORM | O.FLAG_CONV_SILU
 
 
-def head_channels(H, D, heads):
+def head_channels(H, D, heads, V=None):
+    """Conv channels of the given heads, q | k | v parts (D key channels per
+    head in q and k, V value channels, V = D unless given)."""
+    V = D if V is None else V
     idx = []
     for part in range(3):
+        n = D if part < 2 else V
         for h in heads:
-            idx.extend(range(part * H * D + h * D, part * H * D + (h + 1) * D))
+            idx.extend(range(part * H * D + h * n, part * H * D + (h + 1) * n))
     return np.array(idx)
 
 
 def oracle_slice_prefill(wl, req, heads, pool_before_t, pool_before_c):
     """Run the oracle for one request on the given heads of a PrefillWorkload."""
     b = wl.b
-    H, D = b.dims.num_heads, b.dims.head_k
-    ch = head_channels(H, D, heads)
+    H, D, Vd = b.dims.num_heads, b.dims.head_k, b.dims.head_v
+    ch = head_channels(H, D, heads, Vd)
     a, e = int(b.cu_seqlens[req]), int(b.cu_seqlens[req + 1])
     x = np64(b.x[a:e])[:, ch]
     w = np64(b.conv_w)[ch]
@@ -41,7 +45,7 @@ def oracle_slice_prefill(wl, req, heads, pool_before_t, pool_before_c):
     tracks = wl.track.cpu().tolist()[cu_tr[req]:cu_tr[req + 1]]
     S = pool_before_t.shape[1]
     sd = "bf16" if wl.pool.temporal.dtype == torch.bfloat16 else "f32"
-    pool = {"temporal": np.zeros((1, S, len(heads), D, D)), "conv": np.zeros((1, S, len(ch), 3)),
+    pool = {"temporal": np.zeros((1, S, len(heads), Vd, D)), "conv": np.zeros((1, S, len(ch), 3)),
             "state_dtype": sd, "conv_dtype": "bf16"}
     pool["temporal"][0, slot] = np64(pool_before_t[0, slot][heads])
     pool["conv"][0, slot] = np64(pool_before_c[0, slot][ch])
@@ -78,6 +82,14 @@ def test_mamba2_ssd_prefill_full_size_sampled():
     wl = bench.make_workload("mamba2_ssd_prefill", L, DEV)
     assert wl.kw["flags"] & L.LIN_UPDATE_ADDITIVE
     check_prefill_slice(wl, 3, [7, 30], TOL_F32)
+
+
+def test_mamba2_ssd_prefill_hd64_full_size_sampled():
+    """Head dim 64, state size 128 (64 heads), on the chunked kernel with its
+    value side padded: sampled requests and heads against the oracle."""
+    wl = bench.make_workload("mamba2_ssd_prefill_hd64", L, DEV)
+    assert wl.kernel_kind == L.LIN_KERNEL_CHUNKED
+    check_prefill_slice(wl, 6, [0, 63], TOL_F32)
 
 
 def test_kimi_k3_kda_varlen_full_size_sampled():

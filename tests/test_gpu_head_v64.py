@@ -1,8 +1,9 @@
 """Heads with 128 key channels and 64 value channels (state [64][128]: the SSD
 head of the Mamba2 layer, state size 128 and head dim 64; the pool layout of
 the MambaRadixCache page, 1.3, with V != K), against the oracle. Prefill of
-this shape runs token by token; decode, verify, replay, tree verify, commit
-and slot copies run on the same kernels as the square heads."""
+this shape runs on the chunked tensor-core kernel (its value side padded to
+128 rows) and on the token-by-token kernel; decode, verify, replay, tree
+verify, commit and slot copies run on the same kernels as the square heads."""
 
 import numpy as np
 import pytest
@@ -36,12 +37,15 @@ def _pool(sdt, slots, seed, cdt=torch.bfloat16, layers=1):
     return pool
 
 
+@pytest.mark.parametrize("path", ["chunked", "recurrent"])
 @pytest.mark.parametrize("sdt,gate,flags", [("f32", "gdn", GDN), ("bf16", "kda", GDN),
-                                            ("f32", "ssd", SSD)])
-def test_prefill_head_v64(sdt, gate, flags):
+                                            ("f32", "kda", GDN), ("f32", "ssd", SSD)])
+def test_prefill_head_v64(sdt, gate, flags, path):
     """Three ragged requests (two warm from a 64-multiple prefix), snapshots
     every 64 into ping-pong pairs; the delta rule with per-head and per-key
-    gates, and the additive form."""
+    gates, and the additive form; both prefill kernels."""
+    if path == "recurrent":
+        flags = flags | L.LIN_PREFILL_RECURRENT
     gm = W.GATE_PER_KEY if gate == "kda" else W.GATE_PER_HEAD
     b = W.make_prefill_batch(DIMS, [300, 97, 415], gm, dtype=torch.bfloat16, seed=60,
                              gate="ssd" if gate == "ssd" else "softplus", prefixes=[128, 0, 64],
@@ -58,7 +62,8 @@ def test_prefill_head_v64(sdt, gate, flags):
               prefix_len=b.prefix_len.to(DEV), slot=_i32(slots),
               has_initial_state=b.has_initial_state.to(DEV), track_slots=_i32(tracks),
               cu_track=_i32(cu_track), track_stride=64, gate_mode=gm, flags=flags, status=st)
-    assert L.lin_state_prefill_kernel(pool, **kw) == L.LIN_KERNEL_RECURRENT
+    want = L.LIN_KERNEL_CHUNKED if path == "chunked" else L.LIN_KERNEL_RECURRENT
+    assert L.lin_state_prefill_kernel(pool, **kw) == want
     L.lin_state_prefill(pool, **kw)
     oo, ost = O.prefill(op, 0, np64(b.x), np64(b.conv_w), np64(b.g), np64(b.beta),
                         b.cu_seqlens.tolist(), b.prefix_len.tolist(), slots,
@@ -70,6 +75,39 @@ def test_prefill_head_v64(sdt, gate, flags):
     compare_slots(pool, op, list(range(1, 10)), tol)
     # slots the call does not name are untouched
     assert np.array_equal(np64(pool.temporal[0, 10:]), op["temporal"][0, 10:])
+
+
+@pytest.mark.parametrize("gate", ["kda", "ssd"])
+def test_prefill_head_v64_in_segments(gate):
+    """One long request in segments on the chunked kernel (offset and
+    transition runs, the fp32 scan, final runs) with a 64-channel value side:
+    the transition runs carry all 128 key rows of the affine map while the
+    value rows beyond 64 stay zero."""
+    gm = W.GATE_PER_KEY if gate == "kda" else W.GATE_PER_HEAD
+    flags = (GDN if gate == "kda" else SSD) | L.LIN_PREFILL_SEGMENTED
+    n = 1200
+    b = W.make_prefill_batch(DIMS, [n], gm, dtype=torch.bfloat16, seed=64,
+                             gate="ssd" if gate == "ssd" else "softplus", prefixes=[64], warm=[1],
+                             tag=f"hv64s.{gate}")
+    n_tr = (64 + n) // 64 - 1
+    pool = _pool("f32", 2 + n_tr, 65)
+    op = oracle_pool(pool)
+    out = torch.zeros((n, H, V), device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tracks = list(range(2, 2 + n_tr))
+    kw = dict(layer=0, x=b.x.to(DEV), conv_w=b.conv_w.to(DEV), g=b.g.to(DEV),
+              beta=b.beta.to(DEV), out=out, cu_seqlens=b.cu_seqlens.to(DEV),
+              prefix_len=b.prefix_len.to(DEV), slot=_i32([1]),
+              has_initial_state=b.has_initial_state.to(DEV), track_slots=_i32(tracks),
+              cu_track=_i32([0, n_tr]), track_stride=64, gate_mode=gm, flags=flags, status=st)
+    assert L.lin_state_prefill_kernel(pool, **kw) == L.LIN_KERNEL_CHUNKED
+    assert L.lin_state_prefill_workspace(pool, **kw) > 16 * 1024  # per-segment states
+    L.lin_state_prefill(pool, **kw)
+    oo, ost = O.prefill(op, 0, np64(b.x), np64(b.conv_w), np64(b.g), np64(b.beta), [0, n], [64],
+                        [1], [1], tracks, [0, n_tr], 64, gm, flags, 1.0, "f32")
+    assert L.lin_state_read_status(st) == ost == 0
+    compare_outputs(out, oo, [0, n], TOL_F32)
+    compare_slots(pool, op, [1] + tracks, TOL_F32)
 
 
 @pytest.mark.parametrize("sdt,gate,flags", [("f32", "gdn", GDN), ("bf16", "kda", GDN),

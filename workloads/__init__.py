@@ -78,6 +78,9 @@ class LayerDims:
 TINY_GDN = LayerDims(num_heads=2, head_k=16, head_v=16)
 QWEN35_GDN = LayerDims(num_heads=32, head_k=128, head_v=128)
 KIMI_K3_TP8 = LayerDims(num_heads=12, head_k=128, head_v=128)
+# a Mamba2-style SSD layer with head dim 64 and state size 128 (d_inner 4096):
+# in this pool's layout 64 heads of 128 key (B, C) and 64 value (x) channels
+MAMBA2_HD64 = LayerDims(num_heads=64, head_k=128, head_v=64)
 
 
 def gate_log_decay_softplus(shape, seed, name, device="cpu"):
