@@ -723,9 +723,6 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
 
-    // the previous chunk's TMA stores must have read their staging tiles before
-    // the conv writes operands over them (after the barrier in the gate sums)
-    if (tid == 0) bulk_wait_read();
 
     // ---- gates: in-chunk inclusive sums b_t (rows past n carry log-decay 0)
     float cs[TPW][4];
@@ -875,6 +872,10 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
+      // the previous chunk's TMA stores must have read their staging tiles
+      // before the operand rows go over them; those reads ran behind the conv
+      if (tid == 0) bulk_wait_read();
+      __syncthreads();
       bool range_bad = false;
       // KDA: exp(b_last - b) = exp(b_last - b_ref) exp(b_ref - b), the first
       // factor per channel for the chunk; both stay inside e^+-80 (the range
