@@ -117,7 +117,9 @@ class Workload:
     unit = ""
     kernel = ""          # the dominant kernel's name (for the roofline block)
     launches_per_step = 1
-    kern_events = None   # when a list, step() appends (start, end) events around the dominant kernel
+    kern_events = None   # when a dict, step() appends (start, end) events around each timed launch, by tag
+    # the step's other timed launches: tag -> (kernel name, algorithmic bytes per launch)
+    other_launches = {}
 
     def units_per_step(self) -> float: ...
     def algo_bytes_per_step(self) -> float: ...
@@ -125,17 +127,17 @@ class Workload:
         return self.algo_bytes_per_step()
     def step(self, i: int) -> None: ...
 
-    def _k_begin(self):
+    def _k_begin(self, tag="main"):
         if self.kern_events is not None:
             e = torch.cuda.Event(enable_timing=True)
             e.record()
-            self.kern_events.append([e, None])
+            self.kern_events.setdefault(tag, []).append([e, None])
 
-    def _k_end(self):
+    def _k_end(self, tag="main"):
         if self.kern_events is not None:
             e = torch.cuda.Event(enable_timing=True)
             e.record()
-            self.kern_events[-1][1] = e
+            self.kern_events[tag][-1][1] = e
 
 
 def prefill_algo_bytes(dims, lengths, prefixes, warm, gate_mode, es_io, es_out, es_state,
@@ -432,6 +434,11 @@ class DecodeWorkload(Workload):
                 depth[j] = 1 + (depth[pj] if pj >= 0 else 0)
             acc_tokens_tree = float(sum(depth[int(k)] for k in node))
         self.bytes, self.verify_bytes = decode_algo_bytes(dims, B, n_draft, replay)
+        if n_draft > 1:
+            # the commit launch: the replay of the accepted tokens into the slot,
+            # or the copy of the accepted step's state and window out of the buffer
+            self.other_launches = {"commit": ("decode_kernel (replay commit)" if replay else
+                                              "slot_copy_kernel (commit)", self.bytes - self.verify_bytes)}
         if n_draft == 1:
             self.units = B
         else:
@@ -467,10 +474,12 @@ class DecodeWorkload(Workload):
                                slot=self.slot, pos=pos, gate_mode=L.LIN_GATE_PER_KEY,
                                status=self.status)
             self._k_end()
+            self._k_begin("commit")
             L.lin_state_replay_commit(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta,
                                       slot=self.slot, pos=pos, accept_len=self.acc,
                                       track_slot=self.track, track_interval=256,
                                       gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
+            self._k_end("commit")
             return
         elif self.tree:
             self._k_begin()
@@ -478,19 +487,23 @@ class DecodeWorkload(Workload):
                                slot=self.slot, pos=pos, spec=self.specs[r], parent=self.parent,
                                gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
             self._k_end()
+            self._k_begin("commit")
             L.lin_state_spec_commit(p, spec=self.specs[r], slot=self.slot, pos=pos,
                                     n_draft=self.n_draft, track_slot=self.track, track_interval=256,
                                     parent=self.parent, accept_node=self.accept_node,
                                     status=self.status)
+            self._k_end("commit")
         else:
             self._k_begin()
             L.lin_state_decode(p, layer=0, x=x, conv_w=self.conv_w, g=g, beta=beta, out=self.out,
                                slot=self.slot, pos=pos, spec=self.specs[r],
                                gate_mode=L.LIN_GATE_PER_KEY, status=self.status)
             self._k_end()
+            self._k_begin("commit")
             L.lin_state_spec_commit(p, spec=self.specs[r], slot=self.slot, pos=pos,
                                     accept_len=self.acc, n_draft=self.n_draft,
                                     track_slot=self.track, track_interval=256, status=self.status)
+            self._k_end("commit")
 
     def describe(self):
         d = {"batch": self.B, "n_draft": self.n_draft, "pool_slots": 2000,
@@ -502,8 +515,10 @@ class DecodeWorkload(Workload):
 
 class CopyWorkload(Workload):
     """Checkpoint fork/restore copies: Kimi-K3 slots over 69 layers (12 x 128 x 128
-    bf16 + [4608][3] bf16 per layer, 29,039,616 B per slot) in a 256-slot pool,
-    batches of 64 src -> dst pairs (distinct destinations, sources from the rest)."""
+    bf16 + [4608][3] bf16 per layer, 29,039,616 B per slot) in a 128-slot pool
+    (3.7 GB), batches of 64 src -> dst pairs: a random half of the slots are the
+    destinations, the other half the sources, each used once, so every batch
+    reads and writes 64 distinct slots and nothing is read from L2."""
 
     def __init__(self, L, dev, seed=0, n_batches=8, layers=69):
         self.L, self.dev = L, dev
@@ -511,7 +526,8 @@ class CopyWorkload(Workload):
         self.name = f"slot_copy_kimi_k3_{layers}l"
         self.unit = "GB/s"
         self.kernel = "slot_copy"
-        self.pool = L.StatePool(layers, 256, 12, 128, state_dtype=torch.bfloat16,
+        self.n_slots = 128
+        self.pool = L.StatePool(layers, self.n_slots, 12, 128, state_dtype=torch.bfloat16,
                                 conv_dtype=torch.bfloat16, device=dev)
         g = torch.Generator(device=dev)
         g.manual_seed(seed + 5)
@@ -519,9 +535,8 @@ class CopyWorkload(Workload):
         self.pool.conv.view(torch.int16).random_(generator=g)
         self.pairs = []
         for k in range(n_batches):
-            perm = W.randperm(256, seed, f"cp.batch{k}")
-            dst = perm[:64]
-            src = perm[64:][W.randint(0, 191, (64,), seed, f"cp.src{k}")]
+            perm = W.randperm(self.n_slots, seed, f"cp.batch{k}")
+            dst, src = perm[:64], perm[64:128]
             self.pairs.append((src.to(torch.int32).to(dev), dst.to(torch.int32).to(dev)))
         self.slot_bytes = L.lin_state_slot_bytes(self.pool)
         self.bytes = 2.0 * 64 * self.slot_bytes
@@ -540,7 +555,7 @@ class CopyWorkload(Workload):
         self._k_end()
 
     def describe(self):
-        return {"pairs": 64, "layers": self.layers, "pool_slots": 256, "slot_bytes": self.slot_bytes}
+        return {"pairs": 64, "layers": self.layers, "pool_slots": self.n_slots, "slot_bytes": self.slot_bytes}
 
 
 def make_workload(name, L, dev):
@@ -566,6 +581,11 @@ def make_workload(name, L, dev):
         return PrefillWorkload(L, dev, name, W.MAMBA2_HD64, [4096] * 8, [0] * 8, [0] * 8,
                                W.GATE_PER_HEAD, torch.bfloat16, torch.float32, torch.float32,
                                64, 2, "ssd", flags=L.LIN_CONV_SILU | L.LIN_UPDATE_ADDITIVE)
+    if name == "kda_recurrent_prefill":
+        return PrefillWorkload(L, dev, name, W.KIMI_K3_TP8, [2048] * 32, [0] * 32, [0] * 32,
+                               W.GATE_PER_KEY, torch.bfloat16, torch.bfloat16, torch.bfloat16,
+                               256, 2, "softplus",
+                               flags=L.LIN_QK_L2NORM | L.LIN_CONV_SILU | L.LIN_PREFILL_RECURRENT)
     if name == "kda_decode":
         return DecodeWorkload(L, dev, 1)
     if name == "kda_spec_verify4_commit":
@@ -577,8 +597,9 @@ def make_workload(name, L, dev):
     if name == "slot_copy_kimi_k3_69l":
         return CopyWorkload(L, dev)
     if name == "slot_copy_kimi_k3_8l":
-        # the same copies over 8 layers (a 0.86 GB pool): the case profiled
-        # with ncu, whose full capture would otherwise hold the 7.4 GB pool
+        # the same copies over 8 layers (a 0.43 GB pool): the case profiled
+        # with every ncu section; the 69-layer pool (3.7 GB) is captured for
+        # its DRAM counters and duration only
         return CopyWorkload(L, dev, layers=8)
     raise ValueError(name)
 
@@ -587,7 +608,7 @@ HEADLINE = "qwen35_gdn_prefill"
 DEFAULT_EXTRA = ["kimi_k3_kda_varlen_prefill", "kda_decode", "kda_spec_verify4_commit",
                  "kda_spec_verify4_replay", "kda_tree_verify8_commit",
                  "slot_copy_kimi_k3_69l", "kda_long_prefill_131k", "mamba2_ssd_prefill",
-                 "mamba2_ssd_prefill_hd64"]
+                 "mamba2_ssd_prefill_hd64", "kda_recurrent_prefill"]
 
 CONFIG_TEXT = {
     "qwen35_gdn_prefill": "Qwen3.5-style GDN prefill: 1 linear layer, 32 heads, K=V=128, conv 4 over "
@@ -607,9 +628,11 @@ CONFIG_TEXT = {
     "kda_spec_verify4_replay": "KDA speculative verify of 4 drafts (outputs only) + replay commit of "
                                "U{1..4} accepted tokens into the slot, 256 requests, no per-step buffer",
     "slot_copy_kimi_k3_8l": "checkpoint fork/restore copy: Kimi-K3 slot over 8 layers (3,366,912 B), 64 "
-                            "random src->dst pairs per batch in a 256-slot pool (the profiled case)",
+                            "random src->dst pairs per batch over a 128-slot pool, every slot used once "
+                            "(the case profiled with every ncu section)",
     "slot_copy_kimi_k3_69l": "checkpoint fork/restore copy: Kimi-K3 slot over 69 layers (29,039,616 B), "
-                             "64 random src->dst pairs per batch in a 256-slot pool",
+                             "64 random src->dst pairs per batch over a 128-slot pool (3.7 GB), every "
+                             "slot used once",
     "mamba2_ssd_prefill": "Mamba2-style SSD prefill (additive update, no delta correction): 32 heads, "
                           "headdim = d_state = 128, conv 4 + SiLU over x|B|C, no q/k norm, "
                           "dt = softplus(N(0,1)-3), A = -U[1,16] per head, bf16 inputs, fp32 state "
@@ -621,6 +644,10 @@ CONFIG_TEXT = {
                                "snapshot every 64 (ping-pong)",
     "kda_long_prefill_131k": "single-request KDA prefill, 131072 tokens, 12 heads, bf16, cold, "
                              "snapshots every 64 into 2048 distinct track slots",
+    "kda_recurrent_prefill": "KDA prefill on the token-by-token kernel (LIN_PREFILL_RECURRENT, the kernel "
+                             "that also reruns pairs whose decay leaves the chunk's range): Kimi-K3 TP8 "
+                             "shard, 12 heads, K=V=128, bf16, 32 requests x 2048 tokens, cold, snapshots "
+                             "every 256 (ping-pong)",
 }
 
 
@@ -629,8 +656,8 @@ def flush_l2(buf):
 
 
 def time_steps(wl, steps, warmup, stream, flush=None):
-    """Returns (total_ms over `steps`, per-step ms list, per-launch ms list of
-    the dominant kernel). The timed steps are queued behind a short device-side
+    """Returns (total_ms over `steps`, per-step ms list, per-launch ms lists of
+    the timed launches by tag, "main" the dominant kernel). The timed steps are queued behind a short device-side
     sleep so the host enqueues them ahead of the GPU: no step waits on the
     host, and the events measure device time only."""
     for i in range(warmup):
@@ -640,7 +667,7 @@ def time_steps(wl, steps, warmup, stream, flush=None):
            for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    wl.kern_events = []
+    wl.kern_events = {}
     torch.cuda._sleep(int(min(steps, 200) * 300e3))  # ~0.15 ms of host enqueue time per step at 2 GHz
     t0.record(stream)
     for i in range(steps):
@@ -652,7 +679,7 @@ def time_steps(wl, steps, warmup, stream, flush=None):
     t1.record(stream)
     torch.cuda.synchronize()
     per = [a.elapsed_time(b) for a, b in evs]
-    kern = [a.elapsed_time(b) for a, b in wl.kern_events]
+    kern = {tag: [a.elapsed_time(b) for a, b in ev] for tag, ev in wl.kern_events.items()}
     wl.kern_events = None
     return t0.elapsed_time(t1), per, kern
 
@@ -677,7 +704,7 @@ def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=Fals
     flush_buf = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device=dev) if need_flush else None
     total_ms, per, kern = time_steps(wl, steps, warmup, stream,
                                      (lambda: flush_l2(flush_buf)) if need_flush else None)
-    kern_ms = statistics.mean(kern)
+    kern_ms = statistics.mean(kern["main"])
     rank_ms, value = reduce_over_ranks(statistics.mean(per), wl.units_per_step(), dist_info["world"], dev)
     units = wl.units_per_step() * dist_info["world"]
     achieved = wl.kernel_bytes_per_launch() / (kern_ms / 1e3) / 1e9
@@ -689,6 +716,14 @@ def run_workload(name, L, dev, steps, warmup, peaks, stream, dist_info, e2e=Fals
                         "kernel_ms": kern_ms},
            "config": {"workload": CONFIG_TEXT[name], **wl.describe()},
            "gpu_launches": wl.launches_per_step * steps}
+    if wl.other_launches:
+        # the step's other launches, each against the same peak
+        res["other_launches"] = {}
+        for tag, (kname, kbytes) in wl.other_launches.items():
+            ms = statistics.mean(kern[tag])
+            ach = kbytes / (ms / 1e3) / 1e9
+            res["other_launches"][tag] = {"kernel": kname, "kernel_ms": ms, "algo_bytes_per_launch": kbytes,
+                                          "achieved": ach, "frac": ach / peaks["hbm_gbs"]}
     if hasattr(wl, "acc_tokens"):
         res["accepted_tok_s"] = wl.acc_tokens * dist_info["world"] / (rank_ms / 1e3)
     if e2e and hasattr(wl, "setup_e2e"):
@@ -921,6 +956,7 @@ CPU_LEGS = {
     "mamba2_ssd_prefill_hd64": lambda wl: cpu_prefill(wl, 8192),
     "kimi_k3_kda_varlen_prefill": lambda wl: cpu_prefill(wl, 40000),
     "kda_long_prefill_131k": lambda wl: cpu_prefill(wl, 24576),
+    "kda_recurrent_prefill": lambda wl: cpu_prefill(wl, 16384),
     "kda_decode": lambda wl: cpu_decode(wl, 8),
     "kda_spec_verify4_commit": lambda wl: cpu_decode(wl, 3),
     "kda_spec_verify4_replay": lambda wl: cpu_decode(wl, 3),
@@ -1037,6 +1073,7 @@ def main():
                                  "4 pool replicas (432 MB touched per rotation) so no step finds its "
                                  "state in L2"},
                 "roofline": {**head["roofline"], "peak_source": peaks["source"]},
+                **({"other_launches": head["other_launches"]} if "other_launches" in head else {}),
                 "cpu_baseline": head.get("cpu_baseline"),
                 "e2e": head.get("e2e"),
                 "gpu_launches": head["gpu_launches"],

@@ -217,6 +217,10 @@ struct DecodeParams {
   lin_state_pool_t pool;
   lin_decode_args_t a;
   const int32_t* accept;  // replay commit: accepted tokens per request (NULL: decode / verify)
+  // replay commit: byte offsets in dynamic shared memory of the request order
+  // (int16 [batch]) and its histogram (int [n_draft + 1]); order_off 0: the
+  // batch's own order
+  int order_off, hist_off;
 };
 
 constexpr uint32_t kDecWaitTries = 1u << 24;
@@ -390,12 +394,50 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
     for (int s = 0; s < kDecMaxStages; ++s) issued_n[s] = -1;
     int n = 0;
     bool abort = false;
+    // replay commit: the requests ordered by accepted tokens, most first (ties
+    // in request order; a count outside [0, n_draft] counts as 0). Items are
+    // dealt to the CTAs round-robin, so every CTA then gets about the same
+    // number of token passes rather than a random sum of accept lengths.
+    const int16_t* order = nullptr;
+    if (MODE == kDecReplay && p.order_off > 0) {
+      int16_t* ord = reinterpret_cast<int16_t*>(dsm + p.order_off);
+      int* hist = reinterpret_cast<int*>(dsm + p.hist_off);
+      const int nb = a.batch;
+      auto acc_of = [&](int rr) {
+        const int v = p.accept[rr];
+        return (v < 0 || v > ND) ? 0 : v;
+      };
+      for (int v = lane; v <= ND; v += 32) hist[v] = 0;
+      __syncwarp();
+      for (int rr = lane; rr < nb; rr += 32) atomicAdd(&hist[acc_of(rr)], 1);
+      __syncwarp();
+      if (lane == 0) {
+        int run = 0;  // requests with more accepted tokens than v come first
+        for (int v = ND; v >= 0; --v) {
+          const int c = hist[v];
+          hist[v] = run;
+          run += c;
+        }
+      }
+      __syncwarp();
+      for (int r0 = 0; r0 < nb; r0 += 32) {
+        const int rr = r0 + lane;
+        const int v = rr < nb ? acc_of(rr) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, v);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        if (rr < nb) ord[hist[v] + before] = static_cast<int16_t>(rr);
+        __syncwarp();
+        if (rr < nb && before == 0) hist[v] += __popc(peers);
+        __syncwarp();
+      }
+      order = ord;
+    }
     for (int base = blockIdx.x; base < n_items && !abort; base += 32 * gridDim.x) {
       // lane l looks up item base + l * gridDim.x, so 32 lookups overlap
       const int item = base + lane * gridDim.x;
       DecMeta m{0, 0, -1, -1, 0, 0, 0};
       if (item < n_items) {
-        m.r = item / H;
+        m.r = order ? order[item / H] : item / H;
         m.h = item % H;
         m.slot = a.slot[m.r];
         m.ts = a.track_slot ? a.track_slot[m.r] : -1;
@@ -628,8 +670,11 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
                 win[pt][0] = a3 >= 0 ? xr(a3) : (a2 >= 0 ? s2 : (a1 >= 0 ? s1 : s0));
               }
               const float xin = load_elem(sx, cl, a.io_dtype);
-              const float y = w[pt][0] * win[pt][0] + w[pt][1] * win[pt][1] + w[pt][2] * win[pt][2] +
-                              w[pt][3] * xin;
+              // the replay commit writes no outputs: no q (its window still moves)
+              const float y = (REPLAY && pt == 0)
+                                  ? 0.f
+                                  : w[pt][0] * win[pt][0] + w[pt][1] * win[pt][1] + w[pt][2] * win[pt][2] +
+                                        w[pt][3] * xin;
               win[pt][0] = win[pt][1];
               win[pt][1] = win[pt][2];
               win[pt][2] = round_to_dtype(xin, pool.conv_dtype);
@@ -641,7 +686,7 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
                   if (tcv) store_elem(tcv, ch * 3 + q, pool.conv_dtype, win[pt][q]);
                 }
               }
-              gys[jj * C::CH + cl] = silu_on ? silu(y) : y;
+              if (!(REPLAY && pt == 0)) gys[jj * C::CH + cl] = silu_on ? silu(y) : y;
             }
           }
           if (MODE != kDecTree && j0 + gn < ND) {  // the next group starts from this window
@@ -663,14 +708,14 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
         if (warp < NPW) {
           // this warp's partial q.q, k.k, q.k of each draft (its own conv outputs)
           for (int jj = 0; jj < nl; ++jj) {
-            const float yq = t < D ? gys[jj * C::CH + t] : 0.f;
+            const float yq = (t < D && !REPLAY) ? gys[jj * C::CH + t] : 0.f;
             const float yk = t < D ? gys[jj * C::CH + D + t] : 0.f;
             float pqq = yq * yq, pkk = yk * yk, pqk = yq * yk;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-              pqq += __shfl_xor_sync(0xffffffffu, pqq, o);
+              if (!REPLAY) pqq += __shfl_xor_sync(0xffffffffu, pqq, o);
               pkk += __shfl_xor_sync(0xffffffffu, pkk, o);
-              pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+              if (!REPLAY) pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
             }
             if (lane == 0) {
               float* nr = gnr + (jj * NPW + warp) * 3;
@@ -735,9 +780,14 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
             const uint64_t rq2 = f2pack(rq, rq), rk2 = f2pack(rk, rk);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const float4 fq = yq4[h2], fk = yk4[h2];
-              q2[2 * h2] = fmul2(f2pack(fq.x, fq.y), rq2);
-              q2[2 * h2 + 1] = fmul2(f2pack(fq.z, fq.w), rq2);
+              const float4 fk = yk4[h2];
+              if (REPLAY) {
+                q2[2 * h2] = q2[2 * h2 + 1] = 0ull;
+              } else {
+                const float4 fq = yq4[h2];
+                q2[2 * h2] = fmul2(f2pack(fq.x, fq.y), rq2);
+                q2[2 * h2 + 1] = fmul2(f2pack(fq.z, fq.w), rq2);
+              }
               k2[2 * h2] = fmul2(f2pack(fk.x, fk.y), rk2);
               k2[2 * h2 + 1] = fmul2(f2pack(fk.z, fk.w), rk2);
             }
@@ -771,10 +821,10 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
               for (int e2 = 0; e2 < 4; ++e2) {
                 sv[i][e2] = fmul2(sv[i][e2], a2[e2]);
                 dk2 = ffma2(sv[i][e2], k2[e2], dk2);
-                dq2 = ffma2(sv[i][e2], q2[e2], dq2);
+                if (!REPLAY) dq2 = ffma2(sv[i][e2], q2[e2], dq2);
               }
               red[2 * i] = f2sum(dk2);
-              red[2 * i + 1] = f2sum(dq2);
+              red[2 * i + 1] = REPLAY ? 0.f : f2sum(dq2);
             }
             // transposing butterfly, as in the one-token path
 #pragma unroll
@@ -1149,7 +1199,7 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
                                                           : kDecStates;
   static DecodeLaunchCache caches[5];  // indexed by DecMode
   DecodeLaunchCache& cache = caches[mode];
-  DecodeParams p{pool, a, accept};
+  DecodeParams p{pool, a, accept, 0, 0};
   const int stage = decode_stage_bytes(pool, a);
   if (stage > kDecodeMaxStage) return cudaErrorInvalidValue;
   // two CTAs per SM when two stages each fit, else one CTA with two stages
@@ -1168,6 +1218,13 @@ cudaError_t decode_launch(const lin_state_pool_t& pool, const lin_decode_args_t&
     while (group > 1 && smem + gbytes(group) > budget) --group;
     smem += gbytes(group);
     if (smem > kDecMaxDynSmem) return cudaErrorInvalidValue;
+    // the replay commit's request order, where it fits the same budget
+    const int obytes = ((2 * a.batch + 15) & ~15) + ((4 * (a.n_draft + 1) + 15) & ~15);
+    if (mode == kDecReplay && a.batch <= 32767 && smem + obytes <= budget) {
+      p.order_off = smem;
+      p.hist_off = smem + ((2 * a.batch + 15) & ~15);
+      smem += obytes;
+    }
   }
   auto kern = mode == kDecReplay        ? decode_kernel<D, V, ST, kDecReplay>
               : mode == kDecTree        ? decode_kernel<D, V, ST, kDecTree>

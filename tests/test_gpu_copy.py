@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import bench
 import linear_attention_state_chunked_gb300 as L
 import workloads as W
 from oracle import lin_state_oracle as O
@@ -62,6 +63,25 @@ def test_restore_matches_oracle():
     assert his.cpu().tolist() == ohis.tolist() == [1, 0, 7, 7, 0, 1]
     assert np.array_equal(np64(pool.temporal), op["temporal"])
     assert np.array_equal(np64(pool.conv), op["conv"])
+
+
+def test_copy_bench_workload_full_size():
+    """The benchmark's copy workload as it is timed: 64 pairs of 69-layer
+    Kimi-K3 slots over a 128-slot pool, each slot used once. Every destination
+    holds its source's bytes from before the call; nothing else changes."""
+    wl = bench.make_workload("slot_copy_kimi_k3_69l", L, DEV)
+    before_t = wl.pool.temporal.clone()
+    before_c = wl.pool.conv.clone()
+    src, dst = wl.pairs[0]
+    assert len(set(src.tolist()) | set(dst.tolist())) == 128
+    wl.step(0)
+    torch.cuda.synchronize()
+    assert L.lin_state_read_status(wl.status) == 0
+    exp_t, exp_c = before_t.clone(), before_c.clone()
+    exp_t[:, dst.long()] = before_t[:, src.long()]
+    exp_c[:, dst.long()] = before_c[:, src.long()]
+    assert torch.equal(wl.pool.temporal.view(torch.int16), exp_t.view(torch.int16))
+    assert torch.equal(wl.pool.conv.view(torch.int16), exp_c.view(torch.int16))
 
 
 def test_copy_engine_kimi_k3_full_size():

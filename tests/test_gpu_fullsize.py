@@ -103,6 +103,14 @@ def test_kimi_k3_kda_varlen_full_size_sampled():
     check_prefill_slice(wl2, warm[0], [0], TOL_BF16)
 
 
+def test_kda_recurrent_prefill_full_size_sampled():
+    """The token-by-token kernel at the benchmark's size: a sampled request
+    and heads against the oracle."""
+    wl = bench.make_workload("kda_recurrent_prefill", L, DEV)
+    assert wl.kernel_kind == L.LIN_KERNEL_RECURRENT
+    check_prefill_slice(wl, 17, [2, 9], TOL_BF16)
+
+
 def test_kimi_k3_kda_varlen_fp32_state_full_size_sampled():
     """The Kimi-K3 varlen workload (32 requests of U{1k..16k} tokens, half warm
     at a 64-multiple prefix, per-key decay, snapshots every 256) with an fp32
