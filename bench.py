@@ -781,13 +781,29 @@ def _code_only(src):
     return "\n".join(line for line in lines if line)
 
 
-def library_source_hash():
-    """Digest of the CUDA library sources (csrc and the C header), comments and
-    whitespace left out: a traffic figure is reported only while the code of
-    the kernels it was measured on is unchanged."""
+# The source files each kernel family is built from (besides the shared
+# headers, the ABI layer and the C header, which count for all of them).
+KERNEL_SOURCES = {
+    "chunked": ["chunked_prefill.cu", "umma.cuh"],
+    "token": ["token_kernels.cu"],
+    "verify_chunk": ["verify_chunk.cu"],
+    "copy": ["copy_kernels.cu"],
+}
+SHARED_SOURCES = ["common.cuh", "internal.h", "api.cu"]
+
+
+def library_source_hash(family=None):
+    """Digest of the CUDA library sources, comments and whitespace left out:
+    of one kernel family's files plus the shared ones, or of every source
+    (family None). A traffic figure is reported only while the code of the
+    kernel it was measured on is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_state_chunked_gb300", "csrc")
-    files = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh", ".h"))]
+    if family is None:
+        names = [f for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh", ".h"))]
+    else:
+        names = sorted(KERNEL_SOURCES[family] + SHARED_SOURCES)
+    files = [os.path.join(csrc, f) for f in names]
     files.append(os.path.join(ROOT, "include", "lin_state.h"))
     for f in files:
         h.update(os.path.basename(f).encode())
@@ -799,15 +815,14 @@ def library_source_hash():
 def measured_traffic(workload):
     """dram__bytes_read.sum + dram__bytes_write.sum per launch of the workload's
     dominant kernel, from the capture table profiles/dram_traffic.json, or None
-    when there is no row or the row was measured on other library sources."""
+    when there is no row or the row's kernel family has changed since."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
-    cur = library_source_hash()
     with open(path) as fh:
         rows = json.load(fh).get("rows", [])
     for row in rows:
-        if row.get("workload") == workload and row.get("library_source") == cur:
+        if row.get("workload") == workload and row.get("library_source") == library_source_hash(row.get("family")):
             return int(row["traffic_per_launch"])
     return None
 

@@ -63,22 +63,21 @@ struct TokSmem {
 };
 
 // Conv + activation for one token: each thread does its own channels and
-// keeps the window win[c][0..2] (oldest first) in registers.
+// keeps the window win[c][0..2] (oldest first) in registers; the token's
+// inputs are already in registers too.
 template <int D, int V>
-__device__ __forceinline__ void conv_token(float (&win)[TokCfg<D, V>::CPT][3],
-                                           const float (&w)[TokCfg<D, V>::CPT][4],
-                                           const void* x, int64_t xrow, const int (&chan)[TokCfg<D, V>::CPT],
-                                           int io_dtype, bool do_silu, float* ys) {
+__device__ __forceinline__ void conv_token_in(float (&win)[TokCfg<D, V>::CPT][3],
+                                              const float (&w)[TokCfg<D, V>::CPT][4],
+                                              const float (&xin)[TokCfg<D, V>::CPT], bool do_silu, float* ys) {
   using C = TokCfg<D, V>;
 #pragma unroll
   for (int i = 0; i < C::CPT; ++i) {
     const int cl = threadIdx.x + i * C::NT;
     if (cl < C::CH) {
-      const float xin = load_elem(x, xrow + chan[i], io_dtype);
-      float y = w[i][0] * win[i][0] + w[i][1] * win[i][1] + w[i][2] * win[i][2] + w[i][3] * xin;
+      float y = w[i][0] * win[i][0] + w[i][1] * win[i][1] + w[i][2] * win[i][2] + w[i][3] * xin[i];
       win[i][0] = win[i][1];
       win[i][1] = win[i][2];
-      win[i][2] = xin;
+      win[i][2] = xin[i];
       if (do_silu) y = silu(y);
       ys[cl] = y;
     }
@@ -153,20 +152,6 @@ __device__ __forceinline__ void rows_update(float (&s)[TokCfg<D, V>::RPT][8], co
     }
     o = row_sum<C::LPR>(o);
     if (lr == 0) store_elem(out, orow + row, out_dtype, o);
-  }
-}
-
-template <int D>
-__device__ __forceinline__ void load_alpha(float (&a8)[8], const float* g, int64_t gbase,
-                                           int gate_mode) {
-  const int lr = threadIdx.x % TokCfg<D>::LPR;
-  if (gate_mode == LIN_GATE_PER_KEY) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) a8[e] = expf(g[gbase + lr * 8 + e]);
-  } else {
-    const float a = expf(g[gbase]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) a8[e] = a;
   }
 }
 
@@ -1074,7 +1059,7 @@ struct PrefillParams {
 };
 
 template <int D, int V, int ST>
-__global__ void __launch_bounds__(TokCfg<D, V>::NT) prefill_recurrent_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(TokCfg<D, V>::NT, 2) prefill_recurrent_kernel(PrefillParams p) {
   using C = TokCfg<D, V>;
   __shared__ TokSmem<D, V> sm;
   const lin_state_pool_t& pool = p.pool;
@@ -1153,17 +1138,51 @@ __global__ void __launch_bounds__(TokCfg<D, V>::NT) prefill_recurrent_kernel(Pre
   }
 
   const float dmul = (a.flags & LIN_UPDATE_ADDITIVE) ? 0.f : 1.f;
+  const bool per_key = a.gate_mode == LIN_GATE_PER_KEY;
+  const int lr = threadIdx.x % C::LPR;
+  // a token's inputs (this thread's conv inputs, its 8 log decays or the
+  // head's one, beta), loaded a token ahead so their latency hides behind
+  // the current token's arithmetic
+  float xn[C::CPT], gn[8], bn = 0.f;
+  auto load_inputs = [&](int64_t t) {
+#pragma unroll
+    for (int i = 0; i < C::CPT; ++i) {
+      const int cl = threadIdx.x + i * C::NT;
+      xn[i] = cl < C::CH ? load_elem(a.x, t * C_all + chan[i], a.io_dtype) : 0.f;
+    }
+    if (per_key) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gn[e] = a.g[(t * H + h) * D + lr * 8 + e];
+    } else {
+      gn[0] = a.g[t * H + h];
+    }
+    bn = a.beta[t * H + h];
+  };
+  if (bos < eos) load_inputs(bos);
   int snap = 0;
   for (int64_t t = bos; t < eos; ++t) {
+    float xc[C::CPT], gc[8];
+#pragma unroll
+    for (int i = 0; i < C::CPT; ++i) xc[i] = xn[i];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) gc[e] = gn[e];
+    const float beta = bn;
+    if (t + 1 < eos) load_inputs(t + 1);
     float* ys = sm.y[(t - bos) & 1];
-    conv_token<D, V>(win, w, a.x, t * C_all, chan, a.io_dtype, a.flags & LIN_CONV_SILU, ys);
+    conv_token_in<D, V>(win, w, xc, a.flags & LIN_CONV_SILU, ys);
     __syncthreads();
     qk_norms<D, V>(ys, a.flags & LIN_QK_L2NORM);
     __syncthreads();
     float a8[8];
-    const int64_t gbase = a.gate_mode == LIN_GATE_PER_KEY ? (t * H + h) * D : t * H + h;
-    load_alpha<D>(a8, a.g, gbase, a.gate_mode);
-    rows_update<D, V>(s, ys, a8, a.beta[t * H + h], dmul, a.q_scale, a.out, (t * H + h) * V, a.out_dtype);
+    if (per_key) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a8[e] = expf(gc[e]);
+    } else {
+      const float av = expf(gc[0]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a8[e] = av;
+    }
+    rows_update<D, V>(s, ys, a8, beta, dmul, a.q_scale, a.out, (t * H + h) * V, a.out_dtype);
     const int64_t n = P + (t - bos) + 1;
     if (nt > 0 && n % a.track_stride == 0) {
       const int dst = a.track_slots[t0 + (snap % nt)];

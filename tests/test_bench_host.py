@@ -17,6 +17,16 @@ def test_source_digest_ignores_comments_and_whitespace_only():
 
 
 
+def test_source_digest_per_kernel_family():
+    """A traffic row is keyed on its kernel family's sources: the digest of
+    one family covers its own files and the shared ones, and differs between
+    families and from the whole library's."""
+    fams = {f: bench.library_source_hash(f) for f in bench.KERNEL_SOURCES}
+    assert len(set(fams.values())) == len(fams)
+    assert bench.library_source_hash() not in fams.values()
+    assert bench.library_source_hash("chunked") == bench.library_source_hash("chunked")
+
+
 def test_decode_and_verify_bytes_are_the_component_sums():
     """KDA decode at Kimi-K3 TP8 shard shapes (12 heads x 128, bf16, per-key
     gates): per request-step the state read and written (2 x 393,216), the
