@@ -120,7 +120,6 @@ struct Pair8<LIN_F32> {
     q[0] = make_ulonglong2(v[0], v[1]);
     q[1] = make_ulonglong2(v[2], v[3]);
   }
-  static __device__ __forceinline__ void round(uint64_t (&)[4]) {}
 };
 
 template <>
@@ -140,13 +139,6 @@ struct Pair8<LIN_BF16> {
   }
   static __device__ __forceinline__ void store(void* p, const uint64_t (&v)[4]) {
     *reinterpret_cast<uint4*>(p) = make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3]));
-  }
-  static __device__ __forceinline__ void round(uint64_t (&v)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t b = pack(v[i]);
-      v[i] = f2pack(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
-    }
   }
 };
 

@@ -851,10 +851,9 @@ __global__ void __launch_bounds__(DecPCfg<D, V>::NT, 2)
               for (int e2 = 0; e2 < 4; ++e2) sv[i][e2] = ffma2(u2, k2[e2], sv[i][e2]);
               if (dt) Pair8<ST>::store(dt + off, sv[i]);
               if (tt) Pair8<ST>::store(tt + off, sv[i]);
-              if (ND > 1) {
-                Pair8<ST>::round(sv[i]);  // the next draft starts from the stored state
-                Pair8<ST>::store(sst + off, sv[i]);
-              }
+              // the next draft starts from the stored (rounded) state: the
+              // store to the stage rounds as the others do
+              if (ND > 1) Pair8<ST>::store(sst + off, sv[i]);
             }
           }
         }
