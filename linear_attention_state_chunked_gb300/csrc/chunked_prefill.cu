@@ -1541,50 +1541,113 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // S_{k+1} = S_k M_k + B_k for k = 1 .. nseg - 2, where buf[k] holds B_k on entry
 // (buf[0] holds S_1, the offset run of segment 0 from the request's own initial
 // state) and S_{k+1} on exit, and mbuf[k] holds M_k. Rows of S evolve
-// independently, so CTA (head, 16-row block) runs the whole scan for its rows.
+// independently, so CTA (head, 16-row block) runs the whole scan for its rows:
+// each warp owns 4 rows and each lane 4 columns (16 fp32 sums), so every M_k
+// value read from shared memory feeds 4 rows and every S_k value (the same for
+// the whole warp) 4 columns. M_{k+1} lands by a bulk copy into the other of
+// two buffers while step k computes. Each sum adds the terms in key order, as
+// a plain row-by-matrix product does.
 constexpr int kScanRows = 16;
-constexpr int kScanThreads = 256;
-constexpr size_t kScanSmem = (size_t(DH) * DH + size_t(kScanRows) * DH) * sizeof(float);
+constexpr int kScanThreads = 128;  // 4 warps x 4 rows
+constexpr size_t kScanSmem = (2 * size_t(DH) * DH + size_t(kScanRows) * DH) * sizeof(float);
 
-__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(float* buf, const float* mbuf, int nseg, int H) {
+__global__ void __launch_bounds__(kScanThreads)
+    seg_scan_kernel(float* buf, const float* mbuf, int nseg, int H, int32_t* status) {
   extern __shared__ __align__(16) float ssm[];
-  float* Msh = ssm;             // M_k, 128 x 128
-  float* Ssh = ssm + DH * DH;   // this CTA's rows of S_k, 16 x 128
+  __shared__ uint64_t mbar[2];
+  __shared__ int ok_sh;
+  float* Ssh = ssm + 2 * DH * DH;  // this CTA's rows of S_k, 16 x 128
   const int h = blockIdx.x / (DH / kScanRows), rb = blockIdx.x % (DH / kScanRows);
-  const int tid = threadIdx.x;
-  const int row = tid / 16, c0 = (tid % 16) * 8;  // one row, 8 columns per thread
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = warp * 4, c0 = lane * 4;  // this thread's rows (of the CTA's 16) and columns
   const int64_t head_elems = int64_t(DH) * DH;
   auto at = [&](const float* base, int k) { return base + (int64_t(k) * H + h) * head_elems; };
   auto atw = [&](float* base, int k) { return base + (int64_t(k) * H + h) * head_elems; };
+  if (tid == 0) {
+    ok_sh = 1;
+    umma::mbar_init(&mbar[0], 1);
+    umma::mbar_init(&mbar[1], 1);
+    umma::mbar_fence_init();
+  }
   for (int i = tid; i < kScanRows * DH / 4; i += kScanThreads)
     reinterpret_cast<float4*>(Ssh)[i] = reinterpret_cast<const float4*>(at(buf, 0) + int64_t(rb) * kScanRows * DH)[i];
+  __syncthreads();
+  constexpr uint32_t kMBytes = DH * DH * sizeof(float);
+  auto issue = [&](int k) {  // thread 0: M_k into buffer k & 1
+    const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[k & 1]));
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(ssm + (k & 1) * DH * DH));
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kMBytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(at(mbuf, k)), "r"(kMBytes), "r"(bar)
+                 : "memory");
+  };
+  // thread 0's bookkeeping: each buffer's next phase, and whether a copy into
+  // it is in flight
+  uint32_t phase[2] = {0u, 0u};
+  bool pend[2] = {false, false};
+  if (tid == 0 && nseg > 2) {
+    issue(1);
+    pend[1] = true;
+  }
   for (int k = 1; k + 1 < nseg; ++k) {
-    const float4* msrc = reinterpret_cast<const float4*>(at(mbuf, k));
-    for (int i = tid; i < DH * DH / 4; i += kScanThreads) reinterpret_cast<float4*>(Msh)[i] = msrc[i];
-    float* brow = atw(buf, k) + int64_t(rb * kScanRows + row) * DH + c0;
-    const float4 b0 = reinterpret_cast<const float4*>(brow)[0], b1 = reinterpret_cast<const float4*>(brow)[1];
-    float acc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const int bi = k & 1;
+    // the other buffer's last reader was step k - 1, which every thread finished
+    if (tid == 0 && k + 2 < nseg) {
+      issue(k + 1);
+      pend[bi ^ 1] = true;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 bv = *reinterpret_cast<const float4*>(atw(buf, k) + int64_t(rb * kScanRows + r0 + i) * DH + c0);
+      acc[i][0] = bv.x;
+      acc[i][1] = bv.y;
+      acc[i][2] = bv.z;
+      acc[i][3] = bv.w;
+    }
+    if (tid == 0) {
+      if (umma::mbar_wait(&mbar[bi], phase[bi], kWaitTries)) {
+        phase[bi] ^= 1u;
+        pend[bi] = false;
+      } else {
+        ok_sh = 0;
+        if (status) atomicOr(status, LIN_ST_TIMEOUT);
+      }
+    }
     __syncthreads();
-#pragma unroll 4
-    for (int m = 0; m < DH; ++m) {
-      const float sv = Ssh[row * DH + m];
-      const float4 m0 = *reinterpret_cast<const float4*>(Msh + m * DH + c0);
-      const float4 m1 = *reinterpret_cast<const float4*>(Msh + m * DH + c0 + 4);
-      acc[0] = fmaf(sv, m0.x, acc[0]);
-      acc[1] = fmaf(sv, m0.y, acc[1]);
-      acc[2] = fmaf(sv, m0.z, acc[2]);
-      acc[3] = fmaf(sv, m0.w, acc[3]);
-      acc[4] = fmaf(sv, m1.x, acc[4]);
-      acc[5] = fmaf(sv, m1.y, acc[5]);
-      acc[6] = fmaf(sv, m1.z, acc[6]);
-      acc[7] = fmaf(sv, m1.w, acc[7]);
+    if (!ok_sh) break;
+    const float* Msh = ssm + bi * DH * DH;
+#pragma unroll 2
+    for (int m = 0; m < DH; m += 4) {
+      float4 sv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sv[i] = *reinterpret_cast<const float4*>(Ssh + (r0 + i) * DH + m);
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        const float4 mv = *reinterpret_cast<const float4*>(Msh + (m + mm) * DH + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float s = mm == 0 ? sv[i].x : mm == 1 ? sv[i].y : mm == 2 ? sv[i].z : sv[i].w;
+          acc[i][0] = fmaf(s, mv.x, acc[i][0]);
+          acc[i][1] = fmaf(s, mv.y, acc[i][1]);
+          acc[i][2] = fmaf(s, mv.z, acc[i][2]);
+          acc[i][3] = fmaf(s, mv.w, acc[i][3]);
+        }
+      }
     }
     __syncthreads();  // every read of S_k and M_k is done
-    reinterpret_cast<float4*>(Ssh + row * DH + c0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    reinterpret_cast<float4*>(Ssh + row * DH + c0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    reinterpret_cast<float4*>(brow)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    reinterpret_cast<float4*>(brow)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 o = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(Ssh + (r0 + i) * DH + c0) = o;
+      *reinterpret_cast<float4*>(atw(buf, k) + int64_t(rb * kScanRows + r0 + i) * DH + c0) = o;
+    }
     __syncthreads();
+  }
+  if (!ok_sh && tid == 0) {
+    // copies may still be landing: wait for them (bounded) before exit
+    for (int b = 0; b < 2; ++b)
+      if (pend[b]) umma::mbar_wait(&mbar[b], phase[b], kWaitTries);
   }
 }
 
@@ -1701,7 +1764,7 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
       if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kScanSmem))) != cudaSuccess)
         return e;
-      seg_scan_kernel<<<H * (DH / kScanRows), kScanThreads, kScanSmem, s>>>(bbuf, mbuf, sp.nseg, int(H));
+      seg_scan_kernel<<<H * (DH / kScanRows), kScanThreads, kScanSmem, s>>>(bbuf, mbuf, sp.nseg, int(H), a.status);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     ChunkParams p3{pool, a, nullptr, kSegFinal, sp.seg_len, 1, sp.nseg, nullptr, nullptr, bbuf, redo};

@@ -134,7 +134,12 @@ __device__ __forceinline__ float ld_smem_elem(const uint8_t* base, int i, int es
 struct VerParams {
   lin_state_pool_t pool;
   lin_decode_args_t a;
+  int resident;  // CTAs resident at once: the item one wave ahead is blockIdx.x + resident
 };
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 template <int K, int V, int ST, bool KDA>
 __global__ void __launch_bounds__(VT, ST == LIN_BF16 ? 4 : 2) verify_chunk_kernel(const VerParams prm) {
@@ -241,6 +246,39 @@ __global__ void __launch_bounds__(VT, ST == LIN_BF16 ? 4 : 2) verify_chunk_kerne
       } else {
         const int j = q - 6 - 3 * D;
         bulk_g2s(smem_addr(vsm + L.gs) + j * K * 4, a.g + ((int64_t(r) * D + j) * H + h) * K, K * 4, bi);
+      }
+    }
+  }
+  // The CTAs run in waves of `resident`, each waiting first for its inputs
+  // from HBM: the last warp has L2 fetch the inputs of the item one wave
+  // ahead (state rows, window, the drafts' x rows and per-key gates), so that
+  // CTA finds them in L2.
+  if (warp == VT / 32 - 1) {
+    const int nx = static_cast<int>(blockIdx.x) + prm.resident;
+    if (prm.resident > 0 && nx < a.batch * H) {
+      const int r1 = nx / H, h1 = nx % H;
+      const int s1 = a.slot[r1];
+      if (s1 >= 0 && s1 < pool.num_slots) {
+        const char* t1 = static_cast<const char*>(pool.temporal) + a.layer * pool.temporal_layer_stride +
+                         s1 * pool.temporal_slot_stride + int64_t(h1) * C::SBYTES;
+        const char* c1 = static_cast<const char*>(pool.conv) + a.layer * pool.conv_layer_stride +
+                         s1 * pool.conv_slot_stride;
+        auto c0_1 = [&](int pp) { return pp == 0 ? h1 * K : pp == 1 ? H * K + h1 * K : 2 * H * K + h1 * V; };
+        const int nq = 1 + 3 + 3 * D + (KDA ? D : 0);
+        for (int q = lane; q < nq; q += 32) {
+          if (q == 0) {
+            prefetch_l2(t1, C::SBYTES);
+          } else if (q < 4) {
+            prefetch_l2(c1 + int64_t(c0_1(q - 1)) * 3 * ces, part_n(q - 1) * 3 * ces);
+          } else if (q < 4 + 3 * D) {
+            const int j = (q - 4) / 3, pp = (q - 4) % 3;
+            prefetch_l2(static_cast<const char*>(a.x) + ((int64_t(r1) * D + j) * C_all + c0_1(pp)) * ies,
+                        part_n(pp) * ies);
+          } else {
+            const int j = q - 4 - 3 * D;
+            prefetch_l2(a.g + ((int64_t(r1) * D + j) * H + h1) * K, K * 4);
+          }
+        }
       }
     }
   }
@@ -449,7 +487,10 @@ cudaError_t verify_chunk_launch(const lin_state_pool_t& pool, const lin_decode_a
   auto kern = kda ? verify_chunk_kernel<K, V, ST, true> : verify_chunk_kernel<K, V, ST, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  VerParams p{pool, a};
+  int dev = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, VT, smem)) != cudaSuccess) return e;
+  VerParams p{pool, a, per_sm * device_sm_count(dev)};
   kern<<<static_cast<unsigned>(a.batch) * pool.num_heads, VT, smem, stream>>>(p);
   return cudaGetLastError();
 }
