@@ -118,40 +118,72 @@ __device__ __forceinline__ void qk_norms(float* ys, bool l2) {
   }
 }
 
-// Update this thread's rows for one token; writes o for the rows it leads.
+// Update this thread's rows for one token and write their outputs. Both row
+// dot products are taken on the decayed state, d_k = (S A) k and d_q = (S A) q,
+// so o = S' q = d_q + u (k . q) needs no second pass over the updated row. The
+// 2 x RPT sums of the thread's rows are reduced across the row's LPR lanes by
+// one transposing butterfly: at each level a lane keeps half of its values and
+// sends the other half, so sum m ends whole in lane m / (LPR / (2 RPT)).
 template <int D, int V>
 __device__ __forceinline__ void rows_update(float (&s)[TokCfg<D, V>::RPT][8], const float* ys,
                                             const float (&a8)[8], float beta, float dmul,
                                             float q_scale, void* out, int64_t orow, int out_dtype) {
   using C = TokCfg<D, V>;
+  constexpr int NV = 2 * C::RPT;      // sums per thread: d_k, d_q of each row
+  constexpr int VSTEP = C::LPR / NV;  // lanes per reduced sum
+  static_assert(NV <= C::LPR && VSTEP * NV == C::LPR, "one reduced sum per lane group");
   const int lr = threadIdx.x % C::LPR;
+  const int gbase = (threadIdx.x & 31) - lr;  // first lane of the row group
   const int row0 = threadIdx.x / C::LPR;
   const float rq = ys[C::YN] * q_scale, rk = ys[C::YN + 1];
   float q8[8], k8[8];
+  float kqp = 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     q8[e] = ys[lr * 8 + e] * rq;
     k8[e] = ys[D + lr * 8 + e] * rk;
+    kqp = fmaf(k8[e], q8[e], kqp);
+  }
+  const float kq = row_sum<C::LPR>(kqp);
+  float red[NV];
+#pragma unroll
+  for (int i = 0; i < C::RPT; ++i) {
+    float dk = 0.f, dq = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s[i][e] *= a8[e];
+      dk = fmaf(s[i][e], k8[e], dk);
+      dq = fmaf(s[i][e], q8[e], dq);
+    }
+    red[2 * i] = dk;
+    red[2 * i + 1] = dq;
+  }
+#pragma unroll
+  for (int d = C::LPR / 2, nv = NV; d > 0; d >>= 1) {
+    if (nv > 1) {
+      const bool up = lr & d;
+      nv >>= 1;
+#pragma unroll
+      for (int v = 0; v < NV / 2; ++v) {
+        if (v < nv) {
+          const float keep = up ? red[v + nv] : red[v];
+          const float send = up ? red[v] : red[v + nv];
+          red[v] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+      }
+    } else {
+      red[0] += __shfl_xor_sync(0xffffffffu, red[0], d);
+    }
   }
 #pragma unroll
   for (int i = 0; i < C::RPT; ++i) {
     const int row = row0 + i * C::RSTEP;
-    float dot = 0.f;
+    const float dk = __shfl_sync(0xffffffffu, red[0], gbase + 2 * i * VSTEP);
+    const float u = beta * fmaf(-dmul, dk, ys[2 * D + row]);  // dmul 0: additive form
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      s[i][e] *= a8[e];
-      dot = fmaf(s[i][e], k8[e], dot);
-    }
-    dot = row_sum<C::LPR>(dot);
-    const float u = beta * fmaf(-dmul, dot, ys[2 * D + row]);  // dmul 0: additive form
-    float o = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      s[i][e] = fmaf(u, k8[e], s[i][e]);
-      o = fmaf(s[i][e], q8[e], o);
-    }
-    o = row_sum<C::LPR>(o);
-    if (lr == 0) store_elem(out, orow + row, out_dtype, o);
+    for (int e = 0; e < 8; ++e) s[i][e] = fmaf(u, k8[e], s[i][e]);
+    // the lane holding this row's d_q writes its output
+    if (lr == (2 * i + 1) * VSTEP) store_elem(out, orow + row, out_dtype, fmaf(u, kq, red[0]));
   }
 }
 
