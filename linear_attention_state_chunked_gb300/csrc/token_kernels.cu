@@ -35,7 +35,6 @@ struct TokCfg {
   static constexpr int RPT = V * LPR / NT;  // rows per thread
   static constexpr int RSTEP = NT / LPR;    // row stride between a thread's rows
   static constexpr int CH = 2 * D + V;      // conv channels of one head: q | k | v
-  static constexpr int YN = CH;             // the two norm factors follow them in ys
   static constexpr int CPT = (CH + NT - 1) / NT;
   static_assert(NT % 32 == 0, "whole warps");
   static_assert(RPT * RSTEP == V, "rows");
@@ -59,17 +58,21 @@ __device__ __forceinline__ float row_sum(float v) {
 // Per-token shared scratch: post-conv q | k | v and the two norm factors.
 template <int D, int V>
 struct TokSmem {
-  float y[2][2 * D + V + 2];
+  float y[2][2 * D + V];
+  float part[2][(TokCfg<D, V>::NT + 31) / 32][2];  // per warp: sum of q^2, sum of k^2
 };
 
 // Conv + activation for one token: each thread does its own channels and
 // keeps the window win[c][0..2] (oldest first) in registers; the token's
-// inputs are already in registers too.
+// inputs are already in registers too. Each warp also leaves its partial sums
+// of q^2 and k^2 in part[warp] for the L2 norms.
 template <int D, int V>
 __device__ __forceinline__ void conv_token_in(float (&win)[TokCfg<D, V>::CPT][3],
                                               const float (&w)[TokCfg<D, V>::CPT][4],
-                                              const float (&xin)[TokCfg<D, V>::CPT], bool do_silu, float* ys) {
+                                              const float (&xin)[TokCfg<D, V>::CPT], bool do_silu, float* ys,
+                                              float (*part)[2]) {
   using C = TokCfg<D, V>;
+  float pq = 0.f, pk = 0.f;
 #pragma unroll
   for (int i = 0; i < C::CPT; ++i) {
     const int cl = threadIdx.x + i * C::NT;
@@ -80,41 +83,20 @@ __device__ __forceinline__ void conv_token_in(float (&win)[TokCfg<D, V>::CPT][3]
       win[i][2] = xin[i];
       if (do_silu) y = silu(y);
       ys[cl] = y;
+      if (cl < D)
+        pq = fmaf(y, y, pq);
+      else if (cl < 2 * D)
+        pk = fmaf(y, y, pk);
     }
   }
-}
-
-// Sum of squares of q and k (first 2D entries of ys) -> 1/sqrt(ss + eps).
-template <int D, int V>
-__device__ __forceinline__ void qk_norms(float* ys, bool l2) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int YN = TokCfg<D, V>::YN;
-  if (!l2) {
-    if (threadIdx.x == 0) {
-      ys[YN] = 1.f;
-      ys[YN + 1] = 1.f;
-    }
-    return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    pq += __shfl_xor_sync(0xffffffffu, pq, o);
+    pk += __shfl_xor_sync(0xffffffffu, pk, o);
   }
-  constexpr int NW = TokCfg<D, V>::NT / 32;
-  if (NW >= 2) {
-    if (warp < 2) {
-      const float* v = ys + warp * D;
-      float ss = 0.f;
-      for (int i = lane; i < D; i += 32) ss += v[i] * v[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) ys[YN + warp] = rsqrtf(ss + kL2Eps);
-    }
-  } else {
-    for (int part = 0; part < 2; ++part) {
-      const float* v = ys + part * D;
-      float ss = 0.f;
-      for (int i = lane; i < D; i += 32) ss += v[i] * v[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) ys[YN + part] = rsqrtf(ss + kL2Eps);
-    }
+  if ((threadIdx.x & 31) == 0) {
+    part[threadIdx.x >> 5][0] = pq;
+    part[threadIdx.x >> 5][1] = pk;
   }
 }
 
@@ -126,8 +108,8 @@ __device__ __forceinline__ void qk_norms(float* ys, bool l2) {
 // sends the other half, so sum m ends whole in lane m / (LPR / (2 RPT)).
 template <int D, int V>
 __device__ __forceinline__ void rows_update(float (&s)[TokCfg<D, V>::RPT][8], const float* ys,
-                                            const float (&a8)[8], float beta, float dmul,
-                                            float q_scale, void* out, int64_t orow, int out_dtype) {
+                                            const float (&a8)[8], float beta, float dmul, float rq, float rk,
+                                            void* out, int64_t orow, int out_dtype) {
   using C = TokCfg<D, V>;
   constexpr int NV = 2 * C::RPT;      // sums per thread: d_k, d_q of each row
   constexpr int VSTEP = C::LPR / NV;  // lanes per reduced sum
@@ -135,7 +117,6 @@ __device__ __forceinline__ void rows_update(float (&s)[TokCfg<D, V>::RPT][8], co
   const int lr = threadIdx.x % C::LPR;
   const int gbase = (threadIdx.x & 31) - lr;  // first lane of the row group
   const int row0 = threadIdx.x / C::LPR;
-  const float rq = ys[C::YN] * q_scale, rk = ys[C::YN + 1];
   float q8[8], k8[8];
   float kqp = 0.f;
 #pragma unroll
@@ -1199,11 +1180,24 @@ __global__ void __launch_bounds__(TokCfg<D, V>::NT, 2) prefill_recurrent_kernel(
     for (int e = 0; e < 8; ++e) gc[e] = gn[e];
     const float beta = bn;
     if (t + 1 < eos) load_inputs(t + 1);
+    // one barrier per token: the scratch alternates between tokens, and a
+    // thread reaches token t+2's conv only after every thread passed token
+    // t+1's barrier, i.e. finished token t's row update
     float* ys = sm.y[(t - bos) & 1];
-    conv_token_in<D, V>(win, w, xc, a.flags & LIN_CONV_SILU, ys);
+    float(*part)[2] = sm.part[(t - bos) & 1];
+    conv_token_in<D, V>(win, w, xc, a.flags & LIN_CONV_SILU, ys, part);
     __syncthreads();
-    qk_norms<D, V>(ys, a.flags & LIN_QK_L2NORM);
-    __syncthreads();
+    float rq = a.q_scale, rk = 1.f;
+    if (a.flags & LIN_QK_L2NORM) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int wi = 0; wi < (C::NT + 31) / 32; ++wi) {
+        sq += part[wi][0];
+        sk += part[wi][1];
+      }
+      rq = rsqrtf(sq + kL2Eps) * a.q_scale;
+      rk = rsqrtf(sk + kL2Eps);
+    }
     float a8[8];
     if (per_key) {
 #pragma unroll
@@ -1213,7 +1207,7 @@ __global__ void __launch_bounds__(TokCfg<D, V>::NT, 2) prefill_recurrent_kernel(
 #pragma unroll
       for (int e = 0; e < 8; ++e) a8[e] = av;
     }
-    rows_update<D, V>(s, ys, a8, beta, dmul, a.q_scale, a.out, (t * H + h) * V, a.out_dtype);
+    rows_update<D, V>(s, ys, a8, beta, dmul, rq, rk, a.out, (t * H + h) * V, a.out_dtype);
     const int64_t n = P + (t - bos) + 1;
     if (nt > 0 && n % a.track_stride == 0) {
       const int dst = a.track_slots[t0 + (snap % nt)];
