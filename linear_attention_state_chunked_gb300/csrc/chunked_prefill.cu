@@ -857,7 +857,10 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float yy = ypre[i][e];
-            yy = silu_on ? silu(yy) : yy;
+            // a bf16 pool holds 8 significant bits: SiLU from one tanh.approx
+            // (relative error 2^-11) there, from exp and a reciprocal otherwise
+            // (and in the segmented instance, where the extra registers spill)
+            yy = silu_on ? ((BF && !SEG) ? silu_tanh(yy) : silu(yy)) : yy;
             ss += yy * yy;
             if (part == 0) yq[i][e] = yy;
             else if (part == 1) yk[i][e] = yy;
@@ -880,9 +883,17 @@ __global__ void __launch_bounds__(NT, 1)
       // KDA: exp(b_last - b) = exp(b_last - b_ref) exp(b_ref - b), the first
       // factor per channel for the chunk; both stay inside e^+-80 (the range
       // check below), so the product is the exponential up to one rounding
-      float ecl[4];
+      float ecl[4], ebr[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ecl[e] = KDA ? __expf(blast[e] - bref[e]) : 1.f;
+      for (int e = 0; e < 4; ++e) {
+        ecl[e] = KDA ? __expf(blast[e] - bref[e]) : 1.f;
+        ebr[e] = (KDA && !SEG) ? __expf(bref[e]) : 1.f;
+      }
+      // KDA: exp(b) = exp(b - b_ref) exp(b_ref), one exponential fewer per
+      // element, unless exp(b_ref) underflows for some lane of the warp (not in
+      // the segmented instance, where the extra registers spill)
+      const bool eh_prod = KDA && !SEG &&
+                           __all_sync(0xffffffffu, ebr[0] > 0.f && ebr[1] > 0.f && ebr[2] > 0.f && ebr[3] > 0.f);
 #pragma unroll
       for (int i = 0; i < TPW; ++i) {
         const int t = tfirst + i;
@@ -899,8 +910,11 @@ __global__ void __launch_bounds__(NT, 1)
         for (int e = 0; e < 4; ++e) {
           const int ee = KDA ? e : 0;
           const float b = cs[i][ee];
-          eH[e] = __expf(b);
           eL[e] = KDA ? __expf(b - bref[ee]) : 1.f;
+          if (eh_prod)
+            eH[e] = eL[e] * ebr[e];
+          else
+            eH[e] = __expf(b);
           eR[e] = KDA ? __expf(bref[ee] - b) : 1.f;
           eT[e] = KDA ? ecl[e] * eR[e] : __expf(blast[ee] - b);
           // the factored decay must stay inside fp32 range (else the pair is rerun)

@@ -148,4 +148,12 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
 
 __device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
 
+// SiLU as (y/2)(1 + tanh(y/2)): one transcendental, relative error about 2^-11
+__device__ __forceinline__ float silu_tanh(float y) {
+  const float h = 0.5f * y;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
+
 }  // namespace lin
