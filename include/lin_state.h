@@ -150,8 +150,11 @@ typedef struct {
  * so every valid g gives a valid result.
  * Precision: the chunked kernel carries the state in fp32; its tensor-core
  * operands are fp16 with high / low splits where the pool is fp32 (and for
- * per-head gates), so an fp32 pool gets fp32-class results; a bf16 pool with
- * per-key gates takes bf16 operands.
+ * per-head gates), so outputs and states of an fp32 pool stay within a few
+ * 1e-4 (relative L2 per request and head) of an exact computation; a bf16
+ * pool with per-key gates takes bf16 operands. The conv's SiLU is computed as
+ * (y/2)(1 + tanh(y/2)) with a hardware tanh (relative error about 2^-11). The
+ * token-by-token kernel computes in fp32 throughout.
  * Long single requests: with the chunked kernel, a batch of one request
  * whose heads alone cannot fill the GPU (heads x 4 <= SMs, >= 4096 tokens
  * by total_tokens; any request of >= 8 chunks with LIN_PREFILL_SEGMENTED)
