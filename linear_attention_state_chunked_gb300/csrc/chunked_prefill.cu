@@ -858,9 +858,8 @@ __global__ void __launch_bounds__(NT, 1)
           for (int e = 0; e < 4; ++e) {
             float yy = ypre[i][e];
             // SiLU from one tanh.approx (relative error 2^-11, below what the
-            // fp16 operand splits leave in the results); the segmented instance
-            // keeps exp and a reciprocal, where the extra registers spill
-            yy = silu_on ? (!SEG ? silu_tanh(yy) : silu(yy)) : yy;
+            // fp16 operand splits leave in the results)
+            yy = silu_on ? silu_tanh(yy) : yy;
             ss += yy * yy;
             if (part == 0) yq[i][e] = yy;
             else if (part == 1) yk[i][e] = yy;
