@@ -1016,10 +1016,6 @@ __global__ void __launch_bounds__(NT, 1)
       }
       umma::fence_before_sync();
     }
-    if (j + 1 < nch) {
-      const int n2 = (L - (j + 1) * CH) < CH ? (L - (j + 1) * CH) : CH;
-      load_gates<KDA>(a, row0 + CH, n2, h, H, warp, lane, gk, bt);
-    }
     if (!additive) {
       __syncthreads();  // V^T is in tensor memory
       if (tid == 0) {
@@ -1384,6 +1380,13 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
       umma::mma_commit(&bar_mma);
+    }
+    // the next chunk's gates and betas, in flight while the last products run
+    // and the epilogue stores (their registers are not live across this
+    // chunk's heavier phases)
+    if (j + 1 < nch) {
+      const int n2 = (L - (j + 1) * CH) < CH ? (L - (j + 1) * CH) : CH;
+      load_gates<KDA>(a, row0 + CH, n2, h, H, warp, lane, gk, bt);
     }
     if (!wait_mma()) break;
     // every MMA of this chunk is done: the next chunk's x tile may land now
