@@ -1487,14 +1487,29 @@ __global__ void __launch_bounds__(NT, 1)
                                            a.layer * pool.conv_layer_stride +
                                            snap_dst * pool.conv_slot_stride
                                      : nullptr;
-        for (int idx = tid; idx < 3 * 384; idx += NT) {
-          const int cl = idx / 3, m = idx % 3;
-          if (!valid_channel<VD>(cl)) continue;
-          const int ch = head_channel<VD>(cl, h, H);
-          const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
-          const int64_t off = int64_t(ch) * 3 + m;
-          if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
-          if (last_to_slot) store_elem(slot_c, off, pool.conv_dtype, wv);
+        if constexpr (!KDA) {
+          // one thread per channel, its three entries (the KDA instances keep
+          // one thread per entry: there the other form costs registers)
+          for (int cl = tid; cl < 384; cl += NT) {
+            if (!valid_channel<VD>(cl)) continue;
+            const int64_t off = int64_t(head_channel<VD>(cl, h, H)) * 3;
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+              const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
+              if (snap_c) store_elem(snap_c, off + m, pool.conv_dtype, wv);
+              if (last_to_slot) store_elem(slot_c, off + m, pool.conv_dtype, wv);
+            }
+          }
+        } else {
+          for (int idx = tid; idx < 3 * 384; idx += NT) {
+            const int cl = idx / 3, m = idx % 3;
+            if (!valid_channel<VD>(cl)) continue;
+            const int ch = head_channel<VD>(cl, h, H);
+            const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
+            const int64_t off = int64_t(ch) * 3 + m;
+            if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
+            if (last_to_slot) store_elem(slot_c, off, pool.conv_dtype, wv);
+          }
         }
       }
       umma::fence_smem_to_async();
