@@ -74,6 +74,10 @@ constexpr int NW = NT / 32;
 constexpr int TPW = CH / NW; // tokens per warp in the conv phase
 constexpr int XR = CH + 3;   // rows of a staged x tile (3 halo rows)
 constexpr uint32_t kWaitTries = 1u << 26;
+// The thread that issues the TMA stores of outputs and states and owns their
+// bulk groups: lane 0 of warp 1, so thread 0's wait for the next x tile runs
+// beside the store issue instead of after it.
+constexpr int kStoreTid = 32;
 
 // Shared-memory map (offsets from a 1024-byte aligned base). Regions are
 // reused once their previous contents have been consumed by an MMA.
@@ -876,7 +880,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       // the previous chunk's TMA stores must have read their staging tiles
       // before the operand rows go over them; those reads ran behind the conv
-      if (tid == 0) bulk_wait_read();
+      if (tid == kStoreTid) bulk_wait_read();
       __syncthreads();
       bool range_bad = false;
       // KDA: exp(b_last - b) = exp(b_last - b_ref) exp(b_ref - b), the first
@@ -1515,7 +1519,7 @@ __global__ void __launch_bounds__(NT, 1)
       umma::fence_smem_to_async();
       umma::fence_before_sync();
       __syncthreads();
-      if (tid == 0) {
+      if (tid == kStoreTid) {
         // bulk stores carry no order among themselves: an earlier snapshot
         // into the same track slot must have landed before this one starts.
         // Each chunk commits one group and a slot recurs every ntr snapshots,
@@ -1541,12 +1545,10 @@ __global__ void __launch_bounds__(NT, 1)
 
   // ---- teardown: every TMA store issued here has completed, and no x tile is
   // still landing, before exit
-  if (tid == 0) {
-    bulk_wait_all();
-    // after an early exit the last x tile issued may not have been waited for
-    // (each chunk j waited for x tile j, phase j & 1)
-    if (abort_sh) umma::mbar_wait(&bar_x, static_cast<uint32_t>((x_issued - 1) & 1), kWaitTries);
-  }
+  if (tid == kStoreTid) bulk_wait_all();
+  // after an early exit the last x tile issued may not have been waited for
+  // (each chunk j waited for x tile j, phase j & 1)
+  if (tid == 0 && abort_sh) umma::mbar_wait(&bar_x, static_cast<uint32_t>((x_issued - 1) & 1), kWaitTries);
   __syncthreads();
   umma::fence_after_sync();
   if (warp == 0) umma::tmem_dealloc(tm, TMEM_COLS);
