@@ -1392,6 +1392,61 @@ __global__ void __launch_bounds__(NT, 1)
       const int n2 = (L - (j + 1) * CH) < CH ? (L - (j + 1) * CH) : CH;
       load_gates<KDA>(a, row0 + CH, n2, h, H, warp, lane, gk, bt);
     }
+    // the snapshot this chunk ends at (if any), whether the final state goes
+    // to the slot, and the stores of the conv window after the chunk (its last
+    // 3 inputs, known since the conv phase). The GDN and SSD instances do both
+    // while the last products run; the KDA instances, short of registers
+    // there, do them in the epilogue.
+    const bool full = (n == CH);
+    const bool last = (j == nch - 1);
+    int snap_dst = -1;
+    bool last_to_slot = false, store_state = false;
+    auto decide_snapshot = [&]() {
+      const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
+      if (ntr > 0 && full && (end_pos % a.track_stride) == 0) {
+        if (seg_mode == kSegOff || snap >= snap_total - ntr) snap_dst = a.track_slots[t0 + (snap % ntr)];
+        ++snap;
+      }
+      // the final state goes to the slot when this CTA ends the request (and
+      // runs with outputs); segment state runs write it to the workspace
+      last_to_slot = last && outputs_on && seg_last;
+      store_state = snap_dst >= 0 || last_to_slot;
+    };
+    auto store_window = [&]() {
+      if (!store_state) return;
+      char* snap_c = snap_dst >= 0 ? static_cast<char*>(pool.conv) +
+                                         a.layer * pool.conv_layer_stride +
+                                         snap_dst * pool.conv_slot_stride
+                                   : nullptr;
+      if constexpr (!KDA) {
+        // one thread per channel, its three entries (the KDA instances keep
+        // one thread per entry: there the other form costs registers)
+        for (int cl = tid; cl < 384; cl += NT) {
+          if (!valid_channel<VD>(cl)) continue;
+          const int64_t off = int64_t(head_channel<VD>(cl, h, H)) * 3;
+#pragma unroll
+          for (int m = 0; m < 3; ++m) {
+            const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
+            if (snap_c) store_elem(snap_c, off + m, pool.conv_dtype, wv);
+            if (last_to_slot) store_elem(slot_c, off + m, pool.conv_dtype, wv);
+          }
+        }
+      } else {
+        for (int idx = tid; idx < 3 * 384; idx += NT) {
+          const int cl = idx / 3, m = idx % 3;
+          if (!valid_channel<VD>(cl)) continue;
+          const int ch = head_channel<VD>(cl, h, H);
+          const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
+          const int64_t off = int64_t(ch) * 3 + m;
+          if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
+          if (last_to_slot) store_elem(slot_c, off, pool.conv_dtype, wv);
+        }
+      }
+    };
+    if constexpr (!KDA) {
+      decide_snapshot();
+      store_window();
+    }
     if (!wait_mma()) break;
     // every MMA of this chunk is done: the next chunk's x tile may land now
     if (tid == 0 && j + 1 < nch) issue_x_tile(row0 + CH);
@@ -1401,7 +1456,7 @@ __global__ void __launch_bounds__(NT, 1)
     // tiles and TMA stores, so the copy engine drains them while the next
     // chunk's conv phase runs.
     {
-      const bool full = (n == CH);
+      if constexpr (KDA) decide_snapshot();
       const int oes = a.out_dtype == LIN_BF16 ? 2 : 4;
       if (outputs_on) {
         float o16[16];
@@ -1438,17 +1493,6 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
-      const int64_t end_pos = int64_t(P) + int64_t(j) * CH + n;
-      int snap_dst = -1;
-      if (ntr > 0 && full && (end_pos % a.track_stride) == 0) {
-        if (seg_mode == kSegOff || snap >= snap_total - ntr) snap_dst = a.track_slots[t0 + (snap % ntr)];
-        ++snap;
-      }
-      const bool last = (j == nch - 1);
-      // the final state goes to the slot when this CTA ends the request (and
-      // runs with outputs); segment state runs write it to the workspace
-      const bool last_to_slot = last && outputs_on && seg_last;
-      const bool store_state = snap_dst >= 0 || last_to_slot;
       {
         float v[32];
         const int cc = slice * 32;
@@ -1485,37 +1529,7 @@ __global__ void __launch_bounds__(NT, 1)
           }
         }
       }
-      if (store_state) {
-        // conv window after the chunk: its last 3 inputs (chunk rows n-3 .. n-1)
-        char* snap_c = snap_dst >= 0 ? static_cast<char*>(pool.conv) +
-                                           a.layer * pool.conv_layer_stride +
-                                           snap_dst * pool.conv_slot_stride
-                                     : nullptr;
-        if constexpr (!KDA) {
-          // one thread per channel, its three entries (the KDA instances keep
-          // one thread per entry: there the other form costs registers)
-          for (int cl = tid; cl < 384; cl += NT) {
-            if (!valid_channel<VD>(cl)) continue;
-            const int64_t off = int64_t(head_channel<VD>(cl, h, H)) * 3;
-#pragma unroll
-            for (int m = 0; m < 3; ++m) {
-              const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
-              if (snap_c) store_elem(snap_c, off + m, pool.conv_dtype, wv);
-              if (last_to_slot) store_elem(slot_c, off + m, pool.conv_dtype, wv);
-            }
-          }
-        } else {
-          for (int idx = tid; idx < 3 * 384; idx += NT) {
-            const int cl = idx / 3, m = idx % 3;
-            if (!valid_channel<VD>(cl)) continue;
-            const int ch = head_channel<VD>(cl, h, H);
-            const float wv = WIN[(j & 1) * 1152 + m * 384 + cl];
-            const int64_t off = int64_t(ch) * 3 + m;
-            if (snap_c) store_elem(snap_c, off, pool.conv_dtype, wv);
-            if (last_to_slot) store_elem(slot_c, off, pool.conv_dtype, wv);
-          }
-        }
-      }
+      if constexpr (KDA) store_window();
       umma::fence_smem_to_async();
       umma::fence_before_sync();
       __syncthreads();
