@@ -86,12 +86,15 @@ enum {
   LIN_PREFILL_RECURRENT = 8u, /* prefill: force the token-by-token kernel      */
   LIN_PREFILL_SEGMENTED = 16u, /* prefill: run a batch of one request in segments
                                  even when it is short (see lin_state_prefill) */
-  LIN_UPDATE_ADDITIVE = 32u   /* prefill, decode, verify, replay: the additive
+  LIN_UPDATE_ADDITIVE = 32u,  /* prefill, decode, verify, replay: the additive
                                  (Mamba2 SSD) update S' = S Diag(alpha) + beta v k^T
                                  with no delta correction ([MRC] 9.3: S_new =
                                  A S_old + B x; alpha = exp(dt A), beta = dt,
                                  k = B, v = x, q = C); the pool, tracking,
                                  verify and commit work unchanged */
+  LIN_PREFILL_ONE_PIECE = 64u  /* prefill, chunked kernel: every (request, head)
+                                 in one piece on one SM, no wrap-around
+                                 schedule (see lin_state_prefill); same results */
 };
 
 /* ---- the state pool ([MRC] 1.3; [K3] shapes) ----------------------------

@@ -25,6 +25,7 @@ LIN_F32, LIN_BF16 = 0, 1
 LIN_GATE_PER_HEAD, LIN_GATE_PER_KEY = 0, 1
 LIN_QK_L2NORM, LIN_CONV_SILU, LIN_VALIDATE, LIN_PREFILL_RECURRENT = 1, 2, 4, 8
 LIN_PREFILL_SEGMENTED = 16
+LIN_PREFILL_ONE_PIECE = 64
 LIN_UPDATE_ADDITIVE = 32
 LIN_ST_BAD_SLOT, LIN_ST_BAD_PREFIX, LIN_ST_TRACK_ALIAS, LIN_ST_BAD_SEQLEN = 1, 2, 4, 8
 LIN_ST_COPY_ALIAS, LIN_ST_TIMEOUT, LIN_ST_BAD_ACCEPT = 16, 32, 64

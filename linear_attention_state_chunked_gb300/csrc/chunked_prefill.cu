@@ -147,6 +147,31 @@ constexpr uint32_t TMEM_COLS = 512;
 // snapshots; the offset and transition runs share one launch.
 enum SegMode { kSegOff = 0, kSegOffset = 1, kSegTransition = 2, kSegFinal = 3, kSegOffsetAndTransition = 4 };
 
+// Wrap-around schedule of a varlen batch (McNaughton's wrap-around rule for
+// preemptive scheduling on identical machines). The batch's (request, head)
+// chains of n_r chunks are laid end to end and cut into `grid` ranges of T
+// chunk units, T >= the longest chain, one range per SM. A chain crossing the
+// boundary between ranges m and m + 1 becomes two pieces: its first chunks
+// run at the start of range m + 1 and hand the state on; its last chunks run
+// at the end of range m, from that state. The head ends by unit time
+// x <= T - (n - x), when the tail starts. Each piece has its planned start
+// time in its range; CTAs take pieces in that order from a counter (list
+// scheduling), so every wait is for a piece taken earlier, whose first piece
+// waits for nothing: no deadlock, whatever runs concurrently.
+struct WrapPiece {
+  int32_t r, h, c0, c1;  // request, head, chunks [c0, c1)
+  int32_t mode;          // 0: whole chain, 1: tail (waits for link), 2: head (sets link)
+  int32_t link;          // index of the hand-on state and flag
+  int32_t pad0, pad1;
+};
+struct WrapBuf {
+  int32_t* ctl = nullptr;          // [0] pieces, [1] next piece to take
+  const WrapPiece* piece = nullptr;  // [pieces], in any order
+  const int32_t* order = nullptr;  // [pieces] piece indices by planned start time
+  uint32_t* flag = nullptr;        // [grid] set once the state of link i is handed on
+  float* state = nullptr;          // [grid][128][K] fp32: that state
+};
+
 struct ChunkParams {
   lin_state_pool_t pool;
   lin_prefill_args_t a;
@@ -160,6 +185,8 @@ struct ChunkParams {
   const float* seg_state_in;   // mode 3: fp32 state before segment k >= 1 at index k - 1
   uint32_t* redo;              // KDA: bit r * H + h set when (request r, head h) left the
                                // factored decay range (cleared before the launch)
+  // wrap-around schedule of a batch (wrap == nullptr: one CTA per (request, head))
+  WrapBuf wrap;
 };
 
 // Longest-first order of a varlen batch: the sequential chunk chain of the
@@ -199,6 +226,115 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__
     }
   }
   for (int i = threadIdx.x; i < batch; i += blockDim.x) order[i] = static_cast<int32_t>(key[i] & 0xffffffffu);
+}
+
+// The wrap-around plan of a batch (one CTA): the chunk units n_r of every
+// request (0 for an empty request and for one the prefill kernel skips or
+// rejects: a negative slot, a slot past the pool, bad cu_seqlens or
+// prefix_len, the kernel's own checks), T = max(longest chain,
+// ceil(H sum n_r / grid)), the pieces with their planned start times, sorted
+// by start time (bitonic), and cleared hand-on flags and piece counter.
+constexpr int kWrapMaxPieces = 8192;
+constexpr size_t kWrapPlanSmem = kWrapMaxPieces * sizeof(uint64_t) + kOrderMax * (sizeof(int64_t) + sizeof(int32_t));
+
+__global__ void __launch_bounds__(1024) wrap_plan_kernel(const lin_prefill_args_t a, int H, int num_slots, int grid,
+                                                         int32_t* ctl, WrapPiece* piece, int32_t* order,
+                                                         uint32_t* flag) {
+  extern __shared__ uint64_t wkey[];                                       // [kWrapMaxPieces]
+  int64_t* first = reinterpret_cast<int64_t*>(wkey + kWrapMaxPieces);     // [batch] first unit of r
+  int32_t* units = reinterpret_cast<int32_t*>(first + kOrderMax);         // [batch] n_r
+  __shared__ int64_t part[1024], pmax[1024];
+  __shared__ int count;
+  const int t = threadIdx.x, B = a.batch;
+  const int per = (B + 1023) / 1024;  // requests t * per .. of this thread
+  int64_t sum = 0, mx = 0;
+  for (int i = 0; i < per; ++i) {
+    const int r = t * per + i;
+    if (r >= B) break;
+    const int32_t sl = a.slot[r];
+    const int64_t b = a.cu_seqlens[r], e = a.cu_seqlens[r + 1];
+    const int32_t pf = a.prefix_len[r];
+    const bool ok = sl >= 0 && sl < num_slots && b >= 0 && e >= b && e <= a.total_tokens && pf >= 0 && !(pf & 63);
+    const int32_t n = ok ? static_cast<int32_t>((e - b + CH - 1) / CH) : 0;
+    units[r] = n;
+    sum += n;
+    mx = n > mx ? n : mx;
+  }
+  part[t] = sum;
+  pmax[t] = mx;
+  if (t == 0) count = 0;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {  // inclusive prefix sums and maxima
+    const int64_t v = t >= d ? part[t - d] : 0, w = t >= d ? pmax[t - d] : 0;
+    __syncthreads();
+    part[t] += v;
+    if (w > pmax[t]) pmax[t] = w;
+    __syncthreads();
+  }
+  {
+    int64_t run = t > 0 ? part[t - 1] : 0;
+    for (int i = 0; i < per; ++i) {
+      const int r = t * per + i;
+      if (r >= B) break;
+      first[r] = run * H;
+      run += units[r];
+    }
+  }
+  const int64_t total = part[1023] * H;
+  int64_t T = (total + grid - 1) / grid;
+  if (T < pmax[1023]) T = pmax[1023];
+  if (T < 1) T = 1;
+  __syncthreads();
+  auto emit = [&](int r, int h, int c0, int c1, int mode, int link, int64_t start) {
+    const int k = atomicAdd(&count, 1);
+    piece[k] = WrapPiece{r, h, c0, c1, mode, link, 0, 0};
+    const uint64_t st = start < 0x7fffffff ? static_cast<uint64_t>(start) : 0x7fffffffull;
+    wkey[k] = (st << 32) | static_cast<uint32_t>(k);
+  };
+  for (int c = t; c < B * H; c += 1024) {
+    const int r = c / H, h = c % H;
+    const int64_t n = units[r];
+    if (n == 0) {  // nothing to run: checks, and a cold empty request's zero state
+      emit(r, h, 0, 0, 0, 0, 0);
+      continue;
+    }
+    const int64_t cs = first[r] + h * n, ce = cs + n;
+    const int64_t ms = cs / T, me = (ce - 1) / T;
+    if (ms == me) {
+      emit(r, h, 0, static_cast<int>(n), 0, 0, cs - ms * T);
+    } else {  // crosses the start of range me: head there first, tail at the end of range ms
+      const int x = static_cast<int>(ce - me * T);
+      emit(r, h, 0, x, 2, static_cast<int>(me), 0);
+      emit(r, h, x, static_cast<int>(n), 1, static_cast<int>(me), cs - ms * T);
+    }
+  }
+  __syncthreads();
+  const int N = count;
+  int n2 = 2;
+  while (n2 < N) n2 <<= 1;
+  for (int i = N + t; i < n2; i += 1024) wkey[i] = ~0ull;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = t; i < n2; i += 1024) {
+        const int ix = i ^ jj;
+        if (ix > i) {
+          const uint64_t x = wkey[i], y = wkey[ix];
+          if ((x > y) == ((i & k) == 0)) {
+            wkey[i] = y;
+            wkey[ix] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = t; i < N; i += 1024) order[i] = static_cast<int32_t>(wkey[i] & 0xffffffffu);
+  for (int i = t; i < grid; i += 1024) flag[i] = 0u;
+  if (t == 0) {
+    ctl[0] = N;
+    ctl[1] = 0;
+  }
 }
 
 // Global channel of the head's channel cl in [0, 384): q, k and v parts of
@@ -303,6 +439,32 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_but_one() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+// orders this thread's completed bulk (async-proxy) writes before its later
+// generic-proxy operations
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Hand-on flags of the wrap-around schedule: set with release semantics after
+// the state they guard is written; waited for (one thread) with acquire
+// semantics, giving up after about 4 s of device time.
+__device__ __forceinline__ void flag_set(uint32_t* f) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+}
+__device__ __forceinline__ bool flag_wait(const uint32_t* f) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v) return true;
+    if (global_ns() - t0 > 4000000000ull) return false;
+    __nanosleep(256);
+  }
+  return false;
+}
 
 // hi / lo fp16 split of four values: hi = fp16(x), lo = fp16(x - hi).
 __device__ __forceinline__ void split4(float a, float b, float c, float d, uint32_t (&hi)[2],
@@ -416,6 +578,7 @@ __global__ void __launch_bounds__(NT, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int range_sh;  // KDA: a key channel's decay left the factored range
+  __shared__ int piece_sh[6];  // wrap-around schedule: the piece this CTA took
 
   const lin_state_pool_t& pool = p.pool;
   const lin_prefill_args_t& a = p.a;
@@ -434,8 +597,34 @@ __global__ void __launch_bounds__(NT, 1)
   } else if (seg_mode) {
     seg = p.seg_first + static_cast<int>(blockIdx.x) / H;
   }
-  const int r = seg_mode ? 0 : (p.order ? p.order[blockIdx.x / H] : blockIdx.x / H);
-  const int h = blockIdx.x % H;
+  int r, h, c0 = 0, c1 = -1, pmode = 0, plink = 0;
+  if (p.wrap.ctl) {
+    // the next piece of the wrap-around schedule, in planned start order
+    if (threadIdx.x == 0) {
+      const int k = atomicAdd(p.wrap.ctl + 1, 1);
+      piece_sh[0] = -1;
+      if (k < __ldcg(p.wrap.ctl)) {
+        const WrapPiece e = p.wrap.piece[__ldcg(p.wrap.order + k)];
+        piece_sh[0] = e.r;
+        piece_sh[1] = e.h;
+        piece_sh[2] = e.c0;
+        piece_sh[3] = e.c1;
+        piece_sh[4] = e.mode;
+        piece_sh[5] = e.link;
+      }
+    }
+    __syncthreads();
+    r = piece_sh[0];
+    if (r < 0) return;
+    h = piece_sh[1];
+    c0 = piece_sh[2];
+    c1 = piece_sh[3];
+    pmode = piece_sh[4];
+    plink = piece_sh[5];
+  } else {
+    r = seg_mode ? 0 : (p.order ? p.order[blockIdx.x / H] : blockIdx.x / H);
+    h = blockIdx.x % H;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, slice = warp >> 2;  // four warps share each lane quarter
   const int vrow = quarter * 32 + lane;             // TMEM lane owned in the epilogues
@@ -458,19 +647,25 @@ __global__ void __launch_bounds__(NT, 1)
     if (rep && seg == 0) report(a.status, LIN_ST_BAD_PREFIX);
     return;
   }
-  // the tokens this CTA runs: the request, or one segment of it
+  // the tokens this CTA runs: the request, one segment of it, or one piece
+  // (chunks c0 .. c1 - 1) of it under the wrap-around schedule
   int64_t bos = bos_r, eos_c = eos;
   if (seg_mode) {
     bos = bos_r + int64_t(seg) * p.seg_len;
     if (bos >= eos) return;
     eos_c = (eos - bos) < p.seg_len ? eos : bos + p.seg_len;
+  } else if (c1 >= 0) {
+    bos = bos_r + int64_t(c0) * CH;
+    const int64_t e1 = bos_r + int64_t(c1) * CH;
+    eos_c = e1 < eos ? e1 : eos;
   }
   const int P = P_r + static_cast<int>(bos - bos_r);  // tokens before bos in absolute positions
   const bool seg_last = (eos_c == eos);               // this CTA ends the request
   const bool outputs_on =
       !SEG || seg_mode == kSegOff || seg_mode == kSegFinal || (seg_mode == kSegOffset && seg == 0);
-  const bool state_to_ws = seg_mode == kSegOffset || seg_mode == kSegTransition;
-  float* state_ws = seg_mode == kSegTransition ? p.seg_trans_out : p.seg_state_out;
+  // the fp32 state after the last chunk also goes to a workspace: a segment's
+  // offset or transition run, a wrap-around head piece
+  const bool state_to_ws = seg_mode == kSegOffset || seg_mode == kSegTransition || pmode == 2;
   int t0 = 0, ntr = 0;
   if (outputs_on && a.track_stride > 0 && a.cu_track) {
     t0 = a.cu_track[r];
@@ -487,7 +682,8 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   }
-  // initial state: 0 zeros, 1 the slot, 2 identity, 3 the segment workspace
+  // initial state: 0 zeros, 1 the slot, 2 identity, 3 an fp32 workspace state
+  // (the segment's, or the one a wrap-around head piece handed on)
   if (KDA && seg_mode == kSegFinal && p.redo) {
     // an offset or transition run of this (request, head) left the factored
     // decay range: the token-by-token rerun redoes it from the slot
@@ -497,6 +693,7 @@ __global__ void __launch_bounds__(NT, 1)
   const bool warm_r = a.has_initial_state[r] != 0;
   int init_kind = warm_r ? 1 : 0;
   if (seg > 0) init_kind = seg_mode == kSegOffset ? 0 : (seg_mode == kSegTransition ? 2 : 3);
+  if (pmode == 1) init_kind = 3;
   const bool warm = init_kind == 1;
   const bool zero_v = SEG && seg_mode == kSegTransition;  // transition runs take no value input
   const int L = static_cast<int>(eos_c - bos);
@@ -533,7 +730,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int rr = i / 384, cl = i % 384;
     if (!valid_channel<VD>(cl))
       HALO[i] = 0.f;
-    else if (seg > 0)  // the 3 inputs before the segment
+    else if (bos > bos_r)  // the 3 inputs before the segment or piece
       HALO[i] = load_elem(a.x, (bos - 3 + rr) * int64_t(pool.conv_channels) + head_channel<VD>(cl, h, H), LIN_BF16);
     else
       HALO[i] = warm ? load_elem(slot_c, int64_t(head_channel<VD>(cl, h, H)) * 3 + rr, pool.conv_dtype) : 0.f;
@@ -578,6 +775,23 @@ __global__ void __launch_bounds__(NT, 1)
     return (krows == 64 ? dm64 : dm128) + ((off + static_cast<uint32_t>(k0) * 128) >> 4);
   };
 
+  // a wrap-around tail piece starts from the state its head piece hands on;
+  // it runs nothing when that wait gives up or when the head piece left the
+  // KDA factored range (the token-by-token rerun redoes the pair)
+  int nrun = nch;
+  if (pmode == 1) {
+    if (tid == 0 && !flag_wait(p.wrap.flag + plink)) {
+      abort_sh = 1;
+      report(a.status, LIN_ST_TIMEOUT);
+    }
+    __syncthreads();
+    if (abort_sh) nrun = 0;
+    if (KDA && p.redo) {
+      const int idx = r * H + h;
+      if ((__ldcg(p.redo + (idx >> 5)) >> (idx & 31)) & 1u) nrun = 0;
+    }
+  }
+
   // ---- initial state: fp32 into TMEM, 16-bit operand copy into shared memory
   {
     float s[32];
@@ -607,10 +821,12 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     } else if (init_kind == 3) {
-      const float* src = p.seg_state_in + ((int64_t(seg - 1) * H + h) * DH + vrow) * DH + cc;
+      const float* src = (pmode == 1 ? p.wrap.state + int64_t(plink) * DH * DH
+                                     : p.seg_state_in + (int64_t(seg - 1) * H + h) * DH * DH) +
+                         int64_t(vrow) * DH + cc;
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        float4 u = *reinterpret_cast<const float4*>(src + 4 * m);
+        float4 u = __ldcg(reinterpret_cast<const float4*>(src + 4 * m));
         s[4 * m] = u.x; s[4 * m + 1] = u.y; s[4 * m + 2] = u.z; s[4 * m + 3] = u.w;
       }
     } else {
@@ -629,8 +845,8 @@ __global__ void __launch_bounds__(NT, 1)
   load_gates<KDA>(a, bos, L < CH ? L : CH, h, H, warp, lane, gk, bt);
 
   uint32_t ph_mma = 0;
-  // boundaries snapshotted before bos by earlier segments of this request
-  int snap = (ntr > 0 && seg > 0) ? static_cast<int>(P / a.track_stride - P_r / a.track_stride) : 0;
+  // boundaries snapshotted before bos by earlier segments or pieces of this request
+  int snap = (ntr > 0 && bos > bos_r) ? static_cast<int>(P / a.track_stride - P_r / a.track_stride) : 0;
   // Segments run in parallel, so two of them may map boundaries onto the same
   // entry of a cycled track list: there only the snapshots that survive in
   // token order (the request's last ntr) are written.
@@ -668,10 +884,10 @@ __global__ void __launch_bounds__(NT, 1)
                   part < 2 ? part * H * DH + h * DH : 2 * H * DH + h * VD, static_cast<int>(r0), b);
     ++x_issued;
   };
-  if (tid == 0) issue_x_tile(bos);
+  if (tid == 0 && nrun > 0) issue_x_tile(bos);
 
   const int tfirst = warp * TPW;
-  for (int j = 0; j < nch; ++j) {
+  for (int j = 0; j < nrun; ++j) {
     const int n = (L - j * CH) < CH ? (L - j * CH) : CH;
     const int64_t row0 = bos + int64_t(j) * CH;
 
@@ -1499,7 +1715,10 @@ __global__ void __launch_bounds__(NT, 1)
         umma::tmem_ld32(tmem_addr(tm, quarter * 32, COL_S + cc), v);
         if (!last) put32<BF>(sb + OFF_SOP, 128, vrow, cc, v, 1.f);
         if (last && state_to_ws) {
-          float* dst = state_ws + ((int64_t(seg) * H + h) * DH + vrow) * DH + cc;
+          float* dst = (pmode == 2 ? p.wrap.state + int64_t(plink) * DH * DH
+                                   : (seg_mode == kSegTransition ? p.seg_trans_out : p.seg_state_out) +
+                                         (int64_t(seg) * H + h) * DH * DH) +
+                       int64_t(vrow) * DH + cc;
 #pragma unroll
           for (int m = 0; m < 8; ++m)
             *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
@@ -1559,12 +1778,22 @@ __global__ void __launch_bounds__(NT, 1)
 
   // ---- teardown: every TMA store issued here has completed, and no x tile is
   // still landing, before exit
-  if (tid == kStoreTid) bulk_wait_all();
+  if (tid == kStoreTid) {
+    bulk_wait_all();
+    if (pmode == 2) fence_async_global();
+  }
   // after an early exit the last x tile issued may not have been waited for
   // (each chunk j waited for x tile j, phase j & 1)
-  if (tid == 0 && abort_sh) umma::mbar_wait(&bar_x, static_cast<uint32_t>((x_issued - 1) & 1), kWaitTries);
+  if (tid == 0 && abort_sh && x_issued > 0)
+    umma::mbar_wait(&bar_x, static_cast<uint32_t>((x_issued - 1) & 1), kWaitTries);
   __syncthreads();
   umma::fence_after_sync();
+  // a wrap-around head piece: the state it handed on and its snapshot stores
+  // (the tail's next snapshot may go to the same track slot) have landed
+  if (pmode == 2 && tid == 0 && !abort_sh) {
+    __threadfence();
+    flag_set(p.wrap.flag + plink);
+  }
   if (warp == 0) umma::tmem_dealloc(tm, TMEM_COLS);
 }
 
@@ -1731,9 +1960,66 @@ size_t segment_workspace(const lin_state_pool_t& pool, const SegPlan& sp) {
   return 2 * size_t(sp.nseg) * pool.num_heads * DH * DH * sizeof(float);
 }
 
+// Wrap-around schedule: for a batch with more (request, head) chains than
+// SMs (one chain per SM is already as good as it gets), in one piece per
+// chain unless LIN_PREFILL_ONE_PIECE; ranges = SMs.
+struct WrapPlan {
+  int grid = 0, max_pieces = 0;
+};
+
+WrapPlan wrap_plan(const lin_state_pool_t& pool, const lin_prefill_args_t& a, const SegPlan& sp) {
+  WrapPlan wp;
+  if (sp.nseg >= 2 || (a.flags & (LIN_PREFILL_RECURRENT | LIN_PREFILL_ONE_PIECE))) return wp;
+  if (a.batch < 1 || a.batch > kOrderMax) return wp;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return wp;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return wp;
+  const int64_t chains = int64_t(a.batch) * pool.num_heads;
+  if (chains <= sms || chains + sms > kWrapMaxPieces) return wp;
+  wp.grid = sms;
+  wp.max_pieces = static_cast<int>(chains + sms);
+  return wp;
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t wrap_workspace(const WrapPlan& wp) {
+  if (wp.grid == 0) return 0;
+  return align256(2 * sizeof(int32_t)) + align256(size_t(wp.max_pieces) * sizeof(WrapPiece)) +
+         align256(size_t(wp.max_pieces) * sizeof(int32_t)) + align256(size_t(wp.grid) * sizeof(uint32_t)) +
+         size_t(wp.grid) * DH * DH * sizeof(float);
+}
+
+// The wrap-around buffers carved from a workspace of wrap_workspace(wp) bytes.
+struct WrapBufs {
+  int grid = 0;
+  int32_t* ctl = nullptr;
+  WrapPiece* piece = nullptr;
+  int32_t* order = nullptr;
+  uint32_t* flag = nullptr;
+  float* state = nullptr;
+};
+
+WrapBufs carve_wrap(const WrapPlan& wp, char* ws) {
+  WrapBufs b;
+  if (wp.grid == 0 || !ws) return b;
+  b.grid = wp.grid;
+  b.ctl = reinterpret_cast<int32_t*>(ws);
+  ws += align256(2 * sizeof(int32_t));
+  b.piece = reinterpret_cast<WrapPiece*>(ws);
+  ws += align256(size_t(wp.max_pieces) * sizeof(WrapPiece));
+  b.order = reinterpret_cast<int32_t*>(ws);
+  ws += align256(size_t(wp.max_pieces) * sizeof(int32_t));
+  b.flag = reinterpret_cast<uint32_t*>(ws);
+  ws += align256(size_t(wp.grid) * sizeof(uint32_t));
+  b.state = reinterpret_cast<float*>(ws);
+  return b;
+}
+
 template <bool KDA, int ST, int VD>
 cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
-                     const SegPlan& sp, float* seg_buf, uint32_t* redo, cudaStream_t s) {
+                     const SegPlan& sp, float* seg_buf, uint32_t* redo, const WrapBufs& wb, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmap;
@@ -1791,12 +2077,26 @@ cudaError_t launch_t(const lin_state_pool_t& pool, const lin_prefill_args_t& a, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
+  const unsigned H = static_cast<unsigned>(pool.num_heads);
+  if (wb.grid > 0 && !segmented) {
+    // the wrap-around plan, then one CTA per piece (at most chains + ranges)
+    if ((e = cudaFuncSetAttribute(wrap_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kWrapPlanSmem))) != cudaSuccess)
+      return e;
+    wrap_plan_kernel<<<1, 1024, kWrapPlanSmem, s>>>(a, int(H), pool.num_slots, wb.grid, wb.ctl, wb.piece, wb.order,
+                                                    wb.flag);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ChunkParams pw{pool, a, nullptr, kSegOff, 0, 0, 0, nullptr, nullptr, nullptr, redo,
+                   WrapBuf{wb.ctl, wb.piece, wb.order, wb.flag, wb.state}};
+    const unsigned grid = static_cast<unsigned>(a.batch) * H + static_cast<unsigned>(wb.grid);
+    kern<<<grid, NT, SMEM_BYTES, s>>>(tmap, tmap_xt, tmap_state, tmap_out, pw);
+    return cudaGetLastError();
+  }
   if (order) {
     order_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.batch, order);
     cudaError_t e2 = cudaGetLastError();
     if (e2 != cudaSuccess) return e2;
   }
-  const unsigned H = static_cast<unsigned>(pool.num_heads);
   if (segmented) {
     // one long request in segments: offset runs (segments 0 .. n-2) and
     // transition runs (1 .. n-2), the scan, then the final runs (all)
@@ -1855,7 +2155,8 @@ size_t redo_workspace(const lin_state_pool_t& pool, const lin_prefill_args_t& a)
 // token-by-token launch behind the chunked one runs only the flagged pairs
 // (the others return at once), so no host synchronisation is needed.
 cudaError_t launch_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a, int32_t* order,
-                           const SegPlan& sp, float* seg_buf, uint32_t* redo, cudaStream_t stream) {
+                           const SegPlan& sp, float* seg_buf, uint32_t* redo, const WrapBufs& wb,
+                           cudaStream_t stream) {
   const bool kda = a.gate_mode == LIN_GATE_PER_KEY;
   const bool bf = pool.state_dtype == LIN_BF16;
   const bool v64 = pool.head_v == 64;
@@ -1864,40 +2165,45 @@ cudaError_t launch_chunked(const lin_state_pool_t& pool, const lin_prefill_args_
     if (!redo) return cudaErrorInvalidValue;
     if ((e = cudaMemsetAsync(redo, 0, redo_workspace(pool, a), stream)) != cudaSuccess) return e;
     if (v64)
-      e = bf ? launch_t<true, LIN_BF16, 64>(pool, a, order, sp, seg_buf, redo, stream)
-             : launch_t<true, LIN_F32, 64>(pool, a, order, sp, seg_buf, redo, stream);
+      e = bf ? launch_t<true, LIN_BF16, 64>(pool, a, order, sp, seg_buf, redo, wb, stream)
+             : launch_t<true, LIN_F32, 64>(pool, a, order, sp, seg_buf, redo, wb, stream);
     else
-      e = bf ? launch_t<true, LIN_BF16, DH>(pool, a, order, sp, seg_buf, redo, stream)
-             : launch_t<true, LIN_F32, DH>(pool, a, order, sp, seg_buf, redo, stream);
+      e = bf ? launch_t<true, LIN_BF16, DH>(pool, a, order, sp, seg_buf, redo, wb, stream)
+             : launch_t<true, LIN_F32, DH>(pool, a, order, sp, seg_buf, redo, wb, stream);
     if (e != cudaSuccess) return e;
     return launch_prefill_recurrent(pool, a, stream, redo);
   }
   if (v64)
-    return bf ? launch_t<false, LIN_BF16, 64>(pool, a, order, sp, seg_buf, nullptr, stream)
-              : launch_t<false, LIN_F32, 64>(pool, a, order, sp, seg_buf, nullptr, stream);
-  return bf ? launch_t<false, LIN_BF16, DH>(pool, a, order, sp, seg_buf, nullptr, stream)
-            : launch_t<false, LIN_F32, DH>(pool, a, order, sp, seg_buf, nullptr, stream);
+    return bf ? launch_t<false, LIN_BF16, 64>(pool, a, order, sp, seg_buf, nullptr, wb, stream)
+              : launch_t<false, LIN_F32, 64>(pool, a, order, sp, seg_buf, nullptr, wb, stream);
+  return bf ? launch_t<false, LIN_BF16, DH>(pool, a, order, sp, seg_buf, nullptr, wb, stream)
+            : launch_t<false, LIN_F32, DH>(pool, a, order, sp, seg_buf, nullptr, wb, stream);
 }
 }  // namespace
 
 // Workspace: the batch order (varlen batches), the per-segment states of a
 // long single request run in segments, and the KDA rerun flags.
 size_t chunked_prefill_workspace(const lin_state_pool_t& pool, const lin_prefill_args_t& a) {
-  return order_workspace(a) + segment_workspace(pool, segment_plan(pool, a)) + redo_workspace(pool, a);
+  const SegPlan sp = segment_plan(pool, a);
+  return order_workspace(a) + segment_workspace(pool, sp) + redo_workspace(pool, a) +
+         wrap_workspace(wrap_plan(pool, a, sp));
 }
 
 cudaError_t launch_prefill_chunked(const lin_state_pool_t& pool, const lin_prefill_args_t& a,
                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   const size_t ow = order_workspace(a), rw = redo_workspace(pool, a);
   SegPlan sp = segment_plan(pool, a);
-  size_t sw = segment_workspace(pool, sp);
-  if (ow + sw + rw > 0 && (!workspace || workspace_bytes < ow + sw + rw)) return cudaErrorInvalidValue;
+  const size_t sw = segment_workspace(pool, sp);
+  const WrapPlan wp = wrap_plan(pool, a, sp);
+  const size_t ww = wrap_workspace(wp);
+  if (ow + sw + rw + ww > 0 && (!workspace || workspace_bytes < ow + sw + rw + ww)) return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(workspace);
   int32_t* order = ow > 0 ? reinterpret_cast<int32_t*>(ws) : nullptr;
   float* seg_buf = sw > 0 ? reinterpret_cast<float*>(ws + ow) : nullptr;
   uint32_t* redo = rw > 0 ? reinterpret_cast<uint32_t*>(ws + ow + sw) : nullptr;
+  const WrapBufs wb = carve_wrap(wp, ww > 0 ? ws + ow + sw + rw : nullptr);
   if (!seg_buf) sp = SegPlan{};
-  return launch_chunked(pool, a, order, sp, seg_buf, redo, stream);
+  return launch_chunked(pool, a, order, sp, seg_buf, redo, wb, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1991,7 +2297,8 @@ cudaError_t launch_prefill_noalloc(const lin_state_pool_t& pool, const lin_prefi
   }
   // a single long request runs in one piece: the segmented mode needs
   // per-segment state scratch that grows with the request
-  return launch_chunked(pool, a, sorted ? order : nullptr, SegPlan{}, nullptr, kda ? redo : nullptr, stream);
+  return launch_chunked(pool, a, sorted ? order : nullptr, SegPlan{}, nullptr, kda ? redo : nullptr, WrapBufs{},
+                        stream);
 }
 
 }  // namespace lin
