@@ -200,17 +200,25 @@ class PrefillWorkload(Workload):
         self.kernel_kind = L.lin_state_prefill_kernel(self.pool, **self.kw)
         self.kernel = "prefill_chunked" if self.kernel_kind == L.LIN_KERNEL_CHUNKED else "prefill_recurrent"
         # launches per call: the chunked kernel, plus the longest-first order of
-        # a varlen batch; a request in segments takes the offset / transition
-        # launch, the scan (more than two segments) and the final launch
-        # per-key gates add the token-by-token rerun launch behind the chunked
-        # one (its CTAs return at once unless their pair left the chunk's
-        # factored decay range) and the rerun flags in the workspace
+        # a varlen batch; a batch with more (request, head) chains than SMs takes
+        # the wrap-around plan instead of the order (its buffers are the
+        # workspace beyond what the one-piece schedule asks for); a request in
+        # segments takes the offset / transition launch, the scan (more than
+        # two segments) and the final launch; per-key gates add the
+        # token-by-token rerun launch behind the chunked one (its CTAs return at
+        # once unless their pair left the chunk's factored decay range) and the
+        # rerun flags in the workspace
         if self.kernel_kind == L.LIN_KERNEL_CHUNKED:
             kda = gate_mode == W.GATE_PER_KEY
+            kw1 = dict(self.kw, flags=self.kw["flags"] | L.LIN_PREFILL_ONE_PIECE)
+            need1 = L.lin_state_prefill_workspace(self.pool, **kw1)
+            self.wrap = need > need1
             ow = (B * 4 + 255) // 256 * 256 if 1 < B <= 4096 else 0
             rw = ((B * dims.num_heads + 31) // 32 * 4 + 255) // 256 * 256 if kda else 0
-            seg_bytes = need - ow - rw
-            if seg_bytes > 0:
+            seg_bytes = need1 - ow - rw
+            if self.wrap:
+                self.launches_per_step = 2
+            elif seg_bytes > 0:
                 nseg = seg_bytes // (2 * dims.num_heads * dims.head_k * dims.head_k * 4)
                 self.launches_per_step = (1 if ow else 0) + 2 + (1 if nseg > 2 else 0)
             else:

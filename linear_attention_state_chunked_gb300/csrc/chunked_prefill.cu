@@ -228,22 +228,66 @@ __global__ void __launch_bounds__(1024) order_kernel(const int32_t* __restrict__
   for (int i = threadIdx.x; i < batch; i += blockDim.x) order[i] = static_cast<int32_t>(key[i] & 0xffffffffu);
 }
 
+// Exclusive prefix sum of v over a 1024-thread block, and the block's total
+// (warp shuffles, then one warp over the 32 warp sums).
+__device__ __forceinline__ int64_t block_exclusive_sum(int64_t v, int64_t* sums, int64_t& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int64_t z = sums[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, z, d);
+      if (lane >= d) z += y;
+    }
+    sums[lane] = z;
+  }
+  __syncthreads();
+  total = sums[31];
+  const int64_t r = (w > 0 ? sums[w - 1] : 0) + x - v;
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ int64_t block_max(int64_t v, int64_t* sums) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    const int64_t y = __shfl_xor_sync(0xffffffffu, v, d);
+    v = y > v ? y : v;
+  }
+  if ((threadIdx.x & 31) == 0) sums[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int64_t m = sums[0];
+  for (int i = 1; i < 32; ++i) m = sums[i] > m ? sums[i] : m;
+  __syncthreads();
+  return m;
+}
+
 // The wrap-around plan of a batch (one CTA): the chunk units n_r of every
 // request (0 for an empty request and for one the prefill kernel skips or
 // rejects: a negative slot, a slot past the pool, bad cu_seqlens or
 // prefix_len, the kernel's own checks), T = max(longest chain,
-// ceil(H sum n_r / grid)), the pieces with their planned start times, sorted
-// by start time (bitonic), and cleared hand-on flags and piece counter.
+// ceil(H sum n_r / grid)), the pieces with their planned start times, ordered
+// by start time (a counting sort over the T start times, or a bitonic sort of
+// (start, piece) keys when T is large), and cleared hand-on flags and counter.
 constexpr int kWrapMaxPieces = 8192;
 constexpr size_t kWrapPlanSmem = kWrapMaxPieces * sizeof(uint64_t) + kOrderMax * (sizeof(int64_t) + sizeof(int32_t));
 
 __global__ void __launch_bounds__(1024) wrap_plan_kernel(const lin_prefill_args_t a, int H, int num_slots, int grid,
                                                          int32_t* ctl, WrapPiece* piece, int32_t* order,
                                                          uint32_t* flag) {
-  extern __shared__ uint64_t wkey[];                                       // [kWrapMaxPieces]
-  int64_t* first = reinterpret_cast<int64_t*>(wkey + kWrapMaxPieces);     // [batch] first unit of r
-  int32_t* units = reinterpret_cast<int32_t*>(first + kOrderMax);         // [batch] n_r
-  __shared__ int64_t part[1024], pmax[1024];
+  extern __shared__ uint64_t wkey[];                                    // [kWrapMaxPieces] sort keys, or
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wkey);                  //   [kWrapMaxPieces] start counts
+  int32_t* pstart = reinterpret_cast<int32_t*>(hist + kWrapMaxPieces);  //   and [kWrapMaxPieces] starts
+  int64_t* first = reinterpret_cast<int64_t*>(wkey + kWrapMaxPieces);  // [batch] first unit of r
+  int32_t* units = reinterpret_cast<int32_t*>(first + kOrderMax);      // [batch] n_r
+  __shared__ int64_t sums[32];
   __shared__ int count;
   const int t = threadIdx.x, B = a.batch;
   const int per = (B + 1023) / 1024;  // requests t * per .. of this thread
@@ -260,36 +304,34 @@ __global__ void __launch_bounds__(1024) wrap_plan_kernel(const lin_prefill_args_
     sum += n;
     mx = n > mx ? n : mx;
   }
-  part[t] = sum;
-  pmax[t] = mx;
   if (t == 0) count = 0;
-  __syncthreads();
-  for (int d = 1; d < 1024; d <<= 1) {  // inclusive prefix sums and maxima
-    const int64_t v = t >= d ? part[t - d] : 0, w = t >= d ? pmax[t - d] : 0;
-    __syncthreads();
-    part[t] += v;
-    if (w > pmax[t]) pmax[t] = w;
-    __syncthreads();
+  int64_t all = 0;
+  int64_t run = block_exclusive_sum(sum, sums, all);
+  const int64_t maxn = block_max(mx, sums);
+  for (int i = 0; i < per; ++i) {
+    const int r = t * per + i;
+    if (r >= B) break;
+    first[r] = run * H;
+    run += units[r];
   }
-  {
-    int64_t run = t > 0 ? part[t - 1] : 0;
-    for (int i = 0; i < per; ++i) {
-      const int r = t * per + i;
-      if (r >= B) break;
-      first[r] = run * H;
-      run += units[r];
-    }
-  }
-  const int64_t total = part[1023] * H;
+  const int64_t total = all * H;
   int64_t T = (total + grid - 1) / grid;
-  if (T < pmax[1023]) T = pmax[1023];
+  if (T < maxn) T = maxn;
   if (T < 1) T = 1;
+  const bool counting = T <= kWrapMaxPieces;
+  if (counting)
+    for (int i = t; i < T; i += 1024) hist[i] = 0u;
   __syncthreads();
   auto emit = [&](int r, int h, int c0, int c1, int mode, int link, int64_t start) {
     const int k = atomicAdd(&count, 1);
     piece[k] = WrapPiece{r, h, c0, c1, mode, link, 0, 0};
-    const uint64_t st = start < 0x7fffffff ? static_cast<uint64_t>(start) : 0x7fffffffull;
-    wkey[k] = (st << 32) | static_cast<uint32_t>(k);
+    if (counting) {
+      pstart[k] = static_cast<int32_t>(start);
+      atomicAdd(hist + start, 1u);
+    } else {
+      const uint64_t st = start < 0x7fffffff ? static_cast<uint64_t>(start) : 0x7fffffffull;
+      wkey[k] = (st << 32) | static_cast<uint32_t>(k);
+    }
   };
   for (int c = t; c < B * H; c += 1024) {
     const int r = c / H, h = c % H;
@@ -310,26 +352,48 @@ __global__ void __launch_bounds__(1024) wrap_plan_kernel(const lin_prefill_args_
   }
   __syncthreads();
   const int N = count;
-  int n2 = 2;
-  while (n2 < N) n2 <<= 1;
-  for (int i = N + t; i < n2; i += 1024) wkey[i] = ~0ull;
-  __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = t; i < n2; i += 1024) {
-        const int ix = i ^ jj;
-        if (ix > i) {
-          const uint64_t x = wkey[i], y = wkey[ix];
-          if ((x > y) == ((i & k) == 0)) {
-            wkey[i] = y;
-            wkey[ix] = x;
+  if (counting) {
+    // bucket offsets: thread t sums the counts of buckets t * bpt .. (bpt each)
+    const int bpt = static_cast<int>((T + 1023) / 1024);
+    uint32_t local = 0;
+    for (int i = 0; i < bpt; ++i) {
+      const int64_t q = int64_t(t) * bpt + i;
+      if (q < T) local += hist[q];
+    }
+    int64_t dummy = 0;
+    uint32_t off = static_cast<uint32_t>(block_exclusive_sum(local, sums, dummy));
+    for (int i = 0; i < bpt; ++i) {
+      const int64_t q = int64_t(t) * bpt + i;
+      if (q < T) {
+        const uint32_t c = hist[q];
+        hist[q] = off;
+        off += c;
+      }
+    }
+    __syncthreads();
+    for (int k = t; k < N; k += 1024) order[atomicAdd(hist + pstart[k], 1u)] = k;
+  } else {
+    int n2 = 2;
+    while (n2 < N) n2 <<= 1;
+    for (int i = N + t; i < n2; i += 1024) wkey[i] = ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1) {
+      for (int jj = k >> 1; jj > 0; jj >>= 1) {
+        for (int i = t; i < n2; i += 1024) {
+          const int ix = i ^ jj;
+          if (ix > i) {
+            const uint64_t x = wkey[i], y = wkey[ix];
+            if ((x > y) == ((i & k) == 0)) {
+              wkey[i] = y;
+              wkey[ix] = x;
+            }
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
+    for (int i = t; i < N; i += 1024) order[i] = static_cast<int32_t>(wkey[i] & 0xffffffffu);
   }
-  for (int i = t; i < N; i += 1024) order[i] = static_cast<int32_t>(wkey[i] & 0xffffffffu);
   for (int i = t; i < grid; i += 1024) flag[i] = 0u;
   if (t == 0) {
     ctl[0] = N;
