@@ -168,7 +168,19 @@ typedef struct {
  * segment then runs in parallel from its true initial state; with a cycled
  * track list only the snapshots that remain at the end in token order (the
  * request's last n_r) are written, so the slots end up as in one piece. The workspace
- * then holds 2 fp32 states per (segment, head). Less workspace than the
+ * then holds 2 fp32 states per (segment, head).
+ * Batches with more (request, head) pairs than SMs (up to 4096 requests and
+ * 8192 pairs plus SMs): with the chunked kernel, the pairs' chunk chains are
+ * laid end to end and cut into one range of equal chunk units per SM
+ * (McNaughton's wrap-around rule), so the SMs finish together instead of in
+ * rounds of whole requests. A chain crossing a range boundary runs as two
+ * pieces: the first hands its fp32 state (through the workspace) to the
+ * second, which waits for it (bounded: LIN_ST_TIMEOUT after about 4 s). A
+ * one-CTA plan kernel orders the pieces by planned start and the CTAs take
+ * them from a counter, so a wait is always for a piece already running; no
+ * co-residency is assumed. The results equal the one-piece schedule's bit for
+ * bit; LIN_PREFILL_ONE_PIECE selects that schedule. The workspace then holds
+ * the plan and one fp32 state per SM (about 10 MB on 152 SMs). Less workspace than the
  * query reports is an error (LIN_EWORKSPACE); lin_state_prefill_noalloc runs
  * the request in one piece. The workspace also holds the longest-first order
  * of a varlen batch and, for per-key gates, one rerun bit per (request, head). */
@@ -219,7 +231,8 @@ LIN_API int lin_state_prefill(const lin_state_pool_t* pool, const lin_prefill_ar
  * within rounding (a batch equal bit for bit), except that a batch of one long
  * request runs in one piece, not in segments: the same values within the
  * fp32 / bf16 tolerances, but on only `heads` CTAs, so much slower than
- * lin_state_prefill for such a request. Its scratch (the longest-first order
+ * lin_state_prefill for such a request; likewise every (request, head) runs
+ * in one piece, not under the wrap-around schedule. Its scratch (the longest-first order
  * of a batch, the per-key rerun bits) is fixed arrays in the library's device
  * memory (48 KB), held by every GPU that loads the library until the process
  * exits:
