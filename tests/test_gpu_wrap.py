@@ -96,3 +96,42 @@ def test_wrap_pieces_equal_one_piece_and_oracle(case):
     compare_slots(pools[1], op, [1, 2, 3, 4] + tracks, tol)
     # the skipped request's outputs stay as they were
     assert torch.all(out2[cu[3]:cu[4]] == -7.0)
+
+
+def test_wrap_two_calls_at_once_on_two_streams():
+    """Two wrap-around calls in flight together on two streams (separate pools
+    and workspaces), so their pieces compete for the SMs. A tail piece only
+    ever waits for a head piece that a running CTA has taken, and head pieces
+    wait for nothing, so both calls finish, with the one-piece results."""
+    lengths = [700, 0, 130, 1000, 333]
+    dims = W.LayerDims(num_heads=H, head_k=128, head_v=128)
+    b = W.make_prefill_batch(dims, lengths, W.GATE_PER_HEAD, dtype=torch.bfloat16, seed=31, gate="uniform",
+                             prefixes=[0, 64, 128, 0, 64], warm=[0, 1, 1, 0, 1], tag="wrap.streams")
+    slots, tracks, cu_track = [1, 2, 3, 4, 5], list(range(6, 16)), [0, 2, 4, 6, 8, 10]
+    pools = []
+    for _ in range(3):
+        p = L.StatePool(1, 16, H, 128, state_dtype=torch.float32, conv_dtype=torch.bfloat16, device=DEV)
+        fill_pool(p, 32)
+        pools.append(p)
+    ref, _ = _run(pools[0], b, slots, tracks, cu_track, FLAGS | L.LIN_PREFILL_ONE_PIECE)
+    args = []
+    for pool in pools[1:]:
+        out = torch.full((b.total_tokens, H, 128), -7.0, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        kw = dict(layer=0, x=b.x.to(DEV), conv_w=b.conv_w.to(DEV), g=b.g.to(DEV), beta=b.beta.to(DEV),
+                  out=out, cu_seqlens=b.cu_seqlens.to(DEV), prefix_len=b.prefix_len.to(DEV),
+                  slot=_i32(slots), has_initial_state=b.has_initial_state.to(DEV),
+                  track_slots=_i32(tracks), cu_track=_i32(cu_track), track_stride=64,
+                  gate_mode=b.gate_mode, flags=FLAGS, status=st)
+        ws = torch.empty(L.lin_state_prefill_workspace(pool, **kw), dtype=torch.uint8, device=DEV)
+        args.append((pool, kw, ws, out, st))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for (pool, kw, ws, out, st), s in zip(args, streams):
+        L.lin_state_prefill(pool, workspace=ws, stream=s, **kw)
+    torch.cuda.synchronize()
+    for pool, kw, ws, out, st in args:
+        assert L.lin_state_read_status(st) == 0
+        assert torch.equal(out, ref)
+        assert torch.equal(pool.temporal, pools[0].temporal)
+        assert torch.equal(pool.conv, pools[0].conv)
