@@ -192,3 +192,16 @@ def test_decode_rejects_drafts_past_the_staging_limit():
 def test_strerror_and_version():
     assert L.lib.lin_state_strerror(L.LIN_EINVAL) == b"invalid argument"
     assert L.lin_state_version() >> 16 == 1
+
+
+def test_binding_constants_match_header():
+    """Every flag, status bit and dtype / gate code the binding exports has the
+    header's value (the flags of the enum, the LIN_ST_* and LIN_KERNEL_* defines)."""
+    src = "".join(open(h).read() for h in HEADERS)
+    values = {n: int(v) for n, v in re.findall(r"\b(LIN_[A-Z0-9_]+)\s*=\s*(\d+)u?\b", src)}
+    values.update({n: int(v) for n, v in re.findall(r"#define\s+(LIN_(?:ST|KERNEL)_[A-Z0-9_]+)\s+(\d+)", src)})
+    assert "LIN_PREFILL_ONE_PIECE" in values and "LIN_ST_TIMEOUT" in values
+    exported = {n: getattr(L, n) for n in values if hasattr(L, n)}
+    assert len(exported) >= 15
+    assert all(exported[n] == values[n] for n in exported), {n: (exported[n], values[n]) for n in exported
+                                                              if exported[n] != values[n]}
